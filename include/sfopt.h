@@ -1,0 +1,271 @@
+/*
+ * sfopt.h -- C ABI of the GB300 (sm_103a) per-layer gradient-to-update step.
+ *
+ * Two modes of the same step, plus the engine that slides layers through
+ * device memory:
+ *
+ *  (a) fused AdamW: bf16 gradient -> fp32 master weights and Adam moments
+ *      -> bf16 weights, for all tensors of one layer in one launch.
+ *      Follows "An Efficient Heterogeneous Co-Design for Fine-Tuning on a
+ *      Single GPU" (SlideFormer), technical summary section 2.A (the layer
+ *      update that the sliding engine overlaps with the next layer's
+ *      compute) and 2.B (flattened fp32 optimizer states; fp32 -> bf16 type
+ *      conversion).  The update is Adam with bias correction (Kingma & Ba
+ *      2015, Algorithm 1) and decoupled weight decay (Loshchilov & Hutter
+ *      2019, Algorithm 2).
+ *
+ *  (b) learned sparse projectors: S = P^T G Q, AdamW on S in the d x d
+ *      compressed space, W -= P dS Q^T.  Follows "Practical offloading for
+ *      fine-tuning LLM on commodity GPU via learned sparse projectors"
+ *      (LSP-Offload), abstract and method section ("sparse projectors",
+ *      "compress, compute in compressed space, decompress").
+ *
+ *  (c) the layer-sliding window: layers live in pinned host memory and are
+ *      streamed through a fixed set of pre-allocated device slots on side
+ *      streams while the update kernels run (SlideFormer, section 2.A
+ *      "sliding window", "overlap of compute, transfer and update";
+ *      section 2.B "pre-allocated GPU cache queue").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Ownership: the caller owns every tensor buffer (device memory and
+ *    pinned host memory) and every stream.  The library owns only the
+ *    opaque handles it returns (projector index structures, window
+ *    events), released by the matching *_destroy call.
+ *  - Streams are passed as `void*` holding a cudaStream_t (NULL = the
+ *    legacy default stream).  Every compute call is stream-ordered and
+ *    asynchronous: it returns once its kernels are enqueued.
+ *  - Errors: every call returns an sf_status.  Argument errors are found on
+ *    the host before anything is enqueued (nothing is modified).  Launch
+ *    errors return SF_ERR_CUDA; errors raised while kernels run surface at
+ *    the next call that checks, or at sf_sync_status().  sf_last_error()
+ *    gives a message for the calling thread's last failure.  No C++
+ *    exception crosses this boundary.
+ *  - Layouts are dense and row-major; element counts are int64.
+ *  - Floating-point results are deterministic: the same inputs give the
+ *    same bits on every run (no atomics in any reduction).
+ */
+#ifndef SFOPT_H
+#define SFOPT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SF_OK = 0,
+  SF_ERR_INVALID = -1,     /* null pointer, bad size, step < 1, bad index... */
+  SF_ERR_CUDA = -2,        /* a CUDA launch or runtime error                 */
+  SF_ERR_OOM = -3,         /* the library could not allocate its handle      */
+  SF_ERR_UNSUPPORTED = -4, /* a size or dtype outside what a kernel supports */
+  SF_ERR_TIMEOUT = -5      /* a bounded host wait ran out                    */
+} sf_status;
+
+typedef enum { SF_BF16 = 0, SF_FP32 = 1 } sf_dtype;
+
+/* AdamW hyper-parameters.  Given in double; the library derives the fp32
+ * constants the kernels use (1-beta1, 1-beta2, 1-lr*wd, lr/(1-beta1^t),
+ * sqrt(1-beta2^t)) in double and rounds each once. */
+typedef struct {
+  double lr;
+  double beta1;
+  double beta2;
+  double eps;
+  double weight_decay;
+} sf_adamw_hparams;
+
+/* One parameter tensor of a layer, flattened to `numel` elements.
+ *   grad       : bf16 [numel], read
+ *   master     : fp32 [numel], read + written (master weights theta)
+ *   exp_avg    : fp32 [numel], read + written (first moment m)
+ *   exp_avg_sq : fp32 [numel], read + written (second moment v)
+ *   weight     : bf16 [numel], written (RNE of the new master); may be NULL
+ * Pointers are device pointers for sf_adamw_layer_step and the device slots
+ * of a window, pinned host pointers for the host layers of a window.  The
+ * arrays must not overlap.  Any alignment is accepted; 16-byte aligned
+ * arrays take the 128-bit path. */
+typedef struct {
+  const void* grad;
+  float* master;
+  float* exp_avg;
+  float* exp_avg_sq;
+  void* weight;
+  int64_t numel;
+} sf_tensor;
+
+/* ------------------------------------------------------------------------
+ * (a) Fused multi-tensor AdamW over one layer.
+ *
+ * Applies, per element, with t = `step` (>= 1):
+ *   theta <- theta * (1 - lr*wd)
+ *   m     <- beta1*m + (1-beta1)*g
+ *   v     <- beta2*v + (1-beta2)*g^2
+ *   theta <- theta - (lr/(1-beta1^t)) * m / (sqrt(v)/sqrt(1-beta2^t) + eps)
+ *   weight = RNE_bf16(theta)
+ * over all `n_tensors` tensors of the layer, in one kernel launch per
+ * SF_MAX_TENSORS_PER_LAUNCH tensors.  Empty tensors (numel 0) are allowed.
+ * Returns SF_ERR_INVALID for n_tensors < 0, a NULL array, a negative numel,
+ * step < 1, or non-finite hyper-parameters.
+ * ---------------------------------------------------------------------- */
+#define SF_MAX_TENSORS_PER_LAUNCH 48
+
+sf_status sf_adamw_layer_step(const sf_tensor* tensors, int n_tensors,
+                              const sf_adamw_hparams* hp, int64_t step,
+                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * (b) Learned sparse projectors.
+ *
+ * A projector is a rows x d sparse matrix with exactly k entries in every
+ * row, given as ELL: col_idx int32 [rows][k] (ids in [0, d)), val fp32
+ * [rows][k], both device arrays, read once.  lsp_projector_create builds on
+ * the device, in the stream, the library-owned index structures the kernels
+ * use: the column lists of the transpose (CSC; rows ascending inside every
+ * column, built by a stable counting sort), and the column order grouped by
+ * list length (bucket 0 = empty column, else ceil(log2 nnz)+1; ascending
+ * id inside a bucket).  The ELL arrays may be freed after the call returns
+ * and the stream has passed it.
+ *
+ * `validate` != 0 checks on the device that every id is in [0, d) and that
+ * no row repeats an id; a failed check makes the call return
+ * SF_ERR_INVALID (the call then synchronises the stream).  With validate = 0
+ * out-of-range ids are undefined behaviour and repeated ids add up.
+ * Limits: 1 <= d <= 1024, 1 <= k <= 64, rows * k < 2^31.
+ * ---------------------------------------------------------------------- */
+typedef struct lsp_projector_s* lsp_projector;
+
+sf_status lsp_projector_create(int64_t rows, int32_t d, int32_t k,
+                               const int32_t* d_col_idx, const float* d_val,
+                               int validate, void* stream, lsp_projector* out);
+
+/* Copy the CSC and the bucket order out (device buffers, caller-owned):
+ * col_ptr int32 [d+1], row_idx int32 [rows*k], val fp32 [rows*k],
+ * bucket_perm int32 [d].  Any pointer may be NULL to skip that array. */
+sf_status lsp_projector_export_csc(lsp_projector p, int32_t* col_ptr,
+                                   int32_t* row_idx, float* val,
+                                   int32_t* bucket_perm, void* stream);
+
+/* Shape queries (return -1 for a NULL handle). */
+int64_t lsp_projector_rows(lsp_projector p);
+int32_t lsp_projector_dim(lsp_projector p);
+int32_t lsp_projector_nnz_per_row(lsp_projector p);
+
+/* Frees the handle.  The caller must make sure no enqueued work still uses
+ * it (for example by synchronising its streams first). */
+sf_status lsp_projector_destroy(lsp_projector p);
+
+/* Bytes of device workspace that lsp_compress / lsp_decompress_apply need
+ * for an m x n gradient and dimension d (the d x n or n x d intermediate). */
+size_t lsp_workspace_bytes(int64_t m, int64_t n, int32_t d);
+
+/* S = P^T G Q.
+ *   P : projector with rows = m;  Q : projector with rows = n; same d.
+ *   G : device, [m][n], dtype g_dtype (SF_BF16 or SF_FP32), row-major.
+ *   S : device fp32 [d][d], written (S[a][c], a = column of P, c = column of Q).
+ *   ws: device scratch of ws_bytes >= lsp_workspace_bytes(m, n, d).
+ * fp32 accumulation; no atomics.  m, n >= 1. */
+sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G,
+                       sf_dtype g_dtype, int64_t m, int64_t n, float* S,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* AdamW in the compressed space, no weight decay, step t = `step` >= 1:
+ *   m  <- beta1*m + (1-beta1)*S;  v <- beta2*v + (1-beta2)*S^2
+ *   dS  = (lr/(1-beta1^t)) * m / (sqrt(v)/sqrt(1-beta2^t) + eps)
+ * S, m, v, dS: device fp32 [d2] (d2 = d*d; any element count works).
+ * hp->weight_decay is ignored. */
+sf_status lsp_adamw_compressed(const float* S, float* m, float* v, float* dS,
+                               int64_t d2, const sf_adamw_hparams* hp,
+                               int64_t step, void* stream);
+
+/* W <- W - P dS Q^T.
+ *   dS : device fp32 [d][d] (same layout as S).
+ *   W  : device [m][n], dtype w_dtype: SF_FP32 (an fp32 master: W - D in
+ *        fp32) or SF_BF16 (bf16 weights: RNE(float(W) - D)).
+ *   w_bf16_mirror: NULL, or device bf16 [m][n] that receives RNE of the new
+ *        fp32 W (only with w_dtype = SF_FP32).
+ *   ws : device scratch, as for lsp_compress.
+ * No weight decay is applied here. */
+sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS,
+                               void* W, sf_dtype w_dtype, void* w_bf16_mirror,
+                               int64_t m, int64_t n, void* ws, size_t ws_bytes,
+                               void* stream);
+
+/* ------------------------------------------------------------------------
+ * (c) Layer-sliding window.
+ *
+ * A window owns n_slots (>= 1) caller-allocated device slots.  Each slot is
+ * an array of sf_tensor holding device buffers big enough for the largest
+ * layer that will pass through it (tensor i of a slot must have numel >=
+ * tensor i of every layer).  The window creates its own CUDA events; it
+ * uses the three caller streams: h2d (host -> device copies), compute (the
+ * AdamW kernel), d2h (device -> host copies).
+ *
+ * sf_slide_window_step enqueues, for every entry l = order[v] in turn
+ * (v = 0..n_order-1), with slot s = v mod n_slots:
+ *   h2d:     wait until slot s is free and layer l's previous write-back
+ *            has landed; copy grad, master, exp_avg, exp_avg_sq of layer l
+ *            (pinned host) into slot s;
+ *   compute: wait for the copies; run sf_adamw_layer_step on slot s with
+ *            step = ++steps[l];
+ *   d2h:     wait for the update; copy master, exp_avg, exp_avg_sq and
+ *            weight (if the host layer has one) back to layer l; the slot is
+ *            free again when these copies end.
+ * Host-layer pointers must be pinned (page-locked) host memory.  The call
+ * returns when everything is enqueued; `steps` (int64 [n_layers], host) is
+ * updated on return.  Host buffers of a layer must not be touched until its
+ * copies have ended (sf_window_sync).
+ * ---------------------------------------------------------------------- */
+typedef struct sf_window_s* sf_window;
+
+typedef struct {
+  const sf_tensor* tensors; /* pinned host pointers */
+  int n_tensors;
+} sf_host_layer;
+
+sf_status sf_window_create(int n_slots, const sf_tensor* const* device_slots,
+                           int n_tensors_per_slot, void* h2d_stream,
+                           void* compute_stream, void* d2h_stream,
+                           sf_window* out);
+
+sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers,
+                               int n_layers, const int32_t* order, int n_order,
+                               const sf_adamw_hparams* hp, int64_t* steps);
+
+/* Waits, with a bound, until all work the window enqueued has ended.
+ * timeout_ms <= 0 uses the default bound (SF_TIMEOUT_MS environment
+ * variable, else 600000 ms).  Returns SF_ERR_TIMEOUT when the bound runs
+ * out (the work is still in flight; the window stays usable). */
+sf_status sf_window_sync(sf_window w, int64_t timeout_ms);
+
+/* Frees the window's events.  Waits (bounded) for its work first. */
+sf_status sf_window_destroy(sf_window w);
+
+/* ------------------------------------------------------------------------
+ * Utilities.
+ * ---------------------------------------------------------------------- */
+
+/* Waits, with the default bound, for `stream` and returns SF_OK or the
+ * sticky error of the CUDA context (SF_ERR_CUDA), or SF_ERR_TIMEOUT. */
+sf_status sf_sync_status(void* stream);
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char* sf_last_error(void);
+
+/* Library version, e.g. "0.1.0". */
+const char* sf_version(void);
+
+/* Test hook for failure handling: the n-th host->device or device->host
+ * copy that a window enqueues after this call fails once on the host, before
+ * anything is handed to CUDA, and the window call returns SF_ERR_CUDA with
+ * the message "injected copy failure".  n = 0 switches the hook off.  Not
+ * thread-safe; meant for tests only. */
+void sf_test_fail_copy_after(int64_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFOPT_H */

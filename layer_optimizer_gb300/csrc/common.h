@@ -1,0 +1,72 @@
+// Internal helpers shared by the library's translation units: status and
+// error-message plumbing, argument checks, small integer utilities.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "sfopt.h"
+
+namespace sf {
+
+// Records a message for sf_last_error() (thread-local) and returns `st`.
+sf_status fail(sf_status st, const char* fmt, ...);
+
+// Clears the calling thread's last error message.
+void clear_error();
+
+// Maps a CUDA error to SF_ERR_CUDA with a message naming `what`.
+sf_status cuda_fail(cudaError_t e, const char* what);
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+template <typename T>
+constexpr T ceil_div(T a, T b) { return (a + b - 1) / b; }
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Default bound for host waits, in milliseconds (SF_TIMEOUT_MS or 600 s).
+int64_t default_timeout_ms();
+
+// Polls `ev` (or a stream when ev is null) until it completes or the bound
+// runs out.  Returns SF_OK, SF_ERR_TIMEOUT or SF_ERR_CUDA.
+sf_status bounded_wait_event(cudaEvent_t ev, int64_t timeout_ms, const char* what);
+sf_status bounded_wait_stream(cudaStream_t s, int64_t timeout_ms, const char* what);
+
+// Checks for a pending launch error after enqueueing kernels.
+inline sf_status check_launch(const char* what) {
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SF_OK : cuda_fail(e, what);
+}
+
+// fp32 constants of one AdamW step, derived in double and rounded once.
+struct AdamConsts {
+  float beta1, one_minus_beta1;
+  float beta2, one_minus_beta2;
+  float decay;          // 1 - lr * weight_decay
+  float step_size;      // lr / (1 - beta1^t)
+  float sqrt_bc2;       // sqrt(1 - beta2^t)
+  float eps;
+};
+
+sf_status make_adam_consts(const sf_adamw_hparams* hp, int64_t step, bool with_decay,
+                           AdamConsts* out);
+
+}  // namespace sf
+
+#define SF_TRY(expr)                      \
+  do {                                    \
+    sf_status _st = (expr);               \
+    if (_st != SF_OK) return _st;         \
+  } while (0)
+
+#define SF_CUDA_TRY(expr, what)                       \
+  do {                                                \
+    cudaError_t _e = (expr);                          \
+    if (_e != cudaSuccess) return sf::cuda_fail(_e, what); \
+  } while (0)

@@ -1,0 +1,241 @@
+// Layer-sliding window: streams layers between pinned host memory and a
+// fixed set of pre-allocated device slots on three CUDA streams, with the
+// fused AdamW update in between.
+//
+// SlideFormer ("An Efficient Heterogeneous Co-Design for Fine-Tuning on a
+// Single GPU", technical summary section 2.A) keeps only a small active
+// window of layers on the GPU and overlaps computation, host<->device
+// transfer and the optimizer update of neighbouring layers; section 2.B
+// pre-allocates a fixed queue of GPU cache units, each holding one layer,
+// so nothing is allocated while training runs.  This engine is that
+// window for the update step: a visit copies one layer into a free slot
+// (h2d stream), updates it (compute stream), and copies it back (d2h
+// stream).  Visits to different slots run concurrently, so the copy
+// engines in both directions and the HBM-bound kernel overlap.  It does no
+// arithmetic of its own; dependencies are CUDA events only, and the host
+// never blocks while enqueueing.
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "common.h"
+
+namespace sf {
+sf_status adamw_layer_step_impl(const sf_tensor* tensors, int n_tensors, const sf_adamw_hparams* hp,
+                                int64_t step, cudaStream_t stream);
+}
+
+struct sf_window_s {
+  int device = 0;
+  int n_slots = 0;
+  int n_tensors = 0;
+  std::vector<std::vector<sf_tensor>> slots;
+  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  std::vector<cudaEvent_t> ev_in, ev_done, ev_free;
+  std::vector<bool> slot_used;
+  std::vector<cudaEvent_t> ev_layer;   // write-back of a host layer has landed
+  std::vector<bool> layer_pending;
+  int64_t visits = 0;                  // running visit counter (slot rotation)
+};
+
+namespace {
+
+// Test hook: the n-th copy enqueue (1-based) fails once; 0 = off.
+int64_t g_fail_copy_at = 0;
+int64_t g_copy_count = 0;
+
+sf_status copy_async(void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, cudaStream_t s,
+                     const char* what) {
+  if (bytes == 0) return SF_OK;
+  ++g_copy_count;
+  if (g_fail_copy_at > 0 && g_copy_count == g_fail_copy_at) {
+    g_fail_copy_at = 0;
+    return sf::fail(SF_ERR_CUDA, "%s: injected copy failure", what);
+  }
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, kind, s);
+  return e == cudaSuccess ? SF_OK : sf::cuda_fail(e, what);
+}
+
+void destroy_events(sf_window_s* w) {
+  for (auto* v : {&w->ev_in, &w->ev_done, &w->ev_free, &w->ev_layer})
+    for (cudaEvent_t e : *v)
+      if (e) cudaEventDestroy(e);
+}
+
+sf_status new_event(cudaEvent_t* e) {
+  cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+  return r == cudaSuccess ? SF_OK : sf::cuda_fail(r, "cudaEventCreate");
+}
+
+sf_status check_layer(const sf_window_s* w, const sf_host_layer& L, int li) {
+  if (L.n_tensors < 0 || L.n_tensors > w->n_tensors)
+    return sf::fail(SF_ERR_INVALID, "layer %d: %d tensors, window slots hold %d", li, L.n_tensors,
+                    w->n_tensors);
+  if (L.n_tensors > 0 && !L.tensors) return sf::fail(SF_ERR_INVALID, "layer %d: tensors is NULL", li);
+  for (int t = 0; t < L.n_tensors; ++t) {
+    const sf_tensor& h = L.tensors[t];
+    if (h.numel < 0) return sf::fail(SF_ERR_INVALID, "layer %d tensor %d: numel < 0", li, t);
+    if (h.numel == 0) continue;
+    if (!h.grad || !h.master || !h.exp_avg || !h.exp_avg_sq)
+      return sf::fail(SF_ERR_INVALID, "layer %d tensor %d: NULL host array", li, t);
+    for (const auto& slot : w->slots) {
+      const sf_tensor& d = slot[t];
+      if (h.numel > d.numel)
+        return sf::fail(SF_ERR_INVALID, "layer %d tensor %d: numel %lld exceeds slot capacity %lld",
+                        li, t, (long long)h.numel, (long long)d.numel);
+      if (h.weight && !d.weight)
+        return sf::fail(SF_ERR_INVALID, "layer %d tensor %d: slot has no weight buffer", li, t);
+    }
+  }
+  return SF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sf_status sf_window_create(int n_slots, const sf_tensor* const* device_slots, int n_tensors_per_slot,
+                           void* h2d_stream, void* compute_stream, void* d2h_stream,
+                           sf_window* out) {
+  sf::clear_error();
+  if (!out) return sf::fail(SF_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  if (n_slots < 1) return sf::fail(SF_ERR_INVALID, "n_slots must be >= 1");
+  if (n_tensors_per_slot < 0) return sf::fail(SF_ERR_INVALID, "n_tensors_per_slot < 0");
+  if (!device_slots) return sf::fail(SF_ERR_INVALID, "device_slots is NULL");
+  sf_window_s* w = new (std::nothrow) sf_window_s;
+  if (!w) return sf::fail(SF_ERR_OOM, "window allocation failed");
+  cudaGetDevice(&w->device);
+  w->n_slots = n_slots;
+  w->n_tensors = n_tensors_per_slot;
+  w->h2d = sf::as_stream(h2d_stream);
+  w->comp = sf::as_stream(compute_stream);
+  w->d2h = sf::as_stream(d2h_stream);
+  for (int s = 0; s < n_slots; ++s) {
+    if (n_tensors_per_slot > 0 && !device_slots[s]) {
+      delete w;
+      return sf::fail(SF_ERR_INVALID, "slot %d is NULL", s);
+    }
+    w->slots.emplace_back(device_slots[s], device_slots[s] + n_tensors_per_slot);
+  }
+  w->ev_in.assign(n_slots, nullptr);
+  w->ev_done.assign(n_slots, nullptr);
+  w->ev_free.assign(n_slots, nullptr);
+  w->slot_used.assign(n_slots, false);
+  for (int s = 0; s < n_slots; ++s) {
+    sf_status st = SF_OK;
+    if ((st = new_event(&w->ev_in[s])) != SF_OK || (st = new_event(&w->ev_done[s])) != SF_OK ||
+        (st = new_event(&w->ev_free[s])) != SF_OK) {
+      destroy_events(w);
+      delete w;
+      return st;
+    }
+  }
+  *out = w;
+  return SF_OK;
+}
+
+sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_layers,
+                               const int32_t* order, int n_order, const sf_adamw_hparams* hp,
+                               int64_t* steps) {
+  sf::clear_error();
+  if (!w) return sf::fail(SF_ERR_INVALID, "window is NULL");
+  if (n_order < 0 || n_layers < 0) return sf::fail(SF_ERR_INVALID, "negative count");
+  if (n_order == 0) return SF_OK;
+  if (!layers || !order || !steps) return sf::fail(SF_ERR_INVALID, "NULL array");
+  sf::AdamConsts probe;
+  SF_TRY(sf::make_adam_consts(hp, 1, true, &probe));  // validates hp before enqueueing
+  for (int v = 0; v < n_order; ++v)
+    if (order[v] < 0 || order[v] >= n_layers)
+      return sf::fail(SF_ERR_INVALID, "order[%d] = %d out of [0, %d)", v, order[v], n_layers);
+  for (int l = 0; l < n_layers; ++l) {
+    SF_TRY(check_layer(w, layers[l], l));
+    if (steps[l] < 0) return sf::fail(SF_ERR_INVALID, "steps[%d] < 0", l);
+  }
+  if ((int)w->ev_layer.size() < n_layers) {
+    int old = (int)w->ev_layer.size();
+    w->ev_layer.resize(n_layers, nullptr);
+    w->layer_pending.resize(n_layers, false);
+    for (int l = old; l < n_layers; ++l) SF_TRY(new_event(&w->ev_layer[l]));
+  }
+
+  std::vector<sf_tensor> dev(w->n_tensors);
+  for (int v = 0; v < n_order; ++v) {
+    const int l = order[v];
+    const int s = (int)(w->visits % w->n_slots);
+    const sf_host_layer& L = layers[l];
+    const std::vector<sf_tensor>& slot = w->slots[s];
+
+    // h2d: slot free, previous write-back of this layer landed, then copy in.
+    if (w->slot_used[s]) SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_free[s], 0), "wait slot free");
+    if (w->layer_pending[l])
+      SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_layer[l], 0), "wait layer write-back");
+    for (int t = 0; t < L.n_tensors; ++t) {
+      const sf_tensor& h = L.tensors[t];
+      const size_t n = (size_t)h.numel;
+      SF_TRY(copy_async(const_cast<void*>(slot[t].grad), h.grad, 2 * n, cudaMemcpyHostToDevice, w->h2d, "h2d grad"));
+      SF_TRY(copy_async(slot[t].master, h.master, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d master"));
+      SF_TRY(copy_async(slot[t].exp_avg, h.exp_avg, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg"));
+      SF_TRY(copy_async(slot[t].exp_avg_sq, h.exp_avg_sq, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg_sq"));
+    }
+    SF_CUDA_TRY(cudaEventRecord(w->ev_in[s], w->h2d), "record ev_in");
+    w->slot_used[s] = true;
+
+    // compute: the fused update on the slot.
+    SF_CUDA_TRY(cudaStreamWaitEvent(w->comp, w->ev_in[s], 0), "wait ev_in");
+    for (int t = 0; t < L.n_tensors; ++t) {
+      dev[t] = slot[t];
+      dev[t].numel = L.tensors[t].numel;
+      if (!L.tensors[t].weight) dev[t].weight = nullptr;
+    }
+    const int64_t step = steps[l] + 1;
+    SF_TRY(sf::adamw_layer_step_impl(dev.data(), L.n_tensors, hp, step, w->comp));
+    steps[l] = step;
+    SF_CUDA_TRY(cudaEventRecord(w->ev_done[s], w->comp), "record ev_done");
+
+    // d2h: write the layer back; the slot is free when these copies end.
+    SF_CUDA_TRY(cudaStreamWaitEvent(w->d2h, w->ev_done[s], 0), "wait ev_done");
+    for (int t = 0; t < L.n_tensors; ++t) {
+      const sf_tensor& h = L.tensors[t];
+      const size_t n = (size_t)h.numel;
+      SF_TRY(copy_async(h.master, slot[t].master, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h master"));
+      SF_TRY(copy_async(h.exp_avg, slot[t].exp_avg, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg"));
+      SF_TRY(copy_async(h.exp_avg_sq, slot[t].exp_avg_sq, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg_sq"));
+      if (h.weight)
+        SF_TRY(copy_async(h.weight, slot[t].weight, 2 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h weight"));
+    }
+    SF_CUDA_TRY(cudaEventRecord(w->ev_free[s], w->d2h), "record ev_free");
+    SF_CUDA_TRY(cudaEventRecord(w->ev_layer[l], w->d2h), "record ev_layer");
+    w->layer_pending[l] = true;
+    ++w->visits;
+  }
+  return SF_OK;
+}
+
+sf_status sf_window_sync(sf_window w, int64_t timeout_ms) {
+  sf::clear_error();
+  if (!w) return sf::fail(SF_ERR_INVALID, "window is NULL");
+  SF_TRY(sf::bounded_wait_stream(w->h2d, timeout_ms, "window h2d stream"));
+  SF_TRY(sf::bounded_wait_stream(w->comp, timeout_ms, "window compute stream"));
+  SF_TRY(sf::bounded_wait_stream(w->d2h, timeout_ms, "window d2h stream"));
+  return SF_OK;
+}
+
+sf_status sf_window_destroy(sf_window w) {
+  sf::clear_error();
+  if (!w) return SF_OK;
+  sf_status st = sf_window_sync(w, 0);
+  destroy_events(w);
+  delete w;
+  return st;
+}
+
+// Test hook: make the n-th copy the window enqueues from now on fail once
+// (n >= 1), or switch the hook off (n = 0).  Host-side only: the failing
+// copy is never handed to CUDA.
+void sf_test_fail_copy_after(int64_t n) {
+  g_copy_count = 0;
+  g_fail_copy_at = n > 0 ? n : 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,284 @@
+"""Thin ctypes binding over the C ABI of ``libsfopt.so`` (include/sfopt.h).
+
+Argument marshalling only: every step of the update runs in the library's
+CUDA kernels.  Functions keep the C names; they take torch tensors (or raw
+integer addresses), torch CUDA streams and plain Python numbers, and raise
+``SfError`` when the library returns a non-OK status.  There is no fallback:
+if the library is missing or fails to load, ``load()`` raises.
+"""
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libsfopt.so")
+
+SF_OK, SF_ERR_INVALID, SF_ERR_CUDA, SF_ERR_OOM, SF_ERR_UNSUPPORTED, SF_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+SF_BF16, SF_FP32 = 0, 1
+SF_MAX_TENSORS_PER_LAUNCH = 48
+
+# Every symbol include/sfopt.h declares.
+EXPORTS = [
+    "sf_adamw_layer_step", "lsp_projector_create", "lsp_projector_export_csc",
+    "lsp_projector_rows", "lsp_projector_dim", "lsp_projector_nnz_per_row",
+    "lsp_projector_destroy", "lsp_workspace_bytes", "lsp_compress", "lsp_adamw_compressed",
+    "lsp_decompress_apply", "sf_window_create", "sf_slide_window_step", "sf_window_sync",
+    "sf_window_destroy", "sf_sync_status", "sf_last_error", "sf_version",
+    "sf_test_fail_copy_after",
+]
+
+
+class SfError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"status {status}: {msg}")
+        self.status = status
+
+
+class sf_adamw_hparams(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double)]
+
+
+class sf_tensor(ctypes.Structure):
+    _fields_ = [("grad", ctypes.c_void_p), ("master", ctypes.c_void_p), ("exp_avg", ctypes.c_void_p),
+                ("exp_avg_sq", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("numel", ctypes.c_int64)]
+
+
+class sf_host_layer(ctypes.Structure):
+    _fields_ = [("tensors", ctypes.POINTER(sf_tensor)), ("n_tensors", ctypes.c_int)]
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_INT = ctypes.c_int
+_ST = ctypes.c_int
+
+_SIGS = {
+    "sf_adamw_layer_step": (_ST, [ctypes.POINTER(sf_tensor), _INT, ctypes.POINTER(sf_adamw_hparams), _I64, _P]),
+    "lsp_projector_create": (_ST, [_I64, _I32, _I32, _P, _P, _INT, _P, ctypes.POINTER(_P)]),
+    "lsp_projector_export_csc": (_ST, [_P, _P, _P, _P, _P, _P]),
+    "lsp_projector_rows": (_I64, [_P]),
+    "lsp_projector_dim": (_I32, [_P]),
+    "lsp_projector_nnz_per_row": (_I32, [_P]),
+    "lsp_projector_destroy": (_ST, [_P]),
+    "lsp_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I32]),
+    "lsp_compress": (_ST, [_P, _P, _P, _INT, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
+    "lsp_adamw_compressed": (_ST, [_P, _P, _P, _P, _I64, ctypes.POINTER(sf_adamw_hparams), _I64, _P]),
+    "lsp_decompress_apply": (_ST, [_P, _P, _P, _P, _INT, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
+    "sf_window_create": (_ST, [_INT, ctypes.POINTER(ctypes.POINTER(sf_tensor)), _INT, _P, _P, _P, ctypes.POINTER(_P)]),
+    "sf_slide_window_step": (_ST, [_P, ctypes.POINTER(sf_host_layer), _INT, ctypes.POINTER(_I32), _INT,
+                                   ctypes.POINTER(sf_adamw_hparams), ctypes.POINTER(_I64)]),
+    "sf_window_sync": (_ST, [_P, _I64]),
+    "sf_window_destroy": (_ST, [_P]),
+    "sf_sync_status": (_ST, [_P]),
+    "sf_last_error": (ctypes.c_char_p, []),
+    "sf_version": (ctypes.c_char_p, []),
+    "sf_test_fail_copy_after": (None, [_I64]),
+}
+
+_lib = None
+
+
+def load(path=None):
+    """Load libsfopt.so (built by ``layer_optimizer_gb300.build``); raises if absent."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with `python -m layer_optimizer_gb300.build`")
+    try:  # make sure a libcudart with the library's SONAME is in the process (torch ships one)
+        import torch  # noqa: F401
+    except ImportError:
+        pass
+    lib = ctypes.CDLL(p)
+    for name, (res, args) in _SIGS.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(st):
+    if st != SF_OK:
+        raise SfError(st, load().sf_last_error().decode())
+
+
+def _addr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def hparams(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01):
+    return sf_adamw_hparams(lr, beta1, beta2, eps, weight_decay)
+
+
+def make_tensor(grad, master, exp_avg, exp_avg_sq, weight=None, numel=None):
+    """sf_tensor from torch tensors (or addresses; then ``numel`` is required)."""
+    n = numel if numel is not None else master.numel()
+    return sf_tensor(_addr(grad), _addr(master), _addr(exp_avg), _addr(exp_avg_sq), _addr(weight), n)
+
+
+def tensor_array(items):
+    arr = (sf_tensor * max(1, len(items)))()
+    for i, t in enumerate(items):
+        arr[i] = t if isinstance(t, sf_tensor) else make_tensor(*t)
+    return arr
+
+
+# ------------------------------------------------------------------ (a) ----
+
+def sf_adamw_layer_step(tensors, hp, step, stream=None):
+    arr = tensor_array(tensors)
+    _check(load().sf_adamw_layer_step(arr, len(tensors), ctypes.byref(hp), step, _stream(stream)))
+
+
+# ------------------------------------------------------------------ (b) ----
+
+class Projector:
+    """Owning wrapper of an lsp_projector handle."""
+
+    def __init__(self, handle):
+        self.handle = handle
+
+    @property
+    def rows(self):
+        return load().lsp_projector_rows(self.handle)
+
+    @property
+    def d(self):
+        return load().lsp_projector_dim(self.handle)
+
+    @property
+    def k(self):
+        return load().lsp_projector_nnz_per_row(self.handle)
+
+    def close(self):
+        if self.handle:
+            _check(load().lsp_projector_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            if self.handle:
+                load().lsp_projector_destroy(self.handle)
+        except Exception:
+            pass
+
+
+def lsp_projector_create(rows, d, k, col_idx, val, validate=True, stream=None):
+    h = ctypes.c_void_p()
+    _check(load().lsp_projector_create(rows, d, k, _addr(col_idx), _addr(val), int(bool(validate)),
+                                       _stream(stream), ctypes.byref(h)))
+    return Projector(h.value)
+
+
+def lsp_projector_export_csc(p, col_ptr=None, row_idx=None, val=None, bucket_perm=None, stream=None):
+    _check(load().lsp_projector_export_csc(p.handle, _addr(col_ptr), _addr(row_idx), _addr(val),
+                                           _addr(bucket_perm), _stream(stream)))
+
+
+def lsp_workspace_bytes(m, n, d):
+    return load().lsp_workspace_bytes(m, n, d)
+
+
+def lsp_compress(P, Q, G, g_dtype, m, n, S, ws, ws_bytes, stream=None):
+    _check(load().lsp_compress(P.handle, Q.handle, _addr(G), g_dtype, m, n, _addr(S), _addr(ws),
+                               ws_bytes, _stream(stream)))
+
+
+def lsp_adamw_compressed(S, m, v, dS, d2, hp, step, stream=None):
+    _check(load().lsp_adamw_compressed(_addr(S), _addr(m), _addr(v), _addr(dS), d2, ctypes.byref(hp),
+                                       step, _stream(stream)))
+
+
+def lsp_decompress_apply(P, Q, dS, W, w_dtype, w_bf16_mirror, m, n, ws, ws_bytes, stream=None):
+    _check(load().lsp_decompress_apply(P.handle, Q.handle, _addr(dS), _addr(W), w_dtype,
+                                       _addr(w_bf16_mirror), m, n, _addr(ws), ws_bytes, _stream(stream)))
+
+
+# ------------------------------------------------------------------ (c) ----
+
+class Window:
+    """Owning wrapper of an sf_window handle; keeps its slot arrays alive."""
+
+    def __init__(self, handle, keep):
+        self.handle = handle
+        self._keep = keep
+
+    def sync(self, timeout_ms=0):
+        _check(load().sf_window_sync(self.handle, timeout_ms))
+
+    def close(self):
+        if self.handle:
+            st = load().sf_window_destroy(self.handle)
+            self.handle = None
+            _check(st)
+
+    def __del__(self):
+        try:
+            if self.handle:
+                load().sf_window_destroy(self.handle)
+        except Exception:
+            pass
+
+
+def sf_window_create(slots, h2d_stream, compute_stream, d2h_stream):
+    """``slots``: list (one per slot) of lists of sf_tensor (device buffers)."""
+    n_t = len(slots[0]) if slots else 0
+    arrays = [tensor_array(s) for s in slots]
+    ptrs = (ctypes.POINTER(sf_tensor) * max(1, len(slots)))()
+    for i, a in enumerate(arrays):
+        ptrs[i] = ctypes.cast(a, ctypes.POINTER(sf_tensor))
+    h = ctypes.c_void_p()
+    _check(load().sf_window_create(len(slots), ptrs, n_t, _stream(h2d_stream), _stream(compute_stream),
+                                   _stream(d2h_stream), ctypes.byref(h)))
+    return Window(h.value, (arrays, ptrs))
+
+
+def host_layers(layers):
+    """``layers``: list of lists of sf_tensor (pinned host buffers)."""
+    arrays = [tensor_array(l) for l in layers]
+    out = (sf_host_layer * max(1, len(layers)))()
+    for i, (a, l) in enumerate(zip(arrays, layers)):
+        out[i] = sf_host_layer(ctypes.cast(a, ctypes.POINTER(sf_tensor)), len(l))
+    return out, arrays
+
+
+def sf_slide_window_step(window, layers, order, hp, steps):
+    """``layers`` from ``host_layers``; ``steps`` a ctypes int64 array (updated)."""
+    hl, keep = layers
+    n_layers = len(keep)
+    order_arr = (ctypes.c_int32 * max(1, len(order)))(*order)
+    _check(load().sf_slide_window_step(window.handle, hl, n_layers, order_arr, len(order), ctypes.byref(hp),
+                                       steps))
+
+
+def sf_sync_status(stream=None):
+    _check(load().sf_sync_status(_stream(stream)))
+
+
+def sf_last_error():
+    return load().sf_last_error().decode()
+
+
+def sf_version():
+    return load().sf_version().decode()
+
+
+def sf_test_fail_copy_after(n):
+    load().sf_test_fail_copy_after(n)

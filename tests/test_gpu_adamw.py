@@ -1,0 +1,182 @@
+"""Parity of the fused multi-tensor AdamW kernel with the fp64 oracle (GPU)."""
+
+import numpy as np
+import pytest
+import torch
+
+from _util import HP, TOL_STATE, bits, check_bf16, check_close, f64
+from layer_optimizer_gb300 import native, synth
+from oracle import adamw as oa
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _layer(sizes, seed, offset_elems=0):
+    """Device buffers for a layer; optional element offset into larger buffers (misalignment)."""
+    out = []
+    for i, n in enumerate(sizes):
+        o = offset_elems
+        g = torch.empty(n + o, dtype=torch.bfloat16, device=DEV)[o:]
+        p = torch.empty(n + o, device=DEV)[o:]
+        p.copy_(synth.normal((n,), 0.02, synth.sub_seed(seed, 0, i)))
+        m = torch.zeros(n + o, device=DEV)[o:]
+        v = torch.zeros(n + o, device=DEV)[o:]
+        w = torch.empty(n + o, dtype=torch.bfloat16, device=DEV)[o:]
+        out.append([g, p, m, v, w])
+    return out
+
+
+def _run_and_check(sizes, steps=3, seed=0, offset=0, grads=None, with_weight=True):
+    lay = _layer(sizes, seed, offset)
+    states = [oa.AdamWState(f64(x[1])) for x in lay]
+    hp = native.hparams(**HP)
+    for t in range(1, steps + 1):
+        for i, n in enumerate(sizes):
+            g = grads(i, t) if grads else synth.normal((n,), 1e-3, synth.sub_seed(seed, 1, i, t),
+                                                        dtype=torch.bfloat16)
+            lay[i][0].copy_(g)
+        # one-step parity: the oracle starts from the kernel's own previous state
+        pre = [(f64(x[1]), f64(x[2]), f64(x[3])) for x in lay]
+        ts = [native.make_tensor(x[0], x[1], x[2], x[3], x[4] if with_weight else None) for x in lay]
+        native.sf_adamw_layer_step(ts, hp, t)
+        torch.cuda.synchronize()
+        for i, x in enumerate(lay):
+            st = oa.AdamWState(pre[i][0], pre[i][1], pre[i][2])
+            st.m_abs, st.v_abs, st.theta_abs = states[i].m_abs, states[i].v_abs, np.abs(pre[i][0])
+            g64 = f64(x[0].float())
+            wref = oa.adamw_step(st, g64, t, **HP)
+            oa.adamw_step(states[i], g64, t, **HP)
+            check_close(f"master[{i}] t={t}", x[1], st.theta, st.theta_abs, TOL_STATE)
+            check_close(f"m[{i}] t={t}", x[2], st.m, st.m_abs, TOL_STATE)
+            check_close(f"v[{i}] t={t}", x[3], st.v, st.v_abs, TOL_STATE)
+            if with_weight:
+                check_bf16(f"w[{i}] t={t}", bits(x[4]), st.theta)
+    # chained drift over all steps stays within t x the one-step bound
+    for i, x in enumerate(lay):
+        check_close(f"master[{i}] chained", x[1], states[i].theta, states[i].theta_abs, TOL_STATE * steps)
+    return lay
+
+
+def test_one_linear_layer_1024x1024_three_steps():
+    _run_and_check([1024 * 1024], steps=3)
+
+
+def test_ragged_sizes_and_many_tensors():
+    sizes = [1, 2, 7, 8, 9, 15, 16, 17, 255, 4095, 4096, 4097, 8191, 100003, 0, 3]
+    _run_and_check(sizes, steps=2, seed=1)
+
+
+def test_more_tensors_than_one_launch_holds():
+    sizes = [37 + 13 * i for i in range(native.SF_MAX_TENSORS_PER_LAUNCH + 9)]
+    _run_and_check(sizes, steps=2, seed=2)
+
+
+@pytest.mark.parametrize("offset", [1, 3, 4, 5])
+def test_misaligned_pointers(offset):
+    # all arrays shifted by the same element count: bf16 and fp32 offsets
+    # differ in bytes, so some offsets keep a common 16-byte phase and some don't
+    _run_and_check([5000, 33, 70001], steps=2, seed=3, offset=offset)
+
+
+def test_no_weight_output():
+    _run_and_check([3000, 12345], steps=2, seed=4, with_weight=False)
+
+
+def test_constant_gradient_closed_form_22_steps():
+    n = 50000
+    g = synth.normal((n,), 1e-3, 77, dtype=torch.bfloat16).to(DEV)
+    lay = _layer([n], 5)
+    th0 = f64(lay[0][1])
+    hp = native.hparams(**HP)
+    for t in range(1, 23):
+        lay[0][0].copy_(g)
+        native.sf_adamw_layer_step([native.make_tensor(*lay[0])], hp, t)
+    torch.cuda.synchronize()
+    lam = HP["lr"] * HP["weight_decay"]
+    g64 = f64(g.float())
+    s = g64 / (np.abs(g64) + HP["eps"])
+    geo = -np.expm1(22 * np.log1p(-lam)) / lam
+    want = (1 - lam) ** 22 * th0 - HP["lr"] * s * geo
+    mag = np.abs(th0) + HP["lr"] * geo
+    check_close("closed form t=22", lay[0][1], want, mag, TOL_STATE * 22)
+
+
+def test_special_values():
+    n = 64
+    lay = _layer([n], 6)
+    g = torch.zeros(n, dtype=torch.bfloat16)
+    g[1] = float("inf")
+    g[2] = float("nan")
+    g[3] = -1e30
+    g[4] = 1e-40  # bf16 subnormal
+    lay[0][0].copy_(g)
+    native.sf_adamw_layer_step([native.make_tensor(*lay[0])], native.hparams(**HP), 1)
+    torch.cuda.synchronize()
+    p = lay[0][1].cpu()
+    assert torch.isnan(p[1]) and torch.isnan(p[2])       # inf/inf -> nan propagates, no skipping
+    assert torch.isfinite(p[0]) and torch.isfinite(p[3]) and torch.isfinite(p[4])
+
+
+def test_deterministic_repeat():
+    a = _run_and_check([123457], steps=1, seed=8)
+    b = _run_and_check([123457], steps=1, seed=8)
+    for x, y in zip(a[0], b[0]):
+        assert torch.equal(x.view(torch.uint8) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.uint8) if y.dtype == torch.bfloat16 else y.view(torch.int32))
+
+
+def test_guard_bands_untouched():
+    # 4 KiB canaries before and after every array
+    n, pad = 10007, 1024
+    bufs = [torch.full((n + 2 * pad,), 12345.0, device=DEV) for _ in range(3)]
+    gb = torch.full((n + 2 * pad,), 3.0, dtype=torch.bfloat16, device=DEV)
+    wb = torch.full((n + 2 * pad,), 7.0, dtype=torch.bfloat16, device=DEV)
+    t = native.make_tensor(gb[pad:pad + n], bufs[0][pad:pad + n], bufs[1][pad:pad + n], bufs[2][pad:pad + n],
+                           wb[pad:pad + n])
+    native.sf_adamw_layer_step([t], native.hparams(**HP), 1)
+    torch.cuda.synchronize()
+    for b in bufs:
+        assert torch.all(b[:pad] == 12345.0) and torch.all(b[pad + n:] == 12345.0)
+    assert torch.all(wb[:pad] == 7.0) and torch.all(wb[pad + n:] == 7.0)
+    assert torch.all(gb == 3.0)
+
+
+def test_invalid_arguments_raise():
+    lay = _layer([10], 9)
+    t = native.make_tensor(*lay[0])
+    with pytest.raises(native.SfError):
+        native.sf_adamw_layer_step([t], native.hparams(**HP), 0)
+    bad = native.make_tensor(None, lay[0][1], lay[0][2], lay[0][3], None)
+    with pytest.raises(native.SfError):
+        native.sf_adamw_layer_step([bad], native.hparams(**HP), 1)
+
+
+@pytest.mark.slow
+def test_opt13_stack_sampled():
+    """All 24 OPT-1.3B layers, one fused step per layer, checked on sampled elements."""
+    layer = synth.OPT13_LAYER
+    hp = native.hparams(**HP)
+    rng = np.random.default_rng(0)
+    for li in range(synth.OPT13_LAYERS):
+        bufs = []
+        for ti, (_, n) in enumerate(layer):
+            g = synth.fill_normal_(torch.empty(n, dtype=torch.bfloat16, device=DEV), 1e-3, synth.sub_seed(1, li, ti))
+            p = synth.fill_normal_(torch.empty(n, device=DEV), 0.02, synth.sub_seed(2, li, ti))
+            bufs.append([g, p, torch.zeros(n, device=DEV), torch.zeros(n, device=DEV),
+                         torch.empty(n, dtype=torch.bfloat16, device=DEV)])
+        idx = [torch.from_numpy(np.unique(np.concatenate([
+            rng.integers(0, n, 20000), np.arange(min(n, 4096)), np.arange(max(0, n - 4096), n)]))).to(DEV)
+            for _, n in layer]
+        pre = [(f64(b[1][ix]), f64(b[0][ix].float())) for b, ix in zip(bufs, idx)]
+        native.sf_adamw_layer_step([native.make_tensor(*b) for b in bufs], hp, 1)
+        torch.cuda.synchronize()
+        for (th, g64), b, ix in zip(pre, bufs, idx):
+            st = oa.AdamWState(th)
+            wref = oa.adamw_step(st, g64, 1, **HP)
+            check_close("master", b[1][ix], st.theta, st.theta_abs, TOL_STATE)
+            check_close("m", b[2][ix], st.m, st.m_abs, TOL_STATE)
+            check_close("v", b[3][ix], st.v, st.v_abs, TOL_STATE)
+            check_bf16("w", bits(b[4][ix]), st.theta)
+        del bufs

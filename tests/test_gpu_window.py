@@ -1,0 +1,177 @@
+"""Layer-sliding window engine: results, ordering, failure handling (GPU)."""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from _util import HP, TOL_STATE, check_close, f64
+from layer_optimizer_gb300 import native, synth
+from oracle import adamw as oa
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _host_layer(sizes, seed, weight=True):
+    out = []
+    for i, n in enumerate(sizes):
+        g = synth.normal((n,), 1e-3, synth.sub_seed(seed, 0, i), dtype=torch.bfloat16).pin_memory()
+        p = synth.normal((n,), 0.02, synth.sub_seed(seed, 1, i)).pin_memory()
+        m = torch.zeros(n).pin_memory()
+        v = torch.zeros(n).pin_memory()
+        w = torch.zeros(n, dtype=torch.bfloat16).pin_memory() if weight else None
+        out.append([g, p, m, v, w])
+    return out
+
+
+def _slots(n_slots, caps):
+    return [[[torch.empty(c, dtype=torch.bfloat16, device=DEV), torch.empty(c, device=DEV),
+              torch.empty(c, device=DEV), torch.empty(c, device=DEV),
+              torch.empty(c, dtype=torch.bfloat16, device=DEV)] for c in caps] for _ in range(n_slots)]
+
+
+def _window(slots, streams):
+    sl = [[native.make_tensor(*t) for t in s] for s in slots]
+    return native.sf_window_create(sl, *streams)
+
+
+def _resident_reference(layers, order, grads_per_visit=None):
+    """The same visits on device-resident copies with sf_adamw_layer_step."""
+    dev = [[[x.to(DEV) if x is not None else None for x in t] for t in L] for L in layers]
+    steps = [0] * len(layers)
+    hp = native.hparams(**HP)
+    for l in order:
+        steps[l] += 1
+        native.sf_adamw_layer_step([native.make_tensor(*t) for t in dev[l]], hp, steps[l])
+    torch.cuda.synchronize()
+    return dev, steps
+
+
+SIZES = [4099, 17, 65536, 3]
+
+
+def test_window_matches_resident_path_bitwise():
+    layers = [_host_layer(SIZES, 10 + l) for l in range(4)]
+    ref_in = [[[x.clone() if x is not None else None for x in t] for t in L] for L in layers]
+    order = [l % 4 for l in range(12)]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = _window(_slots(2, SIZES), streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in layers])
+    steps = (ctypes.c_int64 * 4)()
+    native.sf_slide_window_step(win, hl, order, native.hparams(**HP), steps)
+    win.sync()
+    assert list(steps) == [3, 3, 3, 3]
+    ref, ref_steps = _resident_reference(ref_in, order)
+    for L, R in zip(layers, ref):
+        for t, r in zip(L, R):
+            for k in (1, 2, 3):
+                assert torch.equal(t[k].view(torch.int32), r[k].cpu().view(torch.int32))
+            assert torch.equal(t[4].view(torch.int16), r[4].cpu().view(torch.int16))
+    win.close()
+
+
+def test_window_constant_gradient_closed_form():
+    # grads stay fixed in the host slots, so every visit applies the same g
+    layers = [_host_layer([20000], 30 + l) for l in range(4)]
+    th0 = [f64(L[0][1]) for L in layers]
+    g64 = [f64(L[0][0].float()) for L in layers]
+    order = [l % 4 for l in range(88)]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = _window(_slots(2, [20000]), streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in layers])
+    steps = (ctypes.c_int64 * 4)()
+    native.sf_slide_window_step(win, hl, order, native.hparams(**HP), steps)
+    win.sync()
+    assert list(steps) == [22] * 4
+    lam = HP["lr"] * HP["weight_decay"]
+    geo = -np.expm1(22 * np.log1p(-lam)) / lam
+    for L, t0, g in zip(layers, th0, g64):
+        s = g / (np.abs(g) + HP["eps"])
+        want = (1 - lam) ** 22 * t0 - HP["lr"] * s * geo
+        check_close("theta_22", L[0][1], want, np.abs(t0) + HP["lr"] * geo, TOL_STATE * 22)
+    win.close()
+
+
+def test_window_three_slots_uneven_order_and_no_weight():
+    layers = [_host_layer(SIZES[:2], 50 + l, weight=(l % 2 == 0)) for l in range(5)]
+    ref_in = [[[x.clone() if x is not None else None for x in t] for t in L] for L in layers]
+    order = [0, 2, 2, 4, 1, 0, 3, 3, 3, 1]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = _window(_slots(3, SIZES[:2]), streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in layers])
+    steps = (ctypes.c_int64 * 5)()
+    native.sf_slide_window_step(win, hl, order, native.hparams(**HP), steps)
+    win.sync()
+    ref, ref_steps = _resident_reference(ref_in, order)
+    assert list(steps) == ref_steps
+    for L, R in zip(layers, ref):
+        for t, r in zip(L, R):
+            assert torch.equal(t[1].view(torch.int32), r[1].cpu().view(torch.int32))
+    win.close()
+
+
+def test_window_oracle_parity_one_visit():
+    layers = [_host_layer([70001, 9], 70)]
+    pre = [(f64(t[1]), f64(t[0].float())) for t in layers[0]]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = _window(_slots(2, [70001, 9]), streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in layers[0]]])
+    steps = (ctypes.c_int64 * 1)()
+    native.sf_slide_window_step(win, hl, [0], native.hparams(**HP), steps)
+    win.sync()
+    for (th, g), t in zip(pre, layers[0]):
+        st = oa.AdamWState(th)
+        oa.adamw_step(st, g, 1, **HP)
+        check_close("master", t[1], st.theta, st.theta_abs, TOL_STATE)
+        check_close("m", t[2], st.m, st.m_abs, TOL_STATE)
+    win.close()
+
+
+def test_injected_copy_failure_leaves_window_usable():
+    layers = [_host_layer(SIZES, 90 + l) for l in range(2)]
+    ref_in = [[[x.clone() if x is not None else None for x in t] for t in L] for L in layers]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = _window(_slots(2, SIZES), streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in layers])
+    steps = (ctypes.c_int64 * 2)()
+    native.sf_test_fail_copy_after(3)   # third h2d copy of the first visit
+    with pytest.raises(native.SfError, match="injected"):
+        native.sf_slide_window_step(win, hl, [0, 1], native.hparams(**HP), steps)
+    assert list(steps) == [0, 0]
+    native.sf_test_fail_copy_after(0)
+    native.sf_slide_window_step(win, hl, [0, 1], native.hparams(**HP), steps)
+    win.sync()
+    ref, _ = _resident_reference(ref_in, [0, 1])
+    for L, R in zip(layers, ref):
+        for t, r in zip(L, R):
+            assert torch.equal(t[1].view(torch.int32), r[1].cpu().view(torch.int32))
+    win.close()
+
+
+def test_bounded_wait_times_out_then_recovers():
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = _window(_slots(1, [16]), streams)
+    with torch.cuda.stream(streams[1]):
+        torch.cuda._sleep(int(3e9))        # a finite spin of ~1.5 s on the compute stream
+    with pytest.raises(native.SfError) as e:
+        win.sync(timeout_ms=50)
+    assert e.value.status == native.SF_ERR_TIMEOUT
+    win.sync()                            # default bound: waits for the spin to end
+    win.close()
+
+
+def test_invalid_visits_rejected_before_enqueue():
+    layers = [_host_layer([100], 99)]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = _window(_slots(2, [50]), streams)   # slot too small
+    hl = native.host_layers([[native.make_tensor(*t) for t in layers[0]]])
+    steps = (ctypes.c_int64 * 1)()
+    with pytest.raises(native.SfError, match="capacity"):
+        native.sf_slide_window_step(win, hl, [0], native.hparams(**HP), steps)
+    with pytest.raises(native.SfError, match="out of"):
+        native.sf_slide_window_step(win, hl, [1], native.hparams(**HP), steps)
+    assert steps[0] == 0
+    win.close()
