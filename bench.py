@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--layers", type=int, default=24, help="OPT-1.3B layers (24 = the full stack)")
     ap.add_argument("--profile-small", action="store_true",
-                    help="2 layers, 1 step, no extras: a small case for ncu captures")
+                    help="1 layer, 1 warm-up + 1 timed step, no extras: a small case for ncu captures")
     return ap.parse_args()
 
 
@@ -305,9 +305,6 @@ def run_e2e(args, world):
     win.sync()
     barrier(world)
     t0 = time.perf_counter()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(streams[0])
     for _ in range(args.steps):
         native.sf_slide_window_step(win, hl, order, hp, steps)
     win.sync()
@@ -475,7 +472,7 @@ def main_reference(args, rank, world):
 def main():
     args = parse()
     if args.profile_small:
-        args.layers, args.steps, args.warmup = 2, 1, 1
+        args.layers, args.steps, args.warmup = 1, 1, 1
         args.no_e2e = args.no_lsp = args.no_cpu = True
     rank, world = dist_init(args)
     if args.impl == "reference":
