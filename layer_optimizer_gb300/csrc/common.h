@@ -54,6 +54,11 @@ struct AdamConsts {
   float eps;
 };
 
+// Reads and clears the device-side error word that bounded waits and index
+// checks in the kernels set (0 = none; bit 1 = a wait ran out; bit 2 = an
+// out-of-range index was skipped).
+int read_and_clear_device_error();
+
 sf_status make_adam_consts(const sf_adamw_hparams* hp, int64_t step, bool with_decay,
                            AdamConsts* out);
 

@@ -1,28 +1,1017 @@
-// Placeholder: the sparse-projector kernels land in the next change.
-#include "common.h"
+// Learned-sparse-projector path: projector bookkeeping, compress
+// S = P^T G Q, decompress-apply W -= P dS Q^T.
+//
+// "Practical offloading for fine-tuning LLM on commodity GPU via learned
+// sparse projectors" (LSP-Offload; abstract and method section) compresses
+// the gradient with sparse projectors holding a fixed number k of nonzeros
+// per row, updates in the d x d compressed space and decompresses the step
+// back.  The pages give no kernel; everything below is designed for sm_103a.
+//
+// Why no tensor cores: P and Q are k/d dense (8/512 = 1.6 %); a dense
+// product would do d/k = 64x the useful multiply-adds.  The work is a
+// gather: every G element meets k projector entries, 2 multiply-adds per
+// G byte (fp32 G, k = 8).  The kernels stream the big matrix once through
+// shared memory and keep the lanes of a warp on its contiguous dimension,
+// so every gathered shared-memory access is conflict-free and every
+// projector entry is a warp-uniform broadcast.
+//
+// Compress, two gathers (R-first):
+//   stage 1  R^T = (P^T G)^T      k_gather_t over G, A = P      (n x d)
+//   stage 2  S   = (Q^T R^T)^T    k_gather_t over R^T, A = Q    (d x d)
+// k_gather_t(A, B) writes Y^T = (A^T B)^T: a CTA owns 128 columns of B and
+// 8 x warps outputs a (columns of A); B streams through shared memory in
+// windows of 64 rows by TMA (cp.async.bulk.tensor), the CTAs of one column
+// block form a cluster and share every window by TMA multicast, so B is read
+// from L2 once.  A's entries come from a window-major column list (entries
+// of window w and column a, rows ascending, with a prefix table), so a warp
+// finds its (window, a) entries with two 16-byte loads.  Row splits (for
+// grid size) write partial outputs that one reduction sums in split order.
+//
+// Decompress:
+//   V = dS Q^T (d x n)          k_v: dS^T block resident in shared memory,
+//                               Q rows as warp-uniform entries
+//   W[i, :] -= sum_l P[i,a_l] V[a_l, :]   k_apply: a 64-column block of V
+//                               resident in shared memory, W read and
+//                               written once, coalesced.
+// Nothing uses atomics on floating-point data: every sum has a fixed order,
+// so results are bitwise deterministic.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
 
-struct lsp_projector_s { int64_t rows; int32_t d, k; };
+#include <algorithm>
+#include <new>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace sf {
+namespace {
+
+constexpr int kWinRows = 64;        // rows of A (and of B) per window
+constexpr int kColsPerCta = 128;    // B columns per gather CTA (4 per lane)
+constexpr int kStages = 4;          // TMA ring depth of the gather kernel
+constexpr int kTargetCtas = 148;    // grid size aimed at (about one CTA per SM)
+constexpr int kApplyCols = 64;      // W columns per apply CTA (2 per lane)
+constexpr int kVRows = 64;          // a rows per V CTA (2 per lane)
+constexpr int kMaxFastD = 512;      // shared-memory tiles of k_v / k_apply hold d <= 512
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+}  // namespace sf
+
+// ----------------------------------------------------------------------------
+// Projector handle
+// ----------------------------------------------------------------------------
+struct lsp_projector_s {
+  int device = 0;
+  int64_t rows = 0;
+  int32_t d = 0, k = 0, dp = 0, n_win = 0;
+  int32_t* ell_idx = nullptr;   // [rows*k], out-of-range ids replaced by (0, 0.0f)
+  float* ell_val = nullptr;
+  int32_t* col_ptr = nullptr;   // [d+1]
+  int32_t* row_idx = nullptr;   // [rows*k]
+  float* csc_val = nullptr;
+  int32_t* bucket_perm = nullptr;  // [d]
+  int32_t* wptr = nullptr;      // [n_win*dp + 1]: start of (window, a) in went
+  int2* went = nullptr;         // [rows*k]: (row, value bits), sorted by (window, a, row)
+  int32_t* wcnt = nullptr;      // [n_win*dp] scratch of the build
+  int32_t* csc_off = nullptr;   // [n_win*dp] scratch of the build
+  int32_t* totals = nullptr;    // [d] scratch of the build
+  int32_t* err = nullptr;       // [1]
+  void* block = nullptr;
+};
+
+namespace sf {
+namespace {
+
+// ----------------------------------------------------------------------------
+// Bookkeeping kernels (run once per projector)
+// ----------------------------------------------------------------------------
+
+// Per-window histogram of column ids.  Out-of-range ids are dropped and flagged.
+__global__ void k_window_hist(const int32_t* __restrict__ idx, int64_t rows, int k, int d, int dp,
+                              int32_t* __restrict__ wcnt, int32_t* __restrict__ err) {
+  extern __shared__ int32_t sh[];
+  const int w = blockIdx.x;
+  for (int c = threadIdx.x; c < dp; c += blockDim.x) sh[c] = 0;
+  __syncthreads();
+  const int64_t e0 = (int64_t)w * kWinRows * k;
+  const int64_t e1 = min(rows, (int64_t)(w + 1) * kWinRows) * k;
+  for (int64_t e = e0 + threadIdx.x; e < e1; e += blockDim.x) {
+    const int c = idx[e];
+    if (c >= 0 && c < d) atomicAdd(&sh[c], 1);
+    else atomicOr(err, kDevErrIndex);
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < dp; c += blockDim.x) wcnt[(int64_t)w * dp + c] = sh[c];
+}
+
+// Per column: exclusive offsets over windows, and the column total.
+__global__ void k_column_offsets(const int32_t* __restrict__ wcnt, int n_win, int d, int dp,
+                                 int32_t* __restrict__ csc_off, int32_t* __restrict__ totals) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= d) return;
+  int32_t off = 0;
+  for (int w = 0; w < n_win; ++w) {
+    csc_off[(int64_t)w * dp + c] = off;
+    off += wcnt[(int64_t)w * dp + c];
+  }
+  totals[c] = off;
+}
+
+// Single-block exclusive scan: out[i] = sum(in[0..i)), out[n] = total.
+__global__ void k_scan_exclusive(const int32_t* __restrict__ in, int64_t n, int32_t* __restrict__ out) {
+  __shared__ int32_t part[1024];
+  const int t = threadIdx.x, T = blockDim.x;
+  const int64_t per = (n + T - 1) / T;
+  const int64_t b = min(n, per * t), e = min(n, b + per);
+  int32_t s = 0;
+  for (int64_t i = b; i < e; ++i) s += in[i];
+  part[t] = s;
+  __syncthreads();
+  if (t == 0) {
+    int32_t run = 0;
+    for (int i = 0; i < T; ++i) {
+      const int32_t v = part[i];
+      part[i] = run;
+      run += v;
+    }
+    out[n] = run;
+  }
+  __syncthreads();
+  int32_t run = part[t];
+  for (int64_t i = b; i < e; ++i) {
+    const int32_t v = in[i];
+    out[i] = run;
+    run += v;
+  }
+}
+
+// One warp per window: stable placement of the window's entries into the
+// column lists (CSC) and the window-major lists.  Within a window the
+// entries are visited in ELL order (row-major), so rows ascend inside every
+// column; equal ids of one warp step are ranked by lane.
+__global__ void k_place(const int32_t* __restrict__ idx, const float* __restrict__ val, int64_t rows, int k,
+                        int d, int dp, int n_win, const int32_t* __restrict__ wptr,
+                        const int32_t* __restrict__ csc_off, const int32_t* __restrict__ col_ptr,
+                        int2* __restrict__ went, int32_t* __restrict__ row_idx, float* __restrict__ csc_val) {
+  extern __shared__ int32_t cnt_all[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int w = blockIdx.x * (blockDim.x >> 5) + warp;
+  int32_t* cnt = cnt_all + warp * dp;
+  for (int c = lane; c < dp; c += 32) cnt[c] = 0;
+  __syncwarp();
+  if (w >= n_win) return;
+  const int64_t e0 = (int64_t)w * kWinRows * k;
+  const int64_t e1 = min(rows, (int64_t)(w + 1) * kWinRows) * k;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int64_t base_e = e0; base_e < e1; base_e += 32) {
+    const int64_t e = base_e + lane;
+    int c = -1;
+    if (e < e1) {
+      c = idx[e];
+      if (c < 0 || c >= d) c = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, c);
+    const int rank = __popc(peers & lt);
+    int32_t base = 0;
+    if (c >= 0) base = cnt[c];
+    __syncwarp();
+    if (c >= 0 && rank == __popc(peers) - 1) cnt[c] = base + __popc(peers);
+    __syncwarp();
+    if (c >= 0) {
+      const int32_t row = (int32_t)(e / k);
+      const float v = val[e];
+      went[wptr[(int64_t)w * dp + c] + base + rank] = make_int2(row, __float_as_int(v));
+      const int32_t pc = col_ptr[c] + csc_off[(int64_t)w * dp + c] + base + rank;
+      row_idx[pc] = row;
+      csc_val[pc] = v;
+    }
+  }
+}
+
+// Column order by (nnz bucket, column id); bucket 0 = empty, else ceil(log2 nnz) + 1.
+__global__ void k_bucket_perm(const int32_t* __restrict__ col_ptr, int d, int32_t* __restrict__ perm) {
+  __shared__ int32_t wsum[32];
+  __shared__ int32_t run;
+  const int c = threadIdx.x;
+  int bucket = -1;
+  if (c < d) {
+    const int nnz = col_ptr[c + 1] - col_ptr[c];
+    bucket = 0;
+    if (nnz > 0) {
+      int b = 0;
+      while ((1 << b) < nnz) ++b;
+      bucket = b + 1;
+    }
+  }
+  if (c == 0) run = 0;
+  __syncthreads();
+  const int warp = c >> 5, lane = c & 31, nw = blockDim.x >> 5;
+  for (int b = 0; b <= 33; ++b) {
+    const bool f = bucket == b;
+    const unsigned bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) wsum[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0;
+    for (int i = 0; i < warp; ++i) before += wsum[i];
+    int total = 0;
+    for (int i = 0; i < nw; ++i) total += wsum[i];
+    if (f) perm[run + before + __popc(bal & ((1u << lane) - 1u))] = c;
+    __syncthreads();
+    if (c == 0) run += total;
+    __syncthreads();
+  }
+}
+
+// Validation: ids in range and no id repeated inside a row.
+__global__ void k_validate_rows(const int32_t* __restrict__ idx, int64_t rows, int k, int d,
+                                int32_t* __restrict__ err) {
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  const int32_t* p = idx + r * k;
+  for (int a = 0; a < k; ++a) {
+    const int ca = p[a];
+    if (ca < 0 || ca >= d) {
+      atomicOr(err, kDevErrIndex);
+      return;
+    }
+    for (int b = 0; b < a; ++b)
+      if (p[b] == ca) {
+        atomicOr(err, 4);
+        return;
+      }
+  }
+}
+
+// Copy of the ELL with out-of-range entries neutralised (id 0, value 0).
+__global__ void k_copy_ell(const int32_t* __restrict__ idx, const float* __restrict__ val, int64_t n, int d,
+                           int32_t* __restrict__ oidx, float* __restrict__ oval) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int c = idx[e];
+    const bool ok = c >= 0 && c < d;
+    oidx[e] = ok ? c : 0;
+    oval[e] = ok ? val[e] : 0.0f;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Gather kernel: Y^T = (A^T B)^T with TMA-staged windows of B
+// ----------------------------------------------------------------------------
+
+struct GatherArgs {
+  const int32_t* wptr;
+  const int2* went;
+  float* yt;               // [split][ncols][d]
+  int64_t split_stride;    // elements between split outputs
+  int32_t ncols;           // columns of B
+  int32_t d, dp;           // columns of A (outputs a)
+  int32_t n_win;           // windows of A / B rows
+  int32_t win_per_split;
+  int32_t cbx;             // B tile row width in elements (<= 128)
+  int32_t stage_tx;        // bytes of one full window tile
+  int32_t stage_stride;    // bytes between stages in shared memory
+  int32_t slice_rows;      // rows each CTA of the cluster loads (kWinRows / cluster)
+  int32_t cluster;         // CTAs per cluster (1, 2, 4 or 8)
+  int32_t vec_out;         // output rows are 16-byte aligned (d % 4 == 0, aligned base)
+};
+
+template <typename TB>
+__device__ __forceinline__ float4 load_tile4(const unsigned char* tile, int r, int cbx, int lane) {
+  if constexpr (sizeof(TB) == 4) {
+    return *reinterpret_cast<const float4*>(tile + ((size_t)r * cbx + 4 * lane) * 4);
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(tile + ((size_t)r * cbx + 4 * lane) * 2);
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
+  }
+}
+
+template <typename TB>
+__global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtensorMap map, const GatherArgs A) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * A.stage_stride);
+  uint64_t* empty = full + kStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int C = A.cluster;
+  const uint32_t rank = C > 1 ? cluster_ctarank() : 0;
+  const uint16_t mask = (uint16_t)((1u << C) - 1u);
+  const int c0 = blockIdx.x * kColsPerCta;
+  const int a0 = blockIdx.y * 8 * nwarps + 8 * warp;
+  const int w_begin = blockIdx.z * A.win_per_split;
+  const int w_end = min(A.n_win, w_begin + A.win_per_split);
+  const int nw = max(0, w_end - w_begin);
+  const bool lane_on = 4 * lane < A.cbx;
+  const bool warp_on = a0 < A.dp;
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&map);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], nwarps * C);
+    }
+    fence_mbar_init_cluster();
+  }
+  if (C > 1) cluster_sync(); else __syncthreads();
+
+  auto issue = [&](int it) {
+    const int s = it % kStages;
+    mbar_arrive_expect_tx(&full[s], (uint32_t)A.stage_tx);
+    unsigned char* dst = smem + (size_t)s * A.stage_stride + (size_t)rank * A.slice_rows * A.cbx * sizeof(TB);
+    const int y = (w_begin + it) * kWinRows + (int)rank * A.slice_rows;
+    if (C > 1) tma_load_2d_multicast(dst, &map, &full[s], c0, y, mask);
+    else tma_load_2d(dst, &map, &full[s], c0, y);
+  };
+
+  int issued = 0;
+  bool failed = false;
+  if (threadIdx.x == 0)
+    for (; issued < min(kStages, nw); ++issued) issue(issued);
+
+  float acc[8][4];
+#pragma unroll
+  for (int s = 0; s < 8; ++s)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[s][j] = 0.0f;
+
+  int it = 0;
+  for (; it < nw; ++it) {
+    const int s = it % kStages;
+    const uint32_t par = (uint32_t)(it / kStages) & 1u;
+    if (!mbar_wait(&full[s], par)) {
+      failed = true;
+      break;
+    }
+    const int w = w_begin + it;
+    if (warp_on) {
+      const int32_t* bp = A.wptr + (int64_t)w * A.dp + a0;
+      const int4 lo = *reinterpret_cast<const int4*>(bp);
+      const int4 hi = *reinterpret_cast<const int4*>(bp + 4);
+      const int bnd[9] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w, bp[8]};
+      const unsigned char* tile = smem + (size_t)s * A.stage_stride;
+      const int rbase = w * kWinRows;
+#pragma unroll
+      for (int sl = 0; sl < 8; ++sl) {
+        for (int e = bnd[sl]; e < bnd[sl + 1]; ++e) {
+          const int2 en = A.went[e];
+          const float v = __int_as_float(en.y);
+          if (lane_on) {
+            const float4 x = load_tile4<TB>(tile, en.x - rbase, A.cbx, lane);
+            acc[sl][0] = fmaf(v, x.x, acc[sl][0]);
+            acc[sl][1] = fmaf(v, x.y, acc[sl][1]);
+            acc[sl][2] = fmaf(v, x.z, acc[sl][2]);
+            acc[sl][3] = fmaf(v, x.w, acc[sl][3]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      if (C > 1) {
+        for (int r = 0; r < C; ++r) mbar_arrive_cluster(&empty[s], (uint32_t)r);
+      } else {
+        mbar_arrive_local(&empty[s]);
+      }
+    }
+    if (threadIdx.x == 0 && issued < nw && issued == it + kStages) {
+      if (!mbar_wait(&empty[s], par)) {
+        failed = true;
+        break;
+      }
+      issue(issued);
+      ++issued;
+    }
+  }
+  if (failed && threadIdx.x == 0) {
+    // drain the copies this CTA still expects (bounded), so none lands after exit
+    for (int j = it; j < issued; ++j) mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u);
+  }
+
+  // Y^T[col][a] for the lane's 4 columns and the warp's 8 outputs.
+  if (warp_on && lane_on && !failed) {
+    float* out = A.yt + (int64_t)blockIdx.z * A.split_stride;
+    const bool vec = A.vec_out && (a0 + 8 <= A.d);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = c0 + 4 * lane + j;
+      if (col >= A.ncols) continue;
+      float* o = out + (int64_t)col * A.d + a0;
+      if (vec) {
+        *reinterpret_cast<float4*>(o) = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+        *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
+      } else {
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl)
+          if (a0 + sl < A.d) o[sl] = acc[sl][j];
+      }
+    }
+  }
+  if (C > 1) cluster_sync();
+}
+
+// Generic gather for shapes the TMA path cannot take: one thread per output.
+template <typename TB>
+__global__ void k_gather_generic(const TB* __restrict__ B, int64_t ldb, int64_t ncols, int d,
+                                 const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ row_idx,
+                                 const float* __restrict__ csc_val, float* __restrict__ yt) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= ncols * d) return;
+  const int a = (int)(t % d);
+  const int64_t col = t / d;
+  float acc = 0.0f;
+  for (int e = col_ptr[a]; e < col_ptr[a + 1]; ++e) {
+    float b;
+    if constexpr (sizeof(TB) == 4) b = B[(int64_t)row_idx[e] * ldb + col];
+    else b = __bfloat162float(B[(int64_t)row_idx[e] * ldb + col]);
+    acc = fmaf(csc_val[e], b, acc);
+  }
+  yt[col * d + a] = acc;
+}
+
+// out[e] = sum over splits s = 0, 1, ... of part[s][e], in that order.
+__global__ void k_reduce_splits(const float* __restrict__ part, int splits, int64_t stride, int64_t n,
+                                float* __restrict__ out) {
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    float s = 0.0f;
+    for (int k = 0; k < splits; ++k) s += part[k * stride + e];
+    out[e] = s;
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Decompress kernels
+// ----------------------------------------------------------------------------
+
+// V[a][j] = sum_l q_{j,l} dS[a][c_{j,l}] for a in a 64-row block, j in 32-column tiles.
+__global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, const int32_t* __restrict__ qidx,
+                                           const float* __restrict__ qval, int k, int64_t n,
+                                           float* __restrict__ V, int tiles_per_warp) {
+  extern __shared__ float st[];      // st[c * 65 + aa] = dS[a0 + aa][c]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a0 = blockIdx.x * kVRows;
+  for (int aa = warp; aa < kVRows; aa += blockDim.x >> 5) {
+    const int a = a0 + aa;
+    for (int c = lane; c < d; c += 32) st[c * 65 + aa] = a < d ? dS[(int64_t)a * d + c] : 0.0f;
+  }
+  __syncthreads();
+  const int64_t n_tiles = (n + 31) / 32;
+  const bool vec = (n % 4) == 0 && (reinterpret_cast<uintptr_t>(V) % 16) == 0;
+  for (int q = 0; q < tiles_per_warp; ++q) {
+    const int64_t t = ((int64_t)blockIdx.y * (blockDim.x >> 5) + warp) * tiles_per_warp + q;
+    if (t >= n_tiles) break;
+    const int64_t j0 = t * 32;
+    float acc0[32], acc1[32];
+#pragma unroll
+    for (int jj = 0; jj < 32; ++jj) {
+      acc0[jj] = 0.0f;
+      acc1[jj] = 0.0f;
+      const int64_t j = j0 + jj;
+      if (j < n) {
+        for (int l = 0; l < k; ++l) {
+          const int c = qidx[j * k + l];
+          const float qv = qval[j * k + l];
+          acc0[jj] = fmaf(qv, st[c * 65 + lane], acc0[jj]);
+          acc1[jj] = fmaf(qv, st[c * 65 + lane + 32], acc1[jj]);
+        }
+      }
+    }
+    const bool full_tile = j0 + 32 <= n;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int a = a0 + lane + 32 * h;
+      if (a >= d) continue;
+      const float* acc = h ? acc1 : acc0;
+      float* o = V + (int64_t)a * n + j0;
+      if (vec && full_tile) {
+#pragma unroll
+        for (int jj = 0; jj < 32; jj += 4)
+          *reinterpret_cast<float4*>(o + jj) = make_float4(acc[jj], acc[jj + 1], acc[jj + 2], acc[jj + 3]);
+      } else {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj)
+          if (j0 + jj < n) o[jj] = acc[jj];
+      }
+    }
+  }
+}
+
+__global__ void k_v_generic(const float* __restrict__ dS, int d, const int32_t* __restrict__ qidx,
+                            const float* __restrict__ qval, int k, int64_t n, float* __restrict__ V) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (int64_t)d * n) return;
+  const int64_t j = t % n;
+  const int a = (int)(t / n);
+  float acc = 0.0f;
+  for (int l = 0; l < k; ++l) acc = fmaf(qval[j * k + l], dS[(int64_t)a * d + qidx[j * k + l]], acc);
+  V[(int64_t)a * n + j] = acc;
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  __nv_bfloat16 h = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+// W[i][j] -= sum_l p_{i,l} V[a_{i,l}][j]; persistent CTAs over (column block, row) work.
+template <bool kBf16W>
+__global__ void __launch_bounds__(512) k_apply(const float* __restrict__ V, int d, int64_t n, int64_t m,
+                                               const int32_t* __restrict__ pidx, const float* __restrict__ pval,
+                                               int k, void* __restrict__ W, uint16_t* __restrict__ mirror,
+                                               int64_t total_items, int64_t items_per_cta, int vec_ok) {
+  extern __shared__ float vs[];      // vs[a * 64 + jj] = V[a][j0 + jj]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  int64_t cur = (int64_t)blockIdx.x * items_per_cta;
+  const int64_t end = min(total_items, cur + items_per_cta);
+  constexpr int R = 4;
+  while (cur < end) {
+    const int64_t jb = cur / m;
+    const int64_t i_begin = cur % m;
+    const int64_t i_end = min(m, i_begin + (end - cur));
+    const int64_t j0 = jb * kApplyCols;
+    __syncthreads();
+    for (int e = threadIdx.x; e < d * kApplyCols; e += blockDim.x) {
+      const int a = e / kApplyCols, jj = e % kApplyCols;
+      vs[e] = (j0 + jj < n) ? V[(int64_t)a * n + j0 + jj] : 0.0f;
+    }
+    __syncthreads();
+    const int64_t j = j0 + 2 * lane;
+    const bool on0 = j < n, on1 = j + 1 < n;
+    const bool vec = vec_ok && on1;
+    for (int64_t ib = i_begin + (int64_t)warp * R; ib < i_end; ib += (int64_t)nwarps * R) {
+      float w0[R], w1[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int64_t i = ib + r;
+        w0[r] = w1[r] = 0.0f;
+        if (i >= i_end) continue;
+        const int64_t off = i * n + j;
+        if (kBf16W) {
+          const uint16_t* Wb = static_cast<const uint16_t*>(W);
+          if (vec) {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(Wb + off);
+            w0[r] = __uint_as_float(u << 16);
+            w1[r] = __uint_as_float(u & 0xFFFF0000u);
+          } else {
+            if (on0) w0[r] = __uint_as_float((uint32_t)Wb[off] << 16);
+            if (on1) w1[r] = __uint_as_float((uint32_t)Wb[off + 1] << 16);
+          }
+        } else {
+          const float* Wf = static_cast<const float*>(W);
+          if (vec) {
+            const float2 u = *reinterpret_cast<const float2*>(Wf + off);
+            w0[r] = u.x;
+            w1[r] = u.y;
+          } else {
+            if (on0) w0[r] = Wf[off];
+            if (on1) w1[r] = Wf[off + 1];
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int64_t i = ib + r;
+        if (i >= i_end) continue;
+        float s0 = 0.0f, s1 = 0.0f;
+        for (int l = 0; l < k; ++l) {
+          const int a = pidx[i * k + l];
+          const float p = pval[i * k + l];
+          const float2 v = *reinterpret_cast<const float2*>(vs + a * kApplyCols + 2 * lane);
+          s0 = fmaf(p, v.x, s0);
+          s1 = fmaf(p, v.y, s1);
+        }
+        const float n0 = w0[r] - s0, n1 = w1[r] - s1;
+        const int64_t off = i * n + j;
+        if (kBf16W) {
+          uint16_t* Wb = static_cast<uint16_t*>(W);
+          if (vec) {
+            *reinterpret_cast<uint32_t*>(Wb + off) = (uint32_t)f32_to_bf16_bits(n0) | ((uint32_t)f32_to_bf16_bits(n1) << 16);
+          } else {
+            if (on0) Wb[off] = f32_to_bf16_bits(n0);
+            if (on1) Wb[off + 1] = f32_to_bf16_bits(n1);
+          }
+        } else {
+          float* Wf = static_cast<float*>(W);
+          if (vec) {
+            *reinterpret_cast<float2*>(Wf + off) = make_float2(n0, n1);
+            if (mirror)
+              *reinterpret_cast<uint32_t*>(mirror + off) =
+                  (uint32_t)f32_to_bf16_bits(n0) | ((uint32_t)f32_to_bf16_bits(n1) << 16);
+          } else {
+            if (on0) {
+              Wf[off] = n0;
+              if (mirror) mirror[off] = f32_to_bf16_bits(n0);
+            }
+            if (on1) {
+              Wf[off + 1] = n1;
+              if (mirror) mirror[off + 1] = f32_to_bf16_bits(n1);
+            }
+          }
+        }
+      }
+    }
+    cur += i_end - i_begin;
+  }
+}
+
+template <bool kBf16W>
+__global__ void k_apply_generic(const float* __restrict__ V, int64_t n, int64_t m, const int32_t* __restrict__ pidx,
+                                const float* __restrict__ pval, int k, void* __restrict__ W,
+                                uint16_t* __restrict__ mirror) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= m * n) return;
+  const int64_t i = t / n, j = t % n;
+  float s = 0.0f;
+  for (int l = 0; l < k; ++l) s = fmaf(pval[i * k + l], V[(int64_t)pidx[i * k + l] * n + j], s);
+  if (kBf16W) {
+    uint16_t* Wb = static_cast<uint16_t*>(W);
+    Wb[t] = f32_to_bf16_bits(__uint_as_float((uint32_t)Wb[t] << 16) - s);
+  } else {
+    float* Wf = static_cast<float*>(W);
+    const float nv = Wf[t] - s;
+    Wf[t] = nv;
+    if (mirror) mirror[t] = f32_to_bf16_bits(nv);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Launch geometry of one gather (pure function of the sizes).
+struct GatherPlan {
+  int warps, n_ar, cluster, n_cb, n_win, splits, win_per_split;
+};
+
+GatherPlan plan_gather(int64_t rows, int64_t ncols, int d) {
+  GatherPlan p;
+  p.warps = std::min(16, (d + 7) / 8);
+  p.n_ar = (d + 8 * p.warps - 1) / (8 * p.warps);
+  p.cluster = (p.n_ar == 1 || p.n_ar == 2 || p.n_ar == 4 || p.n_ar == 8) ? p.n_ar : 1;
+  p.n_cb = (int)ceil_div<int64_t>(ncols, kColsPerCta);
+  p.n_win = (int)ceil_div<int64_t>(rows, kWinRows);
+  const int64_t base = (int64_t)p.n_cb * p.n_ar;
+  int splits = (int)std::max<int64_t>(1, std::min<int64_t>(p.n_win, kTargetCtas / std::max<int64_t>(1, base)));
+  p.win_per_split = (int)ceil_div<int64_t>(p.n_win, splits);
+  p.splits = (int)ceil_div<int64_t>(p.n_win, p.win_per_split);
+  return p;
+}
+
+struct CompressPlan {
+  GatherPlan g1, g2;
+  size_t off_rt, off_rtp, off_sp, bytes;
+};
+
+CompressPlan plan_compress(int64_t m, int64_t n, int d) {
+  CompressPlan c;
+  c.g1 = plan_gather(m, n, d);
+  c.g2 = plan_gather(n, d, d);
+  size_t off = 0;
+  c.off_rt = off;
+  off = align_up(off + (size_t)n * d * 4, 256);
+  c.off_rtp = off;
+  if (c.g1.splits > 1) off = align_up(off + (size_t)c.g1.splits * n * d * 4, 256);
+  c.off_sp = off;
+  if (c.g2.splits > 1) off = align_up(off + (size_t)c.g2.splits * d * d * 4, 256);
+  c.bytes = off;
+  return c;
+}
+
+size_t decompress_bytes(int64_t n, int d) { return align_up((size_t)d * n * 4, 256); }
+
+bool tma_ok(const void* B, int64_t ldb, size_t esize) {
+  return (reinterpret_cast<uintptr_t>(B) % 16) == 0 && (ldb * (int64_t)esize) % 16 == 0 &&
+         tensor_map_encoder() != nullptr;
+}
+
+template <typename TB>
+sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, int64_t ncols, const GatherPlan& p,
+                        float* yt_final, float* yt_partial, cudaStream_t stream) {
+  const int64_t rows = Aproj->rows;
+  const int d = Aproj->d;
+  const size_t es = sizeof(TB);
+  if (!tma_ok(B, ldb, es)) {
+    const int64_t total = ncols * d;
+    k_gather_generic<TB><<<(unsigned)ceil_div<int64_t>(total, 256), 256, 0, stream>>>(
+        B, ldb, ncols, d, Aproj->col_ptr, Aproj->row_idx, Aproj->csc_val, yt_final);
+    return check_launch("k_gather_generic");
+  }
+  const int align_elems = (int)(16 / es);
+  const int cbx = (int)std::min<int64_t>(kColsPerCta, ceil_div<int64_t>(ncols, align_elems) * align_elems);
+  GatherArgs A;
+  A.wptr = Aproj->wptr;
+  A.went = Aproj->went;
+  A.yt = p.splits > 1 ? yt_partial : yt_final;
+  A.split_stride = ncols * d;
+  A.ncols = (int32_t)ncols;
+  A.d = d;
+  A.dp = Aproj->dp;
+  A.n_win = p.n_win;
+  A.win_per_split = p.win_per_split;
+  A.cbx = cbx;
+  A.stage_tx = kWinRows * cbx * (int)es;
+  A.stage_stride = (int)align_up((size_t)A.stage_tx, 1024);
+  A.cluster = p.cluster;
+  A.slice_rows = kWinRows / p.cluster;
+  A.vec_out = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(A.yt) % 16 == 0) ? 1 : 0;
+
+  CUtensorMap map;
+  cuuint64_t dims[2] = {(cuuint64_t)ncols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ldb * (int64_t)es)};
+  cuuint32_t box[2] = {(cuuint32_t)cbx, (cuuint32_t)A.slice_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = tensor_map_encoder()(&map, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                    2, const_cast<TB*>(B), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+
+  const size_t smem = (size_t)kStages * A.stage_stride + 2 * kStages * sizeof(uint64_t) + 1024;
+  static thread_local size_t configured[2] = {0, 0};
+  const int slot = es == 4 ? 0 : 1;
+  if (configured[slot] < smem) {
+    SF_CUDA_TRY(cudaFuncSetAttribute(k_gather_t<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                "cudaFuncSetAttribute(k_gather_t)");
+    configured[slot] = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.n_cb, (unsigned)p.n_ar, (unsigned)p.splits);
+  cfg.blockDim = dim3(32 * p.warps);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = (unsigned)p.cluster;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gather_t<TB>, map, A), "launch k_gather_t");
+  if (p.splits > 1) {
+    const int64_t n_out = ncols * d;
+    const int blocks = (int)std::min<int64_t>(ceil_div<int64_t>(n_out, 256), (int64_t)sm_count() * 4);
+    k_reduce_splits<<<blocks, 256, 0, stream>>>(yt_partial, p.splits, n_out, n_out, yt_final);
+    return check_launch("k_reduce_splits");
+  }
+  return SF_OK;
+}
+
+sf_status check_proj(const lsp_projector_s* p, const char* name) {
+  if (!p) return fail(SF_ERR_INVALID, "projector %s is NULL", name);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev != p->device) return fail(SF_ERR_INVALID, "projector %s was built on device %d, current is %d", name,
+                                    p->device, dev);
+  return SF_OK;
+}
+
+}  // namespace
+
+// Host read-back of the device error word (used by sf_sync_status).
+int read_and_clear_device_error() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_device_error, &z, sizeof z);
+  return v;
+}
+
+}  // namespace sf
+
+using sf::ceil_div;
+using sf::fail;
 
 extern "C" {
-sf_status lsp_projector_create(int64_t, int32_t, int32_t, const int32_t*, const float*, int, void*,
-                               lsp_projector* out) {
-  if (out) *out = nullptr;
-  return sf::fail(SF_ERR_UNSUPPORTED, "not built yet");
+
+sf_status lsp_projector_create(int64_t rows, int32_t d, int32_t k, const int32_t* d_col_idx, const float* d_val,
+                               int validate, void* stream_, lsp_projector* out) {
+  sf::clear_error();
+  if (!out) return fail(SF_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  if (rows < 1 || d < 1 || d > 1024 || k < 1 || k > 64)
+    return fail(SF_ERR_INVALID, "need rows >= 1, 1 <= d <= 1024, 1 <= k <= 64 (got %lld, %d, %d)", (long long)rows,
+                d, k);
+  if (rows * (int64_t)k >= (int64_t)INT32_MAX) return fail(SF_ERR_UNSUPPORTED, "rows * k must be < 2^31");
+  if (!d_col_idx || !d_val) return fail(SF_ERR_INVALID, "ELL arrays are NULL");
+  cudaStream_t stream = sf::as_stream(stream_);
+  lsp_projector_s* p = new (std::nothrow) lsp_projector_s;
+  if (!p) return fail(SF_ERR_OOM, "projector allocation failed");
+  cudaGetDevice(&p->device);
+  p->rows = rows;
+  p->d = d;
+  p->k = k;
+  p->dp = (d + 7) / 8 * 8;
+  p->n_win = (int32_t)ceil_div<int64_t>(rows, sf::kWinRows);
+  const int64_t nnz = rows * k;
+  const int64_t nwd = (int64_t)p->n_win * p->dp;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = sf::align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t o_eidx = take(nnz * 4), o_eval = take(nnz * 4), o_cptr = take((d + 1) * 4), o_ridx = take(nnz * 4),
+               o_cval = take(nnz * 4), o_perm = take(d * 4), o_wptr = take((nwd + 1) * 4), o_went = take(nnz * 8),
+               o_wcnt = take(nwd * 4), o_coff = take(nwd * 4), o_tot = take(d * 4), o_err = take(4);
+  if (cudaMalloc(&p->block, off) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return fail(SF_ERR_OOM, "cudaMalloc of %zu bytes for the projector failed", off);
+  }
+  char* b = static_cast<char*>(p->block);
+  p->ell_idx = reinterpret_cast<int32_t*>(b + o_eidx);
+  p->ell_val = reinterpret_cast<float*>(b + o_eval);
+  p->col_ptr = reinterpret_cast<int32_t*>(b + o_cptr);
+  p->row_idx = reinterpret_cast<int32_t*>(b + o_ridx);
+  p->csc_val = reinterpret_cast<float*>(b + o_cval);
+  p->bucket_perm = reinterpret_cast<int32_t*>(b + o_perm);
+  p->wptr = reinterpret_cast<int32_t*>(b + o_wptr);
+  p->went = reinterpret_cast<int2*>(b + o_went);
+  p->wcnt = reinterpret_cast<int32_t*>(b + o_wcnt);
+  p->csc_off = reinterpret_cast<int32_t*>(b + o_coff);
+  p->totals = reinterpret_cast<int32_t*>(b + o_tot);
+  p->err = reinterpret_cast<int32_t*>(b + o_err);
+
+  auto bail = [&](sf_status st) {
+    cudaFree(p->block);
+    delete p;
+    return st;
+  };
+  if (cudaMemsetAsync(p->err, 0, 4, stream) != cudaSuccess) return bail(sf::cuda_fail(cudaGetLastError(), "memset"));
+  const int nsm = sf::sm_count();
+  sf::k_copy_ell<<<(unsigned)std::min<int64_t>(ceil_div<int64_t>(nnz, 256), nsm * 8), 256, 0, stream>>>(
+      d_col_idx, d_val, nnz, d, p->ell_idx, p->ell_val);
+  if (validate)
+    sf::k_validate_rows<<<(unsigned)ceil_div<int64_t>(rows, 256), 256, 0, stream>>>(d_col_idx, rows, k, d, p->err);
+  sf::k_window_hist<<<p->n_win, 256, p->dp * 4, stream>>>(d_col_idx, rows, k, d, p->dp, p->wcnt, p->err);
+  sf::k_column_offsets<<<(unsigned)ceil_div(d, 128), 128, 0, stream>>>(p->wcnt, p->n_win, d, p->dp, p->csc_off,
+                                                                      p->totals);
+  sf::k_scan_exclusive<<<1, 1024, 0, stream>>>(p->totals, d, p->col_ptr);
+  sf::k_scan_exclusive<<<1, 1024, 0, stream>>>(p->wcnt, nwd, p->wptr);
+  const int wpb = 4;
+  sf::k_place<<<(unsigned)ceil_div(p->n_win, wpb), 32 * wpb, wpb * p->dp * 4, stream>>>(
+      d_col_idx, d_val, rows, k, d, p->dp, p->n_win, p->wptr, p->csc_off, p->col_ptr, p->went, p->row_idx,
+      p->csc_val);
+  sf::k_bucket_perm<<<1, 1024, 0, stream>>>(p->col_ptr, d, p->bucket_perm);
+  sf_status st = sf::check_launch("projector build");
+  if (st != SF_OK) return bail(st);
+  if (validate) {
+    st = sf::bounded_wait_stream(stream, 0, "lsp_projector_create");
+    if (st != SF_OK) return bail(st);
+    int32_t err = 0;
+    if (cudaMemcpy(&err, p->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+      return bail(sf::cuda_fail(cudaGetLastError(), "read validation flag"));
+    if (err & sf::kDevErrIndex) return bail(fail(SF_ERR_INVALID, "projector has a column id outside [0, %d)", d));
+    if (err & 4) return bail(fail(SF_ERR_INVALID, "projector repeats a column id inside a row"));
+  }
+  *out = p;
+  return SF_OK;
 }
-sf_status lsp_projector_export_csc(lsp_projector, int32_t*, int32_t*, float*, int32_t*, void*) {
-  return sf::fail(SF_ERR_UNSUPPORTED, "not built yet");
+
+sf_status lsp_projector_export_csc(lsp_projector p, int32_t* col_ptr, int32_t* row_idx, float* val,
+                                   int32_t* bucket_perm, void* stream_) {
+  sf::clear_error();
+  SF_TRY(sf::check_proj(p, "P"));
+  cudaStream_t s = sf::as_stream(stream_);
+  const size_t nnz = (size_t)p->rows * p->k;
+  if (col_ptr) SF_CUDA_TRY(cudaMemcpyAsync(col_ptr, p->col_ptr, (p->d + 1) * 4, cudaMemcpyDeviceToDevice, s), "export");
+  if (row_idx) SF_CUDA_TRY(cudaMemcpyAsync(row_idx, p->row_idx, nnz * 4, cudaMemcpyDeviceToDevice, s), "export");
+  if (val) SF_CUDA_TRY(cudaMemcpyAsync(val, p->csc_val, nnz * 4, cudaMemcpyDeviceToDevice, s), "export");
+  if (bucket_perm) SF_CUDA_TRY(cudaMemcpyAsync(bucket_perm, p->bucket_perm, p->d * 4, cudaMemcpyDeviceToDevice, s), "export");
+  return SF_OK;
 }
+
 int64_t lsp_projector_rows(lsp_projector p) { return p ? p->rows : -1; }
 int32_t lsp_projector_dim(lsp_projector p) { return p ? p->d : -1; }
 int32_t lsp_projector_nnz_per_row(lsp_projector p) { return p ? p->k : -1; }
-sf_status lsp_projector_destroy(lsp_projector p) { delete p; return SF_OK; }
-size_t lsp_workspace_bytes(int64_t, int64_t, int32_t) { return 0; }
-sf_status lsp_compress(lsp_projector, lsp_projector, const void*, sf_dtype, int64_t, int64_t, float*,
-                       void*, size_t, void*) {
-  return sf::fail(SF_ERR_UNSUPPORTED, "not built yet");
+
+sf_status lsp_projector_destroy(lsp_projector p) {
+  sf::clear_error();
+  if (!p) return SF_OK;
+  cudaError_t e = cudaFree(p->block);
+  delete p;
+  return e == cudaSuccess ? SF_OK : sf::cuda_fail(e, "cudaFree(projector)");
 }
-sf_status lsp_decompress_apply(lsp_projector, lsp_projector, const float*, void*, sf_dtype, void*,
-                               int64_t, int64_t, void*, size_t, void*) {
-  return sf::fail(SF_ERR_UNSUPPORTED, "not built yet");
+
+size_t lsp_workspace_bytes(int64_t m, int64_t n, int32_t d) {
+  if (m < 1 || n < 1 || d < 1) return 0;
+  return std::max(sf::plan_compress(m, n, d).bytes, sf::decompress_bytes(n, d));
 }
+
+sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G, sf_dtype g_dtype, int64_t m, int64_t n,
+                       float* S, void* ws, size_t ws_bytes, void* stream_) {
+  sf::clear_error();
+  SF_TRY(sf::check_proj(P, "P"));
+  SF_TRY(sf::check_proj(Q, "Q"));
+  if (!G || !S) return fail(SF_ERR_INVALID, "G or S is NULL");
+  if (P->rows != m || Q->rows != n)
+    return fail(SF_ERR_INVALID, "P has %lld rows, Q %lld: need m = %lld, n = %lld", (long long)P->rows,
+                (long long)Q->rows, (long long)m, (long long)n);
+  if (P->d != Q->d) return fail(SF_ERR_INVALID, "P and Q differ in d (%d vs %d)", P->d, Q->d);
+  if (g_dtype != SF_BF16 && g_dtype != SF_FP32) return fail(SF_ERR_INVALID, "g_dtype must be SF_BF16 or SF_FP32");
+  const int d = P->d;
+  const sf::CompressPlan cp = sf::plan_compress(m, n, d);
+  if (!ws || ws_bytes < cp.bytes || (reinterpret_cast<uintptr_t>(ws) % 256) != 0)
+    return fail(SF_ERR_INVALID, "workspace needs %zu bytes, 256-byte aligned (got %zu)", cp.bytes, ws_bytes);
+  cudaStream_t s = sf::as_stream(stream_);
+  char* w = static_cast<char*>(ws);
+  float* rt = reinterpret_cast<float*>(w + cp.off_rt);
+  float* rtp = reinterpret_cast<float*>(w + cp.off_rtp);
+  float* sp = reinterpret_cast<float*>(w + cp.off_sp);
+  if (g_dtype == SF_FP32)
+    SF_TRY(sf::launch_gather<float>(P, static_cast<const float*>(G), n, n, cp.g1, rt, rtp, s));
+  else
+    SF_TRY(sf::launch_gather<__nv_bfloat16>(P, static_cast<const __nv_bfloat16*>(G), n, n, cp.g1, rt, rtp, s));
+  return sf::launch_gather<float>(Q, rt, d, d, cp.g2, S, sp, s);
 }
+
+sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS, void* W, sf_dtype w_dtype,
+                               void* w_bf16_mirror, int64_t m, int64_t n, void* ws, size_t ws_bytes, void* stream_) {
+  sf::clear_error();
+  SF_TRY(sf::check_proj(P, "P"));
+  SF_TRY(sf::check_proj(Q, "Q"));
+  if (!dS || !W) return fail(SF_ERR_INVALID, "dS or W is NULL");
+  if (P->rows != m || Q->rows != n)
+    return fail(SF_ERR_INVALID, "P has %lld rows, Q %lld: need m = %lld, n = %lld", (long long)P->rows,
+                (long long)Q->rows, (long long)m, (long long)n);
+  if (P->d != Q->d) return fail(SF_ERR_INVALID, "P and Q differ in d (%d vs %d)", P->d, Q->d);
+  if (w_dtype != SF_BF16 && w_dtype != SF_FP32) return fail(SF_ERR_INVALID, "w_dtype must be SF_BF16 or SF_FP32");
+  if (w_bf16_mirror && w_dtype != SF_FP32) return fail(SF_ERR_INVALID, "a bf16 mirror needs an fp32 W");
+  const int d = P->d;
+  const size_t need = sf::decompress_bytes(n, d);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 256) != 0)
+    return fail(SF_ERR_INVALID, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  cudaStream_t s = sf::as_stream(stream_);
+  float* V = static_cast<float*>(ws);
+  const int nsm = sf::sm_count();
+  uint16_t* mirror = static_cast<uint16_t*>(w_bf16_mirror);
+  if (d <= sf::kMaxFastD) {
+    const int n_ab = (int)ceil_div(d, sf::kVRows);
+    const int64_t n_tiles = ceil_div<int64_t>(n, 32);
+    const int warps = 8;
+    const int tpw = (int)std::max<int64_t>(1, (int64_t)n_ab * n_tiles / ((int64_t)warps * sf::kTargetCtas));
+    const int64_t gy = ceil_div<int64_t>(n_tiles, (int64_t)warps * tpw);
+    const size_t smem_v = (size_t)d * 65 * 4;
+    static thread_local bool v_cfg = false;
+    if (!v_cfg) {
+      SF_CUDA_TRY(cudaFuncSetAttribute(sf::k_v, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)((size_t)sf::kMaxFastD * 65 * 4)),
+                  "cudaFuncSetAttribute(k_v)");
+      v_cfg = true;
+    }
+    sf::k_v<<<dim3((unsigned)n_ab, (unsigned)gy), 32 * warps, smem_v, s>>>(dS, d, Q->ell_idx, Q->ell_val, Q->k, n, V,
+                                                                          tpw);
+    SF_TRY(sf::check_launch("k_v"));
+
+    const size_t smem_a = (size_t)d * sf::kApplyCols * 4;
+    const int64_t n_jb = ceil_div<int64_t>(n, sf::kApplyCols);
+    const int64_t total = n_jb * m;
+    const bool bf16w = w_dtype == SF_BF16;
+    auto kern = bf16w ? sf::k_apply<true> : sf::k_apply<false>;
+    static thread_local bool a_cfg[2] = {false, false};
+    if (!a_cfg[bf16w]) {
+      SF_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)((size_t)sf::kMaxFastD * sf::kApplyCols * 4)),
+                  "cudaFuncSetAttribute(k_apply)");
+      a_cfg[bf16w] = true;
+    }
+    int occ = 1;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 512, smem_a);
+    occ = std::max(1, occ);
+    const int64_t grid = std::min<int64_t>((int64_t)nsm * occ, ceil_div<int64_t>(total, 16));
+    const int64_t ipc = ceil_div<int64_t>(total, grid);
+    const size_t wb = bf16w ? 2 : 4;
+    const int vec_ok = (n % 2 == 0) && (reinterpret_cast<uintptr_t>(W) % (2 * wb) == 0) &&
+                       (!mirror || reinterpret_cast<uintptr_t>(mirror) % 4 == 0);
+    kern<<<(unsigned)ceil_div<int64_t>(total, ipc), 512, smem_a, s>>>(V, d, n, m, P->ell_idx, P->ell_val, P->k, W,
+                                                                       mirror, total, ipc, vec_ok);
+    return sf::check_launch("k_apply");
+  }
+  const int64_t nv = (int64_t)d * n;
+  sf::k_v_generic<<<(unsigned)ceil_div<int64_t>(nv, 256), 256, 0, s>>>(dS, d, Q->ell_idx, Q->ell_val, Q->k, n, V);
+  SF_TRY(sf::check_launch("k_v_generic"));
+  const int64_t nw = m * n;
+  if (w_dtype == SF_BF16)
+    sf::k_apply_generic<true><<<(unsigned)ceil_div<int64_t>(nw, 256), 256, 0, s>>>(V, n, m, P->ell_idx, P->ell_val,
+                                                                                   P->k, W, nullptr);
+  else
+    sf::k_apply_generic<false><<<(unsigned)ceil_div<int64_t>(nw, 256), 256, 0, s>>>(V, n, m, P->ell_idx, P->ell_val,
+                                                                                    P->k, W, mirror);
+  return sf::check_launch("k_apply_generic");
+}
+
+}  // extern "C"
