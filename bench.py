@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=24, help="OPT-1.3B layers (24 = the full stack)")
     ap.add_argument("--profile-small", action="store_true",
                     help="1 layer, 1 warm-up + 1 timed step, no extras: a small case for ncu captures")
+    ap.add_argument("--profile-lsp", action="store_true",
+                    help="only the projector chain on one 4096 x 4096 matrix, 1 warm-up + 1 timed rep (ncu case)")
     return ap.parse_args()
 
 
@@ -317,16 +319,15 @@ def run_e2e(args, world):
     return dict(wall_s=wall, params_per_step=params, h2d=14 * params, d2h=14 * params)
 
 
-def run_lsp(args):
+def run_lsp(args, matrices=None):
     """Compress -> compressed AdamW -> decompress-apply on the LLaMA-7B matrices."""
-    import numpy as np
     import torch
 
     from layer_optimizer_gb300 import native, synth
     d, k = 512, 8
     hp = native.hparams(**HP)
     mats = []
-    for mi, (name, m, n) in enumerate(synth.LLAMA7_LSP_MATRICES):
+    for mi, (name, m, n) in enumerate(matrices or synth.LLAMA7_LSP_MATRICES):
         Pi, Pv = synth.projector(m, d, k, synth.sub_seed(7, mi, 0))
         Qi, Qv = synth.projector(n, d, k, synth.sub_seed(7, mi, 1))
         P = native.lsp_projector_create(m, d, k, torch.from_numpy(Pi).cuda(), torch.from_numpy(Pv).cuda())
@@ -339,7 +340,7 @@ def run_lsp(args):
         mats.append((name, m, n, P, Q, G, W, st, ws, wsb))
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    reps = max(3, args.steps // 2)
+    reps = 1 if args.profile_lsp else max(3, args.steps // 2)
     times = {"compress": [], "adamw_c": [], "decompress": []}
     per = []
     for it in range(args.warmup + reps):
@@ -474,6 +475,13 @@ def main():
     if args.profile_small:
         args.layers, args.steps, args.warmup = 1, 1, 1
         args.no_e2e = args.no_lsp = args.no_cpu = True
+    if args.profile_lsp:
+        import torch
+        from layer_optimizer_gb300 import native
+        native.load()
+        args.warmup = 1
+        print(json.dumps({"profile_lsp": run_lsp(args, matrices=[("q", 4096, 4096)])}))
+        return
     rank, world = dist_init(args)
     if args.impl == "reference":
         main_reference(args, rank, world)

@@ -76,10 +76,13 @@ struct lsp_projector_s {
   int32_t* bucket_perm = nullptr;  // [d]
   int32_t* wptr = nullptr;      // [n_win*dp + 1]: start of (window, a) in went
   int2* went = nullptr;         // [rows*k]: (row, value bits), sorted by (window, a, row)
+  int2* gdesc = nullptr;        // [n_ar][n_win]: (first entry rounded down to even, bytes) of a CTA's slice
+  int32_t a_rng = 0, n_ar = 0;  // outputs per gather CTA (8 x warps) and number of such ranges
+  int32_t max_slice_bytes = 0;  // largest gdesc byte count
   int32_t* wcnt = nullptr;      // [n_win*dp] scratch of the build
   int32_t* csc_off = nullptr;   // [n_win*dp] scratch of the build
   int32_t* totals = nullptr;    // [d] scratch of the build
-  int32_t* err = nullptr;       // [1]
+  int32_t* err = nullptr;       // [2]: error bits, largest slice bytes
   void* block = nullptr;
 };
 
@@ -257,6 +260,21 @@ __global__ void k_copy_ell(const int32_t* __restrict__ idx, const float* __restr
   }
 }
 
+// Per (a-range, window): the slice of the window-major list that one gather
+// CTA needs, as a 16-byte aligned (first entry, byte count) pair for a bulk copy.
+__global__ void k_gdesc(const int32_t* __restrict__ wptr, int n_win, int dp, int a_rng, int n_ar,
+                        int2* __restrict__ gdesc, int32_t* __restrict__ max_bytes) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (int64_t)n_win * n_ar) return;
+  const int w = (int)(t % n_win), ar = (int)(t / n_win);
+  const int lo = ar * a_rng, hi = min(lo + a_rng, dp);
+  const int32_t e0 = wptr[(int64_t)w * dp + lo], e1 = wptr[(int64_t)w * dp + hi];
+  const int32_t e0a = e0 & ~1;
+  const int32_t bytes = ((e1 - e0a) * 8 + 15) / 16 * 16;
+  gdesc[t] = make_int2(e0a, bytes);
+  atomicMax(max_bytes, bytes);
+}
+
 // ----------------------------------------------------------------------------
 // Gather kernel: Y^T = (A^T B)^T with TMA-staged windows of B
 // ----------------------------------------------------------------------------
@@ -264,6 +282,7 @@ __global__ void k_copy_ell(const int32_t* __restrict__ idx, const float* __restr
 struct GatherArgs {
   const int32_t* wptr;
   const int2* went;
+  const int2* gdesc;
   float* yt;               // [split][ncols][d]
   int64_t split_stride;    // elements between split outputs
   int32_t ncols;           // columns of B
@@ -272,6 +291,9 @@ struct GatherArgs {
   int32_t win_per_split;
   int32_t cbx;             // B tile row width in elements (<= 128)
   int32_t stage_tx;        // bytes of one full window tile
+  int32_t wsl_off;         // offset of the staged prefix-table slice inside a stage
+  int32_t wbytes;          // its bytes (8 x warps + 1 ints, padded to 16)
+  int32_t ent_off;         // offset of the staged entry slice inside a stage
   int32_t stage_stride;    // bytes between stages in shared memory
   int32_t slice_rows;      // rows each CTA of the cluster loads (kWinRows / cluster)
   int32_t cluster;         // CTAs per cluster (1, 2, 4 or 8)
@@ -295,6 +317,7 @@ __global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtens
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * A.stage_stride);
   uint64_t* empty = full + kStages;
+  int32_t* hdr = reinterpret_cast<int32_t*>(empty + kStages);   // first staged entry of each stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
@@ -302,7 +325,8 @@ __global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtens
   const uint32_t rank = C > 1 ? cluster_ctarank() : 0;
   const uint16_t mask = (uint16_t)((1u << C) - 1u);
   const int c0 = blockIdx.x * kColsPerCta;
-  const int a0 = blockIdx.y * 8 * nwarps + 8 * warp;
+  const int a_cta = blockIdx.y * 8 * nwarps;
+  const int a0 = a_cta + 8 * warp;
   const int w_begin = blockIdx.z * A.win_per_split;
   const int w_end = min(A.n_win, w_begin + A.win_per_split);
   const int nw = max(0, w_end - w_begin);
@@ -319,19 +343,30 @@ __global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtens
   }
   if (C > 1) cluster_sync(); else __syncthreads();
 
-  auto issue = [&](int it) {
+  // One stage = the B tile of a window (rows split over the cluster and
+  // multicast), this CTA's slice of the prefix table and its entry slice.
+  const int2* gd_row = A.gdesc + (int64_t)blockIdx.y * A.n_win;
+  auto issue = [&](int it, int2 gd) {
     const int s = it % kStages;
-    mbar_arrive_expect_tx(&full[s], (uint32_t)A.stage_tx);
-    unsigned char* dst = smem + (size_t)s * A.stage_stride + (size_t)rank * A.slice_rows * A.cbx * sizeof(TB);
-    const int y = (w_begin + it) * kWinRows + (int)rank * A.slice_rows;
+    const int w = w_begin + it;
+    unsigned char* st = smem + (size_t)s * A.stage_stride;
+    hdr[s] = gd.x;
+    mbar_arrive_expect_tx(&full[s], (uint32_t)(A.stage_tx + A.wbytes + gd.y));
+    unsigned char* dst = st + (size_t)rank * A.slice_rows * A.cbx * sizeof(TB);
+    const int y = w * kWinRows + (int)rank * A.slice_rows;
     if (C > 1) tma_load_2d_multicast(dst, &map, &full[s], c0, y, mask);
     else tma_load_2d(dst, &map, &full[s], c0, y);
+    bulk_load(st + A.wsl_off, A.wptr + (int64_t)w * A.dp + a_cta, (uint32_t)A.wbytes, &full[s]);
+    if (gd.y > 0) bulk_load(st + A.ent_off, A.went + gd.x, (uint32_t)gd.y, &full[s]);
   };
 
   int issued = 0;
   bool failed = false;
-  if (threadIdx.x == 0)
-    for (; issued < min(kStages, nw); ++issued) issue(issued);
+  int2 gd_next = make_int2(0, 0);
+  if (threadIdx.x == 0) {
+    for (; issued < min(kStages, nw); ++issued) issue(issued, gd_row[w_begin + issued]);
+    if (issued < nw) gd_next = gd_row[w_begin + issued];
+  }
 
   float acc[8][4];
 #pragma unroll
@@ -349,16 +384,19 @@ __global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtens
     }
     const int w = w_begin + it;
     if (warp_on) {
-      const int32_t* bp = A.wptr + (int64_t)w * A.dp + a0;
+      const unsigned char* tile = smem + (size_t)s * A.stage_stride;
+      const int32_t* bp = reinterpret_cast<const int32_t*>(tile + A.wsl_off) + 8 * warp;
       const int4 lo = *reinterpret_cast<const int4*>(bp);
       const int4 hi = *reinterpret_cast<const int4*>(bp + 4);
-      const int bnd[9] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w, bp[8]};
-      const unsigned char* tile = smem + (size_t)s * A.stage_stride;
+      const int32_t e_base = hdr[s];
+      const int bnd[9] = {lo.x - e_base, lo.y - e_base, lo.z - e_base, lo.w - e_base, hi.x - e_base,
+                          hi.y - e_base, hi.z - e_base, hi.w - e_base, bp[8] - e_base};
+      const int2* ent = reinterpret_cast<const int2*>(tile + A.ent_off);
       const int rbase = w * kWinRows;
 #pragma unroll
       for (int sl = 0; sl < 8; ++sl) {
         for (int e = bnd[sl]; e < bnd[sl + 1]; ++e) {
-          const int2 en = A.went[e];
+          const int2 en = ent[e];
           const float v = __int_as_float(en.y);
           if (lane_on) {
             const float4 x = load_tile4<TB>(tile, en.x - rbase, A.cbx, lane);
@@ -383,8 +421,9 @@ __global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtens
         failed = true;
         break;
       }
-      issue(issued);
+      issue(issued, gd_next);
       ++issued;
+      if (issued < nw) gd_next = gd_row[w_begin + issued];
     }
   }
   if (failed && threadIdx.x == 0) {
@@ -448,13 +487,18 @@ __global__ void k_reduce_splits(const float* __restrict__ part, int splits, int6
 // ----------------------------------------------------------------------------
 
 // V[a][j] = sum_l q_{j,l} dS[a][c_{j,l}] for a in a 64-row block, j in 32-column tiles.
+// dS^T of the block sits in shared memory (st[c * 65 + aa], padded: the
+// transposing fill and the lane-along-a reads are both conflict-free); the
+// k entries of the tile's 32 Q rows are fetched with coalesced loads into a
+// per-warp buffer and read back as warp-uniform broadcasts.
 __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, const int32_t* __restrict__ qidx,
                                            const float* __restrict__ qval, int k, int64_t n,
                                            float* __restrict__ V, int tiles_per_warp) {
-  extern __shared__ float st[];      // st[c * 65 + aa] = dS[a0 + aa][c]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  extern __shared__ float st[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  int2* ebuf = reinterpret_cast<int2*>(st + (size_t)d * 65) + (size_t)warp * 32 * k;
   const int a0 = blockIdx.x * kVRows;
-  for (int aa = warp; aa < kVRows; aa += blockDim.x >> 5) {
+  for (int aa = warp; aa < kVRows; aa += nwarps) {
     const int a = a0 + aa;
     for (int c = lane; c < d; c += 32) st[c * 65 + aa] = a < d ? dS[(int64_t)a * d + c] : 0.0f;
   }
@@ -462,25 +506,30 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
   const int64_t n_tiles = (n + 31) / 32;
   const bool vec = (n % 4) == 0 && (reinterpret_cast<uintptr_t>(V) % 16) == 0;
   for (int q = 0; q < tiles_per_warp; ++q) {
-    const int64_t t = ((int64_t)blockIdx.y * (blockDim.x >> 5) + warp) * tiles_per_warp + q;
+    const int64_t t = ((int64_t)blockIdx.y * nwarps + warp) * tiles_per_warp + q;
     if (t >= n_tiles) break;
     const int64_t j0 = t * 32;
+    const int rows_here = (int)(n - j0 < 32 ? n - j0 : 32);
+    const int ne = rows_here * k;
+    __syncwarp();
+    for (int e = lane; e < ne; e += 32)
+      ebuf[e] = make_int2(qidx[j0 * k + e], __float_as_int(qval[j0 * k + e]));
+    __syncwarp();
     float acc0[32], acc1[32];
 #pragma unroll
     for (int jj = 0; jj < 32; ++jj) {
       acc0[jj] = 0.0f;
       acc1[jj] = 0.0f;
-      const int64_t j = j0 + jj;
-      if (j < n) {
+      if (jj < rows_here) {
         for (int l = 0; l < k; ++l) {
-          const int c = qidx[j * k + l];
-          const float qv = qval[j * k + l];
-          acc0[jj] = fmaf(qv, st[c * 65 + lane], acc0[jj]);
-          acc1[jj] = fmaf(qv, st[c * 65 + lane + 32], acc1[jj]);
+          const int2 en = ebuf[jj * k + l];
+          const float qv = __int_as_float(en.y);
+          acc0[jj] = fmaf(qv, st[en.x * 65 + lane], acc0[jj]);
+          acc1[jj] = fmaf(qv, st[en.x * 65 + lane + 32], acc1[jj]);
         }
       }
     }
-    const bool full_tile = j0 + 32 <= n;
+    const bool full_tile = rows_here == 32;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int a = a0 + lane + 32 * h;
@@ -494,7 +543,7 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
       } else {
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj)
-          if (j0 + jj < n) o[jj] = acc[jj];
+          if (jj < rows_here) o[jj] = acc[jj];
       }
     }
   }
@@ -517,16 +566,24 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
 }
 
 // W[i][j] -= sum_l p_{i,l} V[a_{i,l}][j]; persistent CTAs over (column block, row) work.
+// A 64-column block of V sits in shared memory (vs[a * 64 + jj]); each warp
+// takes groups of R rows whose R*k <= 32 projector entries are fetched with
+// one coalesced load per lane, one group ahead, staged in a per-warp buffer
+// and read back as warp-uniform broadcasts.  W is read and written once,
+// two columns per lane.
+constexpr int kApplyMaxR = 8;
+
 template <bool kBf16W>
 __global__ void __launch_bounds__(512) k_apply(const float* __restrict__ V, int d, int64_t n, int64_t m,
                                                const int32_t* __restrict__ pidx, const float* __restrict__ pval,
-                                               int k, void* __restrict__ W, uint16_t* __restrict__ mirror,
+                                               int k, int R, void* __restrict__ W, uint16_t* __restrict__ mirror,
                                                int64_t total_items, int64_t items_per_cta, int vec_ok) {
-  extern __shared__ float vs[];      // vs[a * 64 + jj] = V[a][j0 + jj]
+  extern __shared__ float vs[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
+  int2* ebuf = reinterpret_cast<int2*>(vs + (size_t)d * kApplyCols) + warp * 32;
   int64_t cur = (int64_t)blockIdx.x * items_per_cta;
   const int64_t end = min(total_items, cur + items_per_cta);
-  constexpr int R = 4;
+  const int ne = R * k;
   while (cur < end) {
     const int64_t jb = cur / m;
     const int64_t i_begin = cur % m;
@@ -541,13 +598,25 @@ __global__ void __launch_bounds__(512) k_apply(const float* __restrict__ V, int 
     const int64_t j = j0 + 2 * lane;
     const bool on0 = j < n, on1 = j + 1 < n;
     const bool vec = vec_ok && on1;
-    for (int64_t ib = i_begin + (int64_t)warp * R; ib < i_end; ib += (int64_t)nwarps * R) {
-      float w0[R], w1[R];
+    int64_t ib = i_begin + (int64_t)warp * R;
+    const int64_t stride = (int64_t)nwarps * R;
+    // entries of the first group
+    int2 pre = make_int2(0, 0);
+    if (ib < i_end && lane < ne && ib + lane / k < i_end)
+      pre = make_int2(pidx[ib * k + lane], __float_as_int(pval[ib * k + lane]));
+    for (; ib < i_end; ib += stride) {
+      __syncwarp();
+      ebuf[lane] = pre;
+      __syncwarp();
+      const int64_t nb = ib + stride;
+      if (nb < i_end && lane < ne && nb + lane / k < i_end)
+        pre = make_int2(pidx[nb * k + lane], __float_as_int(pval[nb * k + lane]));
+      float w0[kApplyMaxR], w1[kApplyMaxR];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
+      for (int r = 0; r < kApplyMaxR; ++r) {
         const int64_t i = ib + r;
         w0[r] = w1[r] = 0.0f;
-        if (i >= i_end) continue;
+        if (r >= R || i >= i_end) continue;
         const int64_t off = i * n + j;
         if (kBf16W) {
           const uint16_t* Wb = static_cast<const uint16_t*>(W);
@@ -572,14 +641,14 @@ __global__ void __launch_bounds__(512) k_apply(const float* __restrict__ V, int 
         }
       }
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
+      for (int r = 0; r < kApplyMaxR; ++r) {
         const int64_t i = ib + r;
-        if (i >= i_end) continue;
+        if (r >= R || i >= i_end) continue;
         float s0 = 0.0f, s1 = 0.0f;
         for (int l = 0; l < k; ++l) {
-          const int a = pidx[i * k + l];
-          const float p = pval[i * k + l];
-          const float2 v = *reinterpret_cast<const float2*>(vs + a * kApplyCols + 2 * lane);
+          const int2 en = ebuf[r * k + l];
+          const float p = __int_as_float(en.y);
+          const float2 v = *reinterpret_cast<const float2*>(vs + en.x * kApplyCols + 2 * lane);
           s0 = fmaf(p, v.x, s0);
           s1 = fmaf(p, v.y, s1);
         }
@@ -588,7 +657,8 @@ __global__ void __launch_bounds__(512) k_apply(const float* __restrict__ V, int 
         if (kBf16W) {
           uint16_t* Wb = static_cast<uint16_t*>(W);
           if (vec) {
-            *reinterpret_cast<uint32_t*>(Wb + off) = (uint32_t)f32_to_bf16_bits(n0) | ((uint32_t)f32_to_bf16_bits(n1) << 16);
+            *reinterpret_cast<uint32_t*>(Wb + off) =
+                (uint32_t)f32_to_bf16_bits(n0) | ((uint32_t)f32_to_bf16_bits(n1) << 16);
           } else {
             if (on0) Wb[off] = f32_to_bf16_bits(n0);
             if (on1) Wb[off + 1] = f32_to_bf16_bits(n1);
@@ -695,6 +765,14 @@ CompressPlan plan_compress(int64_t m, int64_t n, int d) {
 
 size_t decompress_bytes(int64_t n, int d) { return align_up((size_t)d * n * 4, 256); }
 
+constexpr size_t kMaxGatherSmem = 220 * 1024;
+
+size_t gather_smem_estimate(const lsp_projector_s* Ap, size_t es) {
+  const size_t tile = (size_t)kWinRows * kColsPerCta * es;
+  const size_t per = align_up(align_up(tile, 128) + 16 * 40 + (size_t)Ap->max_slice_bytes, 1024);
+  return kStages * per + 2048;
+}
+
 bool tma_ok(const void* B, int64_t ldb, size_t esize) {
   return (reinterpret_cast<uintptr_t>(B) % 16) == 0 && (ldb * (int64_t)esize) % 16 == 0 &&
          tensor_map_encoder() != nullptr;
@@ -706,7 +784,7 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   const int64_t rows = Aproj->rows;
   const int d = Aproj->d;
   const size_t es = sizeof(TB);
-  if (!tma_ok(B, ldb, es)) {
+  if (!tma_ok(B, ldb, es) || Aproj->a_rng != 8 * p.warps || gather_smem_estimate(Aproj, es) > kMaxGatherSmem) {
     const int64_t total = ncols * d;
     k_gather_generic<TB><<<(unsigned)ceil_div<int64_t>(total, 256), 256, 0, stream>>>(
         B, ldb, ncols, d, Aproj->col_ptr, Aproj->row_idx, Aproj->csc_val, yt_final);
@@ -717,6 +795,7 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   GatherArgs A;
   A.wptr = Aproj->wptr;
   A.went = Aproj->went;
+  A.gdesc = Aproj->gdesc;
   A.yt = p.splits > 1 ? yt_partial : yt_final;
   A.split_stride = ncols * d;
   A.ncols = (int32_t)ncols;
@@ -726,7 +805,10 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   A.win_per_split = p.win_per_split;
   A.cbx = cbx;
   A.stage_tx = kWinRows * cbx * (int)es;
-  A.stage_stride = (int)align_up((size_t)A.stage_tx, 1024);
+  A.wsl_off = (int)align_up((size_t)A.stage_tx, 128);
+  A.wbytes = (int)align_up((size_t)(8 * p.warps + 1) * 4, 16);
+  A.ent_off = (int)align_up((size_t)A.wsl_off + A.wbytes, 128);
+  A.stage_stride = (int)align_up((size_t)A.ent_off + Aproj->max_slice_bytes, 1024);
   A.cluster = p.cluster;
   A.slice_rows = kWinRows / p.cluster;
   A.vec_out = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(A.yt) % 16 == 0) ? 1 : 0;
@@ -742,7 +824,7 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
 
-  const size_t smem = (size_t)kStages * A.stage_stride + 2 * kStages * sizeof(uint64_t) + 1024;
+  const size_t smem = (size_t)kStages * A.stage_stride + 2 * kStages * sizeof(uint64_t) + kStages * 4 + 1024;
   static thread_local size_t configured[2] = {0, 0};
   const int slot = es == 4 ? 0 : 1;
   if (configured[slot] < smem) {
@@ -825,9 +907,14 @@ sf_status lsp_projector_create(int64_t rows, int32_t d, int32_t k, const int32_t
     off = sf::align_up(off + bytes, 256);
     return o;
   };
+  p->a_rng = 8 * std::min(16, (d + 7) / 8);
+  p->n_ar = (int32_t)ceil_div(d, p->a_rng);
+  // wptr and went are padded so the 16-byte rounded bulk copies of the
+  // gather kernel never read past the allocation
   const size_t o_eidx = take(nnz * 4), o_eval = take(nnz * 4), o_cptr = take((d + 1) * 4), o_ridx = take(nnz * 4),
-               o_cval = take(nnz * 4), o_perm = take(d * 4), o_wptr = take((nwd + 1) * 4), o_went = take(nnz * 8),
-               o_wcnt = take(nwd * 4), o_coff = take(nwd * 4), o_tot = take(d * 4), o_err = take(4);
+               o_cval = take(nnz * 4), o_perm = take(d * 4), o_wptr = take((nwd + 1 + 16) * 4),
+               o_went = take((nnz + 4) * 8), o_gd = take((size_t)p->n_ar * p->n_win * 8), o_wcnt = take(nwd * 4),
+               o_coff = take(nwd * 4), o_tot = take(d * 4), o_err = take(8);
   if (cudaMalloc(&p->block, off) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -842,6 +929,7 @@ sf_status lsp_projector_create(int64_t rows, int32_t d, int32_t k, const int32_t
   p->bucket_perm = reinterpret_cast<int32_t*>(b + o_perm);
   p->wptr = reinterpret_cast<int32_t*>(b + o_wptr);
   p->went = reinterpret_cast<int2*>(b + o_went);
+  p->gdesc = reinterpret_cast<int2*>(b + o_gd);
   p->wcnt = reinterpret_cast<int32_t*>(b + o_wcnt);
   p->csc_off = reinterpret_cast<int32_t*>(b + o_coff);
   p->totals = reinterpret_cast<int32_t*>(b + o_tot);
@@ -852,7 +940,9 @@ sf_status lsp_projector_create(int64_t rows, int32_t d, int32_t k, const int32_t
     delete p;
     return st;
   };
-  if (cudaMemsetAsync(p->err, 0, 4, stream) != cudaSuccess) return bail(sf::cuda_fail(cudaGetLastError(), "memset"));
+  if (cudaMemsetAsync(p->err, 0, 8, stream) != cudaSuccess || cudaMemsetAsync(p->wptr + nwd + 1, 0, 64, stream) != cudaSuccess ||
+      cudaMemsetAsync(p->went + nnz, 0, 32, stream) != cudaSuccess)
+    return bail(sf::cuda_fail(cudaGetLastError(), "memset"));
   const int nsm = sf::sm_count();
   sf::k_copy_ell<<<(unsigned)std::min<int64_t>(ceil_div<int64_t>(nnz, 256), nsm * 8), 256, 0, stream>>>(
       d_col_idx, d_val, nnz, d, p->ell_idx, p->ell_val);
@@ -868,16 +958,21 @@ sf_status lsp_projector_create(int64_t rows, int32_t d, int32_t k, const int32_t
       d_col_idx, d_val, rows, k, d, p->dp, p->n_win, p->wptr, p->csc_off, p->col_ptr, p->went, p->row_idx,
       p->csc_val);
   sf::k_bucket_perm<<<1, 1024, 0, stream>>>(p->col_ptr, d, p->bucket_perm);
+  sf::k_gdesc<<<(unsigned)ceil_div<int64_t>((int64_t)p->n_ar * p->n_win, 256), 256, 0, stream>>>(
+      p->wptr, p->n_win, p->dp, p->a_rng, p->n_ar, p->gdesc, p->err + 1);
   sf_status st = sf::check_launch("projector build");
   if (st != SF_OK) return bail(st);
+  // the build ends with one bounded wait: the gather launches need the
+  // largest slice size on the host
+  st = sf::bounded_wait_stream(stream, 0, "lsp_projector_create");
+  if (st != SF_OK) return bail(st);
+  int32_t flags[2] = {0, 0};
+  if (cudaMemcpy(flags, p->err, 8, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return bail(sf::cuda_fail(cudaGetLastError(), "read build flags"));
+  p->max_slice_bytes = flags[1];
   if (validate) {
-    st = sf::bounded_wait_stream(stream, 0, "lsp_projector_create");
-    if (st != SF_OK) return bail(st);
-    int32_t err = 0;
-    if (cudaMemcpy(&err, p->err, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
-      return bail(sf::cuda_fail(cudaGetLastError(), "read validation flag"));
-    if (err & sf::kDevErrIndex) return bail(fail(SF_ERR_INVALID, "projector has a column id outside [0, %d)", d));
-    if (err & 4) return bail(fail(SF_ERR_INVALID, "projector repeats a column id inside a row"));
+    if (flags[0] & sf::kDevErrIndex) return bail(fail(SF_ERR_INVALID, "projector has a column id outside [0, %d)", d));
+    if (flags[0] & 4) return bail(fail(SF_ERR_INVALID, "projector repeats a column id inside a row"));
   }
   *out = p;
   return SF_OK;
@@ -960,16 +1055,17 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
   float* V = static_cast<float*>(ws);
   const int nsm = sf::sm_count();
   uint16_t* mirror = static_cast<uint16_t*>(w_bf16_mirror);
-  if (d <= sf::kMaxFastD) {
+  if (d <= sf::kMaxFastD && P->k <= 32 && Q->k <= 32) {
     const int n_ab = (int)ceil_div(d, sf::kVRows);
     const int64_t n_tiles = ceil_div<int64_t>(n, 32);
     const int warps = 8;
     const int tpw = (int)std::max<int64_t>(1, (int64_t)n_ab * n_tiles / ((int64_t)warps * sf::kTargetCtas));
     const int64_t gy = ceil_div<int64_t>(n_tiles, (int64_t)warps * tpw);
-    const size_t smem_v = (size_t)d * 65 * 4;
+    const size_t smem_v = (size_t)d * 65 * 4 + (size_t)warps * 32 * Q->k * 8;
     static thread_local bool v_cfg = false;
     if (!v_cfg) {
-      SF_CUDA_TRY(cudaFuncSetAttribute(sf::k_v, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)((size_t)sf::kMaxFastD * 65 * 4)),
+      SF_CUDA_TRY(cudaFuncSetAttribute(sf::k_v, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)((size_t)sf::kMaxFastD * 65 * 4 + 8 * 32 * 32 * 8)),
                   "cudaFuncSetAttribute(k_v)");
       v_cfg = true;
     }
@@ -977,7 +1073,7 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
                                                                           tpw);
     SF_TRY(sf::check_launch("k_v"));
 
-    const size_t smem_a = (size_t)d * sf::kApplyCols * 4;
+    const size_t smem_a = (size_t)d * sf::kApplyCols * 4 + 16 * 32 * 8;
     const int64_t n_jb = ceil_div<int64_t>(n, sf::kApplyCols);
     const int64_t total = n_jb * m;
     const bool bf16w = w_dtype == SF_BF16;
@@ -985,7 +1081,7 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
     static thread_local bool a_cfg[2] = {false, false};
     if (!a_cfg[bf16w]) {
       SF_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)((size_t)sf::kMaxFastD * sf::kApplyCols * 4)),
+                                       (int)((size_t)sf::kMaxFastD * sf::kApplyCols * 4 + 16 * 32 * 8)),
                   "cudaFuncSetAttribute(k_apply)");
       a_cfg[bf16w] = true;
     }
@@ -997,7 +1093,8 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
     const size_t wb = bf16w ? 2 : 4;
     const int vec_ok = (n % 2 == 0) && (reinterpret_cast<uintptr_t>(W) % (2 * wb) == 0) &&
                        (!mirror || reinterpret_cast<uintptr_t>(mirror) % 4 == 0);
-    kern<<<(unsigned)ceil_div<int64_t>(total, ipc), 512, smem_a, s>>>(V, d, n, m, P->ell_idx, P->ell_val, P->k, W,
+    const int R = std::min(sf::kApplyMaxR, 32 / P->k);
+    kern<<<(unsigned)ceil_div<int64_t>(total, ipc), 512, smem_a, s>>>(V, d, n, m, P->ell_idx, P->ell_val, P->k, R, W,
                                                                        mirror, total, ipc, vec_ok);
     return sf::check_launch("k_apply");
   }

@@ -49,3 +49,18 @@ def check_bf16(name, got_bits, ref_f64, max_ulp=1):
 
 
 HP = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+def check_bf16_applied(name, got_bits, w_in, D, D_abs):
+    """bf16 W after W -= D: within 1 ulp of RNE(W - D), or, where W and D
+    cancel so that the bf16 spacing of the result is finer than the fp32
+    accumulation error of D, within the applied-W bound
+    TOL_LSP * (|W| + |D|_abs) of the exact result."""
+    ref = w_in - D
+    d = ob.ulp_distance(got_bits, ob.bf16_bits(ref))
+    err = np.abs(ob.bits_to_f64(got_bits) - ref)
+    ok = (d <= 1) | (err <= TOL_LSP * (np.abs(w_in) + D_abs))
+    if not ok.all():
+        i = int(np.flatnonzero(~ok.ravel())[0])
+        raise AssertionError(f"{name}: {int((~ok).sum())} elements out; first at {i}: {int(d.ravel()[i])} ulp, "
+                             f"err {err.ravel()[i]!r}")

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from _util import HP, TOL_LSP, TOL_STATE, bits, check_bf16, check_close, f64
+from _util import HP, TOL_LSP, TOL_STATE, bits, check_bf16_applied, check_close, f64
 from layer_optimizer_gb300 import native, synth
 from oracle import adamw as oa
 from oracle import bf16 as ob
@@ -172,7 +172,7 @@ def test_decompress_apply_parity(m, n, d, k, wtype):
         wb0 = bits(W)
         native.lsp_decompress_apply(P, Q, dS, W, native.SF_BF16, None, m, n, ws, nb)
         torch.cuda.synchronize()
-        check_bf16("W bf16", bits(W), ob.bits_to_f64(wb0) - D)
+        check_bf16_applied("W bf16", bits(W), ob.bits_to_f64(wb0), D, D_abs)
     else:
         W = W0.to(DEV)
         mirror = torch.empty(m, n, dtype=torch.bfloat16, device=DEV) if wtype.endswith("mirror") else None
@@ -260,7 +260,7 @@ def test_llama7b_matrices_full_size():
         torch.cuda.synchronize()
         S_ref, S_abs = ol.compress(Pr, Qr, f64(G))
         check_close(f"S {name}", S, S_ref, S_abs, TOL_LSP)
-        D, _ = ol.decompress(Pr, Qr, f64(dS))
-        check_bf16(f"W {name}", bits(W), ob.bits_to_f64(wb0) - D)
+        D, D_abs = ol.decompress(Pr, Qr, f64(dS))
+        check_bf16_applied(f"W {name}", bits(W), ob.bits_to_f64(wb0), D, D_abs)
         del G, W, ws
         torch.cuda.empty_cache()
