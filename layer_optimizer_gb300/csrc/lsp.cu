@@ -486,6 +486,8 @@ __global__ void k_reduce_splits(const float* __restrict__ part, int splits, int6
 // Decompress kernels
 // ----------------------------------------------------------------------------
 
+__host__ __device__ __forceinline__ size_t v_ebuf_offset(int d) { return ((size_t)d * 65 * 4 + 15) / 16 * 16; }
+
 // V[a][j] = sum_l q_{j,l} dS[a][c_{j,l}] for a in a 64-row block, j in 32-column tiles.
 // dS^T of the block sits in shared memory (st[c * 65 + aa], padded: the
 // transposing fill and the lane-along-a reads are both conflict-free); the
@@ -496,7 +498,9 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
                                            float* __restrict__ V, int tiles_per_warp) {
   extern __shared__ float st[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  int2* ebuf = reinterpret_cast<int2*>(st + (size_t)d * 65) + (size_t)warp * 32 * k;
+  // entry buffers start at the first 16-byte boundary after the tile (d * 65 floats)
+  int2* ebuf = reinterpret_cast<int2*>(reinterpret_cast<unsigned char*>(st) + v_ebuf_offset(d)) +
+               (size_t)warp * 32 * k;
   const int a0 = blockIdx.x * kVRows;
   for (int aa = warp; aa < kVRows; aa += nwarps) {
     const int a = a0 + aa;
@@ -1061,11 +1065,11 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
     const int warps = 8;
     const int tpw = (int)std::max<int64_t>(1, (int64_t)n_ab * n_tiles / ((int64_t)warps * sf::kTargetCtas));
     const int64_t gy = ceil_div<int64_t>(n_tiles, (int64_t)warps * tpw);
-    const size_t smem_v = (size_t)d * 65 * 4 + (size_t)warps * 32 * Q->k * 8;
+    const size_t smem_v = sf::v_ebuf_offset(d) + (size_t)warps * 32 * Q->k * 8;
     static thread_local bool v_cfg = false;
     if (!v_cfg) {
       SF_CUDA_TRY(cudaFuncSetAttribute(sf::k_v, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)((size_t)sf::kMaxFastD * 65 * 4 + 8 * 32 * 32 * 8)),
+                                       (int)(sf::v_ebuf_offset(sf::kMaxFastD) + 8 * 32 * 32 * 8)),
                   "cudaFuncSetAttribute(k_v)");
       v_cfg = true;
     }
