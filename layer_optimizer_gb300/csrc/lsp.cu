@@ -57,6 +57,8 @@ constexpr int kVRows = 64;          // a rows per V CTA (2 per lane)
 constexpr int kMaxFastD = 512;      // shared-memory tiles of k_v / k_apply hold d <= 512
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t imax64(int64_t a, int64_t b) { return a > b ? a : b; }
 
 }  // namespace
 }  // namespace sf
@@ -691,6 +693,192 @@ __global__ void __launch_bounds__(512) k_apply(const float* __restrict__ V, int 
   }
 }
 
+// TMA-streamed apply: the same arithmetic as k_apply, but W arrives in
+// 64 x 64 tiles and P's rows in 64-row blocks through a ring of shared-memory
+// stages fed by one producer warp (2D TMA for W, 1D bulk copies for the
+// entries), so every SM keeps tens of KB of HBM reads in flight.  16
+// consumer warps each take 4 rows of a tile (2 columns per lane); results
+// go straight to global memory with coalesced stores.  The V block is
+// restaged when a CTA's work crosses into the next column block.
+constexpr int kApplyRows = 64;
+constexpr int kApplyConsumerWarps = 16;
+constexpr int kApplyMaxStages = 4;
+
+struct ApplyArgs {
+  const float* V;
+  const int32_t* pidx;
+  const float* pval;
+  void* W;
+  uint16_t* mirror;
+  int64_t n, m;
+  int64_t n_rt;          // row tiles
+  int64_t total;         // column blocks x row tiles
+  int64_t per_cta;
+  int32_t d, k;
+  int32_t tile_bytes;    // 64 x 64 x element size
+  int32_t ent_stride;    // bytes reserved for one entry array of a stage
+  int32_t stage_stride;
+  int32_t stages;
+  int32_t vs_bytes;      // bytes of the V block (1024-aligned)
+  int32_t vec_ok;
+};
+
+template <bool kBf16W>
+__global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
+    k_apply_tma(const __grid_constant__ CUtensorMap wmap, const ApplyArgs A) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* vs = reinterpret_cast<float*>(smem);
+  unsigned char* stages = smem + A.vs_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + (size_t)A.stages * A.stage_stride);
+  uint64_t* empty = full + kApplyMaxStages;
+  int32_t* shared_flags = reinterpret_cast<int32_t*>(empty + kApplyMaxStages);   // [0] issued, [1] failed
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = A.stages;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kApplyConsumerWarps);
+    }
+    shared_flags[0] = 0;
+    shared_flags[1] = 0;
+    fence_mbar_init_cluster();
+  }
+  __syncthreads();
+  const int64_t it0 = (int64_t)blockIdx.x * A.per_cta;
+  const int64_t nit = imax64(0, imin64(A.total, it0 + A.per_cta) - it0);
+  const int k = A.k;
+
+  if (warp == kApplyConsumerWarps) {
+    // producer
+    if (lane == 0) {
+      int64_t q = 0;
+      for (; q < nit; ++q) {
+        const int s = (int)(q % S);
+        if (q >= S && !mbar_wait(&empty[s], (uint32_t)((q / S) & 1) ^ 1u)) {
+          shared_flags[1] = 1;
+          break;
+        }
+        const int64_t item = it0 + q, jb = item / A.n_rt, rt = item % A.n_rt;
+        const int rows_here = (int)imin64(kApplyRows, A.m - rt * kApplyRows);
+        const uint32_t eb = (uint32_t)((rows_here * k * 4 + 15) / 16 * 16);
+        unsigned char* st = stages + (size_t)s * A.stage_stride;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)A.tile_bytes + 2 * eb);
+        tma_load_2d(st, &wmap, &full[s], (int)(jb * kApplyCols), (int)(rt * kApplyRows));
+        bulk_load(st + A.tile_bytes, A.pidx + rt * kApplyRows * k, eb, &full[s]);
+        bulk_load(st + A.tile_bytes + A.ent_stride, A.pval + rt * kApplyRows * k, eb, &full[s]);
+      }
+      shared_flags[0] = (int32_t)q;
+    }
+  } else {
+    // consumers
+    int64_t cur_jb = -1;
+    bool failed = false;
+    for (int64_t q = 0; q < nit; ++q) {
+      const int64_t item = it0 + q, jb = item / A.n_rt, rt = item % A.n_rt;
+      const int64_t j0 = jb * kApplyCols;
+      if (jb != cur_jb) {
+        named_bar_sync(1, 32 * kApplyConsumerWarps);
+        for (int e = threadIdx.x; e < A.d * kApplyCols; e += 32 * kApplyConsumerWarps) {
+          const int a = e / kApplyCols, jj = e % kApplyCols;
+          vs[e] = (j0 + jj < A.n) ? A.V[(int64_t)a * A.n + j0 + jj] : 0.0f;
+        }
+        named_bar_sync(1, 32 * kApplyConsumerWarps);
+        cur_jb = jb;
+      }
+      const int s = (int)(q % S);
+      if (!failed && !mbar_wait(&full[s], (uint32_t)(q / S) & 1u)) {
+        failed = true;
+        shared_flags[1] = 1;
+      }
+      if (failed) continue;
+      const unsigned char* st = stages + (size_t)s * A.stage_stride;
+      const int32_t* eidx = reinterpret_cast<const int32_t*>(st + A.tile_bytes);
+      const float* evals = reinterpret_cast<const float*>(st + A.tile_bytes + A.ent_stride);
+      const int64_t j = j0 + 2 * lane;
+      const bool on0 = j < A.n, on1 = j + 1 < A.n;
+      const bool vec = A.vec_ok && on1;
+#pragma unroll
+      for (int r4 = 0; r4 < 4; ++r4) {
+        const int r = warp * 4 + r4;
+        const int64_t i = rt * kApplyRows + r;
+        if (i >= A.m) break;
+        float w0, w1;
+        if (kBf16W) {
+          const uint32_t u = *reinterpret_cast<const uint32_t*>(st + ((size_t)r * kApplyCols + 2 * lane) * 2);
+          w0 = __uint_as_float(u << 16);
+          w1 = __uint_as_float(u & 0xFFFF0000u);
+        } else {
+          const float2 u = *reinterpret_cast<const float2*>(st + ((size_t)r * kApplyCols + 2 * lane) * 4);
+          w0 = u.x;
+          w1 = u.y;
+        }
+        float s0 = 0.0f, s1 = 0.0f;
+        const int32_t* ri = eidx + r * k;
+        const float* rv = evals + r * k;
+        if ((k & 3) == 0) {
+          for (int l = 0; l < k; l += 4) {
+            const int4 a4 = *reinterpret_cast<const int4*>(ri + l);
+            const float4 p4 = *reinterpret_cast<const float4*>(rv + l);
+            const int aa[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 v = *reinterpret_cast<const float2*>(vs + aa[u] * kApplyCols + 2 * lane);
+              s0 = fmaf(pp[u], v.x, s0);
+              s1 = fmaf(pp[u], v.y, s1);
+            }
+          }
+        } else {
+          for (int l = 0; l < k; ++l) {
+            const float2 v = *reinterpret_cast<const float2*>(vs + ri[l] * kApplyCols + 2 * lane);
+            s0 = fmaf(rv[l], v.x, s0);
+            s1 = fmaf(rv[l], v.y, s1);
+          }
+        }
+        const float n0 = w0 - s0, n1 = w1 - s1;
+        const int64_t off = i * A.n + j;
+        if (kBf16W) {
+          uint16_t* Wb = static_cast<uint16_t*>(A.W);
+          if (vec) {
+            *reinterpret_cast<uint32_t*>(Wb + off) =
+                (uint32_t)f32_to_bf16_bits(n0) | ((uint32_t)f32_to_bf16_bits(n1) << 16);
+          } else {
+            if (on0) Wb[off] = f32_to_bf16_bits(n0);
+            if (on1) Wb[off + 1] = f32_to_bf16_bits(n1);
+          }
+        } else {
+          float* Wf = static_cast<float*>(A.W);
+          if (vec) {
+            *reinterpret_cast<float2*>(Wf + off) = make_float2(n0, n1);
+            if (A.mirror)
+              *reinterpret_cast<uint32_t*>(A.mirror + off) =
+                  (uint32_t)f32_to_bf16_bits(n0) | ((uint32_t)f32_to_bf16_bits(n1) << 16);
+          } else {
+            if (on0) {
+              Wf[off] = n0;
+              if (A.mirror) A.mirror[off] = f32_to_bf16_bits(n0);
+            }
+            if (on1) {
+              Wf[off + 1] = n1;
+              if (A.mirror) A.mirror[off + 1] = f32_to_bf16_bits(n1);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(&empty[s]);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && shared_flags[1]) {
+    // a wait ran out: let the copies still in flight land (bounded) before exit
+    const int64_t issued = shared_flags[0];
+    for (int64_t q = imax64(0, issued - S); q < issued; ++q)
+      mbar_wait(&full[q % S], (uint32_t)(q / S) & 1u);
+  }
+}
+
 template <bool kBf16W>
 __global__ void k_apply_generic(const float* __restrict__ V, int64_t n, int64_t m, const int32_t* __restrict__ pidx,
                                 const float* __restrict__ pval, int k, void* __restrict__ W,
@@ -915,7 +1103,7 @@ sf_status lsp_projector_create(int64_t rows, int32_t d, int32_t k, const int32_t
   p->n_ar = (int32_t)ceil_div(d, p->a_rng);
   // wptr and went are padded so the 16-byte rounded bulk copies of the
   // gather kernel never read past the allocation
-  const size_t o_eidx = take(nnz * 4), o_eval = take(nnz * 4), o_cptr = take((d + 1) * 4), o_ridx = take(nnz * 4),
+  const size_t o_eidx = take(nnz * 4 + 64), o_eval = take(nnz * 4 + 64), o_cptr = take((d + 1) * 4), o_ridx = take(nnz * 4),
                o_cval = take(nnz * 4), o_perm = take(d * 4), o_wptr = take((nwd + 1 + 16) * 4),
                o_went = take((nnz + 4) * 8), o_gd = take((size_t)p->n_ar * p->n_win * 8), o_wcnt = take(nwd * 4),
                o_coff = take(nwd * 4), o_tot = take(d * 4), o_err = take(8);
@@ -1097,6 +1285,52 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
     const size_t wb = bf16w ? 2 : 4;
     const int vec_ok = (n % 2 == 0) && (reinterpret_cast<uintptr_t>(W) % (2 * wb) == 0) &&
                        (!mirror || reinterpret_cast<uintptr_t>(mirror) % 4 == 0);
+    const size_t wes = bf16w ? 2 : 4;
+    if (sf::tma_ok(W, n, wes)) {
+      sf::ApplyArgs A;
+      A.V = V;
+      A.pidx = P->ell_idx;
+      A.pval = P->ell_val;
+      A.W = W;
+      A.mirror = mirror;
+      A.n = n;
+      A.m = m;
+      A.n_rt = ceil_div<int64_t>(m, sf::kApplyRows);
+      A.total = n_jb * A.n_rt;
+      A.d = d;
+      A.k = P->k;
+      A.tile_bytes = sf::kApplyRows * sf::kApplyCols * (int)wes;
+      A.ent_stride = (int)sf::align_up((size_t)sf::kApplyRows * P->k * 4, 128);
+      A.stage_stride = (int)sf::align_up((size_t)A.tile_bytes + 2 * A.ent_stride, 1024);
+      A.vs_bytes = (int)sf::align_up((size_t)d * sf::kApplyCols * 4, 1024);
+      const size_t fixed = (size_t)A.vs_bytes + 2 * sf::kApplyMaxStages * 8 + 16 + 1024;
+      A.stages = (int)std::min<size_t>(sf::kApplyMaxStages, (220 * 1024 - fixed) / A.stage_stride);
+      if (A.stages >= 2) {
+        A.vec_ok = vec_ok;
+        const int64_t grid2 = std::min<int64_t>(nsm, A.total);
+        A.per_cta = ceil_div<int64_t>(A.total, grid2);
+        const size_t smem2 = fixed + (size_t)A.stages * A.stage_stride;
+        CUtensorMap wmap;
+        cuuint64_t dims[2] = {(cuuint64_t)n, (cuuint64_t)m};
+        cuuint64_t strides[1] = {(cuuint64_t)(n * (int64_t)wes)};
+        cuuint32_t box[2] = {(cuuint32_t)sf::kApplyCols, (cuuint32_t)sf::kApplyRows};
+        cuuint32_t estr[2] = {1, 1};
+        CUresult r = sf::tensor_map_encoder()(&wmap, bf16w ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                              2, W, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled(W) failed (%d)", (int)r);
+        auto kt = bf16w ? sf::k_apply_tma<true> : sf::k_apply_tma<false>;
+        static thread_local bool t_cfg[2] = {false, false};
+        if (!t_cfg[bf16w]) {
+          SF_CUDA_TRY(cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024),
+                      "cudaFuncSetAttribute(k_apply_tma)");
+          t_cfg[bf16w] = true;
+        }
+        kt<<<(unsigned)ceil_div<int64_t>(A.total, A.per_cta), 32 * (sf::kApplyConsumerWarps + 1), smem2, s>>>(wmap, A);
+        return sf::check_launch("k_apply_tma");
+      }
+    }
     const int R = std::min(sf::kApplyMaxR, 32 / P->k);
     kern<<<(unsigned)ceil_div<int64_t>(total, ipc), 512, smem_a, s>>>(V, d, n, m, P->ell_idx, P->ell_val, P->k, R, W,
                                                                        mirror, total, ipc, vec_ok);
