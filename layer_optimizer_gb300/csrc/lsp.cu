@@ -316,7 +316,9 @@ __device__ __forceinline__ float4 load_tile4(const unsigned char* tile, int r, i
 template <typename TB>
 __global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtensorMap map, const GatherArgs A) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // round up to 1024 with arithmetic on the __shared__ array itself, so the
+  // compiler keeps the shared address space (plain LDS, not generic loads)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * A.stage_stride);
   uint64_t* empty = full + kStages;
   int32_t* hdr = reinterpret_cast<int32_t*>(empty + kStages);   // first staged entry of each stage
@@ -504,9 +506,38 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
   int2* ebuf = reinterpret_cast<int2*>(reinterpret_cast<unsigned char*>(st) + v_ebuf_offset(d)) +
                (size_t)warp * 32 * k;
   const int a0 = blockIdx.x * kVRows;
-  for (int aa = warp; aa < kVRows; aa += nwarps) {
-    const int a = a0 + aa;
-    for (int c = lane; c < d; c += 32) st[c * 65 + aa] = a < d ? dS[(int64_t)a * d + c] : 0.0f;
+  if ((d & 3) == 0 && (reinterpret_cast<uintptr_t>(dS) & 15) == 0) {
+    // lanes along a (one dS row each), warps along 4-column groups: 16-byte
+    // loads, 8 in flight per thread; the transposing stores hit 32 distinct banks
+    const int c4n = d / 4;
+    for (int half = 0; half < 2; ++half) {
+      const int aa = lane + 32 * half;
+      const int a = a0 + aa;
+      for (int c4 = warp; c4 < c4n; c4 += 8 * nwarps) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int cc = c4 + u * nwarps;
+          v[u] = (a < d && cc < c4n) ? *reinterpret_cast<const float4*>(dS + (int64_t)a * d + 4 * cc)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int cc = c4 + u * nwarps;
+          if (cc < c4n) {
+            st[(4 * cc + 0) * 65 + aa] = v[u].x;
+            st[(4 * cc + 1) * 65 + aa] = v[u].y;
+            st[(4 * cc + 2) * 65 + aa] = v[u].z;
+            st[(4 * cc + 3) * 65 + aa] = v[u].w;
+          }
+        }
+      }
+    }
+  } else {
+    for (int aa = warp; aa < kVRows; aa += nwarps) {
+      const int a = a0 + aa;
+      for (int c = lane; c < d; c += 32) st[c * 65 + aa] = a < d ? dS[(int64_t)a * d + c] : 0.0f;
+    }
   }
   __syncthreads();
   const int64_t n_tiles = (n + 31) / 32;
@@ -727,7 +758,9 @@ template <bool kBf16W>
 __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
     k_apply_tma(const __grid_constant__ CUtensorMap wmap, const ApplyArgs A) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // round up to 1024 with arithmetic on the __shared__ array itself, so the
+  // compiler keeps the shared address space (plain LDS, not generic loads)
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   float* vs = reinterpret_cast<float*>(smem);
   unsigned char* stages = smem + A.vs_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + (size_t)A.stages * A.stage_stride);
