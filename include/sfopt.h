@@ -171,6 +171,33 @@ sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G,
                        sf_dtype g_dtype, int64_t m, int64_t n, float* S,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* lsp_compress for callers that cannot allocate device memory or hand the
+ * library a workspace: callers under a framework whose caching allocator owns
+ * the device memory pool, latency-critical loops where cudaMalloc's implicit
+ * device-wide synchronisation is not acceptable, and thin bindings without an
+ * allocator.  The papers have no counterpart; this is a library convenience.
+ *
+ * Same arguments, result and errors as lsp_compress, minus the workspace:
+ * the intermediate lives in a fixed array of SF_NOALLOC_SCRATCH_BYTES that
+ * is part of the library image (every GPU that loads the library holds it
+ * until the process exits).  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *  - Shapes whose lsp_workspace_bytes(m, n, d) exceeds the array are
+ *    rejected with SF_ERR_UNSUPPORTED and a message (for example
+ *    d = 512 covers n up to about 11,000 columns).
+ *  - The first call on a device looks up the array's device address on the
+ *    current device (cudaGetSymbolAddress) and caches it; make that first
+ *    call before any stream capture.
+ *  - Every call, on any stream, shares the one array, which keeps the last
+ *    call's contents: calls that overlap on the GPU race and give undefined
+ *    results.  Serialise them (one stream, or events).  Nothing in the
+ *    array needs to start at zero. */
+#define SF_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+sf_status lsp_compress_noalloc(lsp_projector P, lsp_projector Q, const void* G,
+                               sf_dtype g_dtype, int64_t m, int64_t n, float* S,
+                               void* stream);
+
 /* AdamW in the compressed space, no weight decay, step t = `step` >= 1:
  *   m  <- beta1*m + (1-beta1)*S;  v <- beta2*v + (1-beta2)*S^2
  *   dS  = (lr/(1-beta1^t)) * m / (sqrt(v)/sqrt(1-beta2^t) + eps)

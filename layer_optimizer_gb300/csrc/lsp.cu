@@ -40,6 +40,7 @@
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <mutex>
 #include <new>
 
 #include "common.h"
@@ -1258,6 +1259,76 @@ sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G, sf_dtype
   else
     SF_TRY(sf::launch_gather<__nv_bfloat16>(P, static_cast<const __nv_bfloat16*>(G), n, n, cp.g1, rt, rtp, s));
   return sf::launch_gather<float>(Q, rt, d, d, cp.g2, S, sp, s);
+}
+
+}  // extern "C"
+
+// ----------------------------------------------------------------------------
+// lsp_compress without a caller workspace
+// ----------------------------------------------------------------------------
+// Some callers cannot hand the library a device workspace: code that runs
+// under a framework whose caching allocator owns the device memory pool (a
+// raw cudaMalloc there competes with, or fails against, that pool), code in
+// a latency-critical loop where cudaMalloc's implicit device-wide
+// synchronisation is not acceptable, and thin bindings that have no
+// allocator of their own.  For them the compress intermediate lives in this
+// fixed array instead.  It is part of the library image: every GPU that
+// loads the library holds it until the process exits.
+namespace sf {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SF_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.  In host code the array's name is only
+// a host-side stand-in, never a device address, so it is never passed to a kernel.
+sf_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kNoAllocMaxDevices)
+    return fail(SF_ERR_UNSUPPORTED, "lsp_compress_noalloc supports device ids below %d (got %d)", kNoAllocMaxDevices,
+                dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SF_OK;
+}
+
+}  // namespace
+}  // namespace sf
+
+extern "C" {
+
+sf_status lsp_compress_noalloc(lsp_projector P, lsp_projector Q, const void* G, sf_dtype g_dtype, int64_t m, int64_t n,
+                               float* S, void* stream) {
+  sf::clear_error();
+  SF_TRY(sf::check_proj(P, "P"));
+  SF_TRY(sf::check_proj(Q, "Q"));
+  if (P->rows != m || Q->rows != n)
+    return fail(SF_ERR_INVALID, "P has %lld rows, Q %lld: need m = %lld, n = %lld", (long long)P->rows,
+                (long long)Q->rows, (long long)m, (long long)n);
+  if (P->d != Q->d) return fail(SF_ERR_INVALID, "P and Q differ in d (%d vs %d)", P->d, Q->d);
+  const size_t need = sf::plan_compress(m, n, P->d).bytes;
+  if (need > (size_t)SF_NOALLOC_SCRATCH_BYTES)
+    return fail(SF_ERR_UNSUPPORTED,
+                "lsp_compress_noalloc: this shape needs %zu bytes of scratch, above the fixed %zu bytes; "
+                "use lsp_compress with a workspace",
+                need, (size_t)SF_NOALLOC_SCRATCH_BYTES);
+  void* ws = nullptr;
+  SF_TRY(sf::noalloc_scratch(&ws));
+  // Everything the compress writes into the scratch is written before it is
+  // read, so nothing needs clearing between calls.
+  return lsp_compress(P, Q, G, g_dtype, m, n, S, ws, (size_t)SF_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS, void* W, sf_dtype w_dtype,

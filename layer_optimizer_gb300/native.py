@@ -24,7 +24,7 @@ EXPORTS = [
     "lsp_projector_destroy", "lsp_workspace_bytes", "lsp_compress", "lsp_adamw_compressed",
     "lsp_decompress_apply", "sf_window_create", "sf_slide_window_step", "sf_window_sync",
     "sf_window_destroy", "sf_sync_status", "sf_last_error", "sf_version",
-    "sf_test_fail_copy_after",
+    "sf_test_fail_copy_after", "lsp_compress_noalloc",
 ]
 
 
@@ -64,6 +64,7 @@ _SIGS = {
     "lsp_projector_destroy": (_ST, [_P]),
     "lsp_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I32]),
     "lsp_compress": (_ST, [_P, _P, _P, _INT, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
+    "lsp_compress_noalloc": (_ST, [_P, _P, _P, _INT, _I64, _I64, _P, _P]),
     "lsp_adamw_compressed": (_ST, [_P, _P, _P, _P, _I64, ctypes.POINTER(sf_adamw_hparams), _I64, _P]),
     "lsp_decompress_apply": (_ST, [_P, _P, _P, _P, _INT, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
     "sf_window_create": (_ST, [_INT, ctypes.POINTER(ctypes.POINTER(sf_tensor)), _INT, _P, _P, _P, ctypes.POINTER(_P)]),
@@ -199,6 +200,13 @@ def lsp_workspace_bytes(m, n, d):
 def lsp_compress(P, Q, G, g_dtype, m, n, S, ws, ws_bytes, stream=None):
     _check(load().lsp_compress(P.handle, Q.handle, _addr(G), g_dtype, m, n, _addr(S), _addr(ws),
                                ws_bytes, _stream(stream)))
+
+
+def lsp_compress_noalloc(P, Q, G, g_dtype, m, n, S, stream=None):
+    _check(load().lsp_compress_noalloc(P.handle, Q.handle, _addr(G), g_dtype, m, n, _addr(S), _stream(stream)))
+
+
+SF_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def lsp_adamw_compressed(S, m, v, dS, d2, hp, step, stream=None):

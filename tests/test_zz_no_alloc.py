@@ -1,0 +1,71 @@
+"""lsp_compress_noalloc: compress without a caller workspace (GPU).
+
+Some callers cannot allocate device memory or hand over a workspace (a
+framework's caching allocator owns the pool, or cudaMalloc's implicit
+synchronisation is not acceptable in their loop).  The no-alloc entry point
+keeps the compress intermediate in a fixed array inside the library.  These
+tests call it through the C ABI and compare it with lsp_compress, which
+takes a caller workspace, on two calls in a row: the second call must not be
+affected by what the first left in the shared array.
+
+The file name sorts last so that a run stopping at the first failure has
+already run every other test.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from _util import TOL_LSP, check_close, f64
+from layer_optimizer_gb300 import native, synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _proj(rows, d, k, seed):
+    idx, val = synth.projector(rows, d, k, seed)
+    return native.lsp_projector_create(rows, d, k, torch.from_numpy(idx).to(DEV), torch.from_numpy(val).to(DEV))
+
+
+def _reference(P, Q, G, dt, m, n, d):
+    S = torch.empty(d, d, device=DEV)
+    nb = native.lsp_workspace_bytes(m, n, d)
+    ws = torch.empty(nb, dtype=torch.uint8, device=DEV)
+    native.lsp_compress(P, Q, G, dt, m, n, S, ws, nb)
+    torch.cuda.synchronize()
+    return S
+
+
+@pytest.mark.parametrize("m,n,d,k,torch_dt,dt", [
+    (4096, 4096, 512, 8, torch.float32, native.SF_FP32),    # LLaMA-7B q-shaped gradient
+    (1024, 1024, 64, 4, torch.bfloat16, native.SF_BF16),    # one 1024 x 1024 linear layer, bf16 grads
+    (333, 264, 200, 3, torch.float32, native.SF_FP32),      # ragged tiles, 2-CTA clusters
+])
+def test_noalloc_matches_workspace_entry_point_twice(m, n, d, k, torch_dt, dt):
+    lib = native.load()
+    P, Q = _proj(m, d, k, 1000 + m), _proj(n, d, k, 2000 + n)
+    for call in range(2):
+        G = synth.normal((m, n), 1e-3, 3000 + call, dtype=torch_dt).to(DEV)
+        S = torch.full((d, d), float("nan"), device=DEV)
+        st = lib.lsp_compress_noalloc(P.handle, Q.handle, G.data_ptr(), dt, m, n, S.data_ptr(), None)
+        assert st == native.SF_OK, native.sf_last_error()
+        torch.cuda.synchronize()
+        ref = _reference(P, Q, G, dt, m, n, d)
+        r = f64(ref)
+        check_close(f"S (call {call + 1})", S, r, np.abs(r), TOL_LSP)
+
+
+def test_noalloc_rejects_shapes_beyond_the_fixed_scratch():
+    lib = native.load()
+    m, n, d = 64, 20000, 512          # the intermediate alone is 20000 x 512 fp32 = 41 MB
+    assert native.lsp_workspace_bytes(m, n, d) > native.SF_NOALLOC_SCRATCH_BYTES
+    P, Q = _proj(m, d, 8, 1), _proj(n, d, 8, 2)
+    G = torch.empty(1, device=DEV)    # never read: the size check comes first
+    S = torch.empty(d, d, device=DEV)
+    st = lib.lsp_compress_noalloc(P.handle, Q.handle, G.data_ptr(), native.SF_FP32, m, n, S.data_ptr(), None)
+    assert st == native.SF_ERR_UNSUPPORTED
+    assert "scratch" in native.sf_last_error()
+    native.sf_sync_status()
