@@ -49,9 +49,9 @@
 namespace sf {
 namespace {
 
-constexpr int kWinRows = 64;        // rows of A (and of B) per window
+constexpr int kWinRows = 128;       // rows of A (and of B) per window
 constexpr int kColsPerCta = 128;    // B columns per gather CTA (4 per lane)
-constexpr int kStages = 4;          // TMA ring depth of the gather kernel
+constexpr int kMaxStages = 4;       // TMA ring depth of the gather kernel (at most)
 constexpr int kTargetCtas = 148;    // grid size aimed at (about one CTA per SM)
 constexpr int kApplyCols = 64;      // W columns per apply CTA (2 per lane)
 constexpr int kVRows = 64;          // a rows per V CTA (2 per lane)
@@ -301,6 +301,7 @@ struct GatherArgs {
   int32_t slice_rows;      // rows each CTA of the cluster loads (kWinRows / cluster)
   int32_t cluster;         // CTAs per cluster (1, 2, 4 or 8)
   int32_t vec_out;         // output rows are 16-byte aligned (d % 4 == 0, aligned base)
+  int32_t stages;          // depth of the TMA ring
 };
 
 template <typename TB>
@@ -315,96 +316,117 @@ __device__ __forceinline__ float4 load_tile4(const unsigned char* tile, int r, i
 }
 
 template <typename TB>
-__global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtensorMap map, const GatherArgs A) {
+__global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtensorMap map, const GatherArgs A) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // round up to 1024 with arithmetic on the __shared__ array itself, so the
   // compiler keeps the shared address space (plain LDS, not generic loads)
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * A.stage_stride);
-  uint64_t* empty = full + kStages;
-  int32_t* hdr = reinterpret_cast<int32_t*>(empty + kStages);   // first staged entry of each stage
+  const int S = A.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)S * A.stage_stride);
+  uint64_t* empty = full + kMaxStages;
+  int32_t* hdr = reinterpret_cast<int32_t*>(empty + kMaxStages);   // first staged entry of each stage
+  int32_t* flags = hdr + kMaxStages;                                // [0] issued, [1] failed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
+  const int ncw = (blockDim.x >> 5) - 1;        // consumer warps; the last warp produces
   const int C = A.cluster;
   const uint32_t rank = C > 1 ? cluster_ctarank() : 0;
   const uint16_t mask = (uint16_t)((1u << C) - 1u);
   const int c0 = blockIdx.x * kColsPerCta;
-  const int a_cta = blockIdx.y * 8 * nwarps;
-  const int a0 = a_cta + 8 * warp;
+  const int a_cta = blockIdx.y * 8 * ncw;
   const int w_begin = blockIdx.z * A.win_per_split;
   const int w_end = min(A.n_win, w_begin + A.win_per_split);
   const int nw = max(0, w_end - w_begin);
-  const bool lane_on = 4 * lane < A.cbx;
-  const bool warp_on = a0 < A.dp;
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&map);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], nwarps * C);
+      mbar_init(&empty[s], ncw * C);
     }
+    flags[0] = 0;
+    flags[1] = 0;
     fence_mbar_init_cluster();
   }
   if (C > 1) cluster_sync(); else __syncthreads();
 
-  // One stage = the B tile of a window (rows split over the cluster and
-  // multicast), this CTA's slice of the prefix table and its entry slice.
-  const int2* gd_row = A.gdesc + (int64_t)blockIdx.y * A.n_win;
-  auto issue = [&](int it, int2 gd) {
-    const int s = it % kStages;
-    const int w = w_begin + it;
-    unsigned char* st = smem + (size_t)s * A.stage_stride;
-    hdr[s] = gd.x;
-    mbar_arrive_expect_tx(&full[s], (uint32_t)(A.stage_tx + A.wbytes + gd.y));
-    unsigned char* dst = st + (size_t)rank * A.slice_rows * A.cbx * sizeof(TB);
-    const int y = w * kWinRows + (int)rank * A.slice_rows;
-    if (C > 1) tma_load_2d_multicast(dst, &map, &full[s], c0, y, mask);
-    else tma_load_2d(dst, &map, &full[s], c0, y);
-    bulk_load(st + A.wsl_off, A.wptr + (int64_t)w * A.dp + a_cta, (uint32_t)A.wbytes, &full[s]);
-    if (gd.y > 0) bulk_load(st + A.ent_off, A.went + gd.x, (uint32_t)gd.y, &full[s]);
-  };
-
-  int issued = 0;
-  bool failed = false;
-  int2 gd_next = make_int2(0, 0);
-  if (threadIdx.x == 0) {
-    for (; issued < min(kStages, nw); ++issued) issue(issued, gd_row[w_begin + issued]);
-    if (issued < nw) gd_next = gd_row[w_begin + issued];
-  }
-
-  float acc[8][4];
-#pragma unroll
-  for (int s = 0; s < 8; ++s)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) acc[s][j] = 0.0f;
-
-  int it = 0;
-  for (; it < nw; ++it) {
-    const int s = it % kStages;
-    const uint32_t par = (uint32_t)(it / kStages) & 1u;
-    if (!mbar_wait(&full[s], par)) {
-      failed = true;
-      break;
+  if (warp == ncw) {
+    // Producer: one stage = the B tile of a window (rows split over the
+    // cluster and multicast), this CTA's slice of the prefix table and its
+    // entry slice.  A stage is refilled once every consumer warp of every
+    // CTA in the cluster has released it.
+    if (lane == 0) {
+      const int2* gd_row = A.gdesc + (int64_t)blockIdx.y * A.n_win;
+      int it = 0;
+      int2 gd = nw > 0 ? gd_row[w_begin] : make_int2(0, 0);
+      for (; it < nw; ++it) {
+        const int s = it % S;
+        if (it >= S && !mbar_wait(&empty[s], ((uint32_t)(it / S) & 1u) ^ 1u)) {
+          flags[1] = 1;
+          break;
+        }
+        const int w = w_begin + it;
+        unsigned char* st = smem + (size_t)s * A.stage_stride;
+        hdr[s] = gd.x;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(A.stage_tx + A.wbytes + gd.y));
+        unsigned char* dst = st + (size_t)rank * A.slice_rows * A.cbx * sizeof(TB);
+        const int y = w * kWinRows + (int)rank * A.slice_rows;
+        if (C > 1) tma_load_2d_multicast(dst, &map, &full[s], c0, y, mask);
+        else tma_load_2d(dst, &map, &full[s], c0, y);
+        bulk_load(st + A.wsl_off, A.wptr + (int64_t)w * A.dp + a_cta, (uint32_t)A.wbytes, &full[s]);
+        if (gd.y > 0) bulk_load(st + A.ent_off, A.went + gd.x, (uint32_t)gd.y, &full[s]);
+        if (it + 1 < nw) gd = gd_row[w + 1];
+      }
+      flags[0] = it;
     }
-    const int w = w_begin + it;
-    if (warp_on) {
-      const unsigned char* tile = smem + (size_t)s * A.stage_stride;
-      const int32_t* bp = reinterpret_cast<const int32_t*>(tile + A.wsl_off) + 8 * warp;
-      const int4 lo = *reinterpret_cast<const int4*>(bp);
-      const int4 hi = *reinterpret_cast<const int4*>(bp + 4);
-      const int32_t e_base = hdr[s];
-      const int bnd[9] = {lo.x - e_base, lo.y - e_base, lo.z - e_base, lo.w - e_base, hi.x - e_base,
-                          hi.y - e_base, hi.z - e_base, hi.w - e_base, bp[8] - e_base};
-      const int2* ent = reinterpret_cast<const int2*>(tile + A.ent_off);
-      const int rbase = w * kWinRows;
+  } else {
+    const int a0 = a_cta + 8 * warp;
+    const bool lane_on = 4 * lane < A.cbx;
+    const bool warp_on = a0 < A.dp;
+    float acc[8][4];
 #pragma unroll
-      for (int sl = 0; sl < 8; ++sl) {
-        for (int e = bnd[sl]; e < bnd[sl + 1]; ++e) {
-          const int2 en = ent[e];
-          const float v = __int_as_float(en.y);
-          if (lane_on) {
+    for (int sl = 0; sl < 8; ++sl)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[sl][j] = 0.0f;
+    bool failed = false;
+    for (int it = 0; it < nw; ++it) {
+      const int s = it % S;
+      if (!mbar_wait(&full[s], (uint32_t)(it / S) & 1u)) {
+        failed = true;
+        flags[1] = 1;
+        break;
+      }
+      const int w = w_begin + it;
+      if (warp_on && lane_on) {
+        const unsigned char* tile = smem + (size_t)s * A.stage_stride;
+        const int32_t* bp = reinterpret_cast<const int32_t*>(tile + A.wsl_off) + 8 * warp;
+        const int4 lo = *reinterpret_cast<const int4*>(bp);
+        const int4 hi = *reinterpret_cast<const int4*>(bp + 4);
+        const int32_t e_base = hdr[s];
+        const int bnd[9] = {lo.x - e_base, lo.y - e_base, lo.z - e_base, lo.w - e_base, hi.x - e_base,
+                            hi.y - e_base, hi.z - e_base, hi.w - e_base, bp[8] - e_base};
+        const int2* ent = reinterpret_cast<const int2*>(tile + A.ent_off);
+        const int rbase = w * kWinRows;
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl) {
+          int e = bnd[sl];
+          const int e_end = bnd[sl + 1];
+          // two entries per step: independent loads in flight
+          for (; e + 1 < e_end; e += 2) {
+            const int2 en0 = ent[e];
+            const int2 en1 = ent[e + 1];
+            const float4 x0 = load_tile4<TB>(tile, en0.x - rbase, A.cbx, lane);
+            const float4 x1 = load_tile4<TB>(tile, en1.x - rbase, A.cbx, lane);
+            const float v0 = __int_as_float(en0.y), v1 = __int_as_float(en1.y);
+            acc[sl][0] = fmaf(v1, x1.x, fmaf(v0, x0.x, acc[sl][0]));
+            acc[sl][1] = fmaf(v1, x1.y, fmaf(v0, x0.y, acc[sl][1]));
+            acc[sl][2] = fmaf(v1, x1.z, fmaf(v0, x0.z, acc[sl][2]));
+            acc[sl][3] = fmaf(v1, x1.w, fmaf(v0, x0.w, acc[sl][3]));
+          }
+          if (e < e_end) {
+            const int2 en = ent[e];
             const float4 x = load_tile4<TB>(tile, en.x - rbase, A.cbx, lane);
+            const float v = __int_as_float(en.y);
             acc[sl][0] = fmaf(v, x.x, acc[sl][0]);
             acc[sl][1] = fmaf(v, x.y, acc[sl][1]);
             acc[sl][2] = fmaf(v, x.z, acc[sl][2]);
@@ -412,48 +434,41 @@ __global__ void __launch_bounds__(512) k_gather_t(const __grid_constant__ CUtens
           }
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      if (C > 1) {
-        for (int r = 0; r < C; ++r) mbar_arrive_cluster(&empty[s], (uint32_t)r);
-      } else {
-        mbar_arrive_local(&empty[s]);
+      __syncwarp();
+      if (lane == 0) {
+        if (C > 1) {
+          for (int r = 0; r < C; ++r) mbar_arrive_cluster(&empty[s], (uint32_t)r);
+        } else {
+          mbar_arrive_local(&empty[s]);
+        }
       }
     }
-    if (threadIdx.x == 0 && issued < nw && issued == it + kStages) {
-      if (!mbar_wait(&empty[s], par)) {
-        failed = true;
-        break;
-      }
-      issue(issued, gd_next);
-      ++issued;
-      if (issued < nw) gd_next = gd_row[w_begin + issued];
-    }
-  }
-  if (failed && threadIdx.x == 0) {
-    // drain the copies this CTA still expects (bounded), so none lands after exit
-    for (int j = it; j < issued; ++j) mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u);
-  }
 
-  // Y^T[col][a] for the lane's 4 columns and the warp's 8 outputs.
-  if (warp_on && lane_on && !failed) {
-    float* out = A.yt + (int64_t)blockIdx.z * A.split_stride;
-    const bool vec = A.vec_out && (a0 + 8 <= A.d);
+    // Y^T[col][a] for the lane's 4 columns and the warp's 8 outputs.
+    if (warp_on && lane_on && !failed) {
+      float* out = A.yt + (int64_t)blockIdx.z * A.split_stride;
+      const bool vec = A.vec_out && (a0 + 8 <= A.d);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int col = c0 + 4 * lane + j;
-      if (col >= A.ncols) continue;
-      float* o = out + (int64_t)col * A.d + a0;
-      if (vec) {
-        *reinterpret_cast<float4*>(o) = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
-        *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
-      } else {
+      for (int j = 0; j < 4; ++j) {
+        const int col = c0 + 4 * lane + j;
+        if (col >= A.ncols) continue;
+        float* o = out + (int64_t)col * A.d + a0;
+        if (vec) {
+          *reinterpret_cast<float4*>(o) = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
+          *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
+        } else {
 #pragma unroll
-        for (int sl = 0; sl < 8; ++sl)
-          if (a0 + sl < A.d) o[sl] = acc[sl][j];
+          for (int sl = 0; sl < 8; ++sl)
+            if (a0 + sl < A.d) o[sl] = acc[sl][j];
+        }
       }
     }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && flags[1]) {
+    // a wait ran out: let this CTA's copies still in flight land (bounded)
+    const int issued = flags[0];
+    for (int j = max(0, issued - S); j < issued; ++j) mbar_wait(&full[j % S], (uint32_t)(j / S) & 1u);
   }
   if (C > 1) cluster_sync();
 }
@@ -993,10 +1008,13 @@ size_t decompress_bytes(int64_t n, int d) { return align_up((size_t)d * n * 4, 2
 
 constexpr size_t kMaxGatherSmem = 220 * 1024;
 
-size_t gather_smem_estimate(const lsp_projector_s* Ap, size_t es) {
+size_t gather_stage_bytes(const lsp_projector_s* Ap, size_t es) {
   const size_t tile = (size_t)kWinRows * kColsPerCta * es;
-  const size_t per = align_up(align_up(tile, 128) + 16 * 40 + (size_t)Ap->max_slice_bytes, 1024);
-  return kStages * per + 2048;
+  return align_up(align_up(align_up(tile, 128) + 16 * 40, 128) + (size_t)Ap->max_slice_bytes, 1024);
+}
+
+size_t gather_smem_estimate(const lsp_projector_s* Ap, size_t es) {
+  return 2 * gather_stage_bytes(Ap, es) + 2048;   // the ring needs at least two stages
 }
 
 bool tma_ok(const void* B, int64_t ldb, size_t esize) {
@@ -1035,6 +1053,7 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   A.wbytes = (int)align_up((size_t)(8 * p.warps + 1) * 4, 16);
   A.ent_off = (int)align_up((size_t)A.wsl_off + A.wbytes, 128);
   A.stage_stride = (int)align_up((size_t)A.ent_off + Aproj->max_slice_bytes, 1024);
+  A.stages = (int)std::min<size_t>(kMaxStages, (kMaxGatherSmem - 2048) / A.stage_stride);
   A.cluster = p.cluster;
   A.slice_rows = kWinRows / p.cluster;
   A.vec_out = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(A.yt) % 16 == 0) ? 1 : 0;
@@ -1050,17 +1069,17 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
 
-  const size_t smem = (size_t)kStages * A.stage_stride + 2 * kStages * sizeof(uint64_t) + kStages * 4 + 1024;
+  const size_t smem = (size_t)A.stages * A.stage_stride + 2 * kMaxStages * sizeof(uint64_t) + kMaxStages * 4 + 8 + 1024;
   static thread_local size_t configured[2] = {0, 0};
   const int slot = es == 4 ? 0 : 1;
   if (configured[slot] < smem) {
-    SF_CUDA_TRY(cudaFuncSetAttribute(k_gather_t<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+    SF_CUDA_TRY(cudaFuncSetAttribute(k_gather_t<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxGatherSmem),
                 "cudaFuncSetAttribute(k_gather_t)");
     configured[slot] = smem;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_cb, (unsigned)p.n_ar, (unsigned)p.splits);
-  cfg.blockDim = dim3(32 * p.warps);
+  cfg.blockDim = dim3(32 * (p.warps + 1));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
