@@ -304,12 +304,13 @@ struct GatherArgs {
   int32_t stages;          // depth of the TMA ring
 };
 
+// 4 consecutive B elements of a tile row as fp32 (bf16 widened exactly).
 template <typename TB>
-__device__ __forceinline__ float4 load_tile4(const unsigned char* tile, int r, int cbx, int lane) {
+__device__ __forceinline__ float4 tile_load(uint32_t addr) {
   if constexpr (sizeof(TB) == 4) {
-    return *reinterpret_cast<const float4*>(tile + ((size_t)r * cbx + 4 * lane) * 4);
+    return lds_f4(addr);
   } else {
-    const uint2 u = *reinterpret_cast<const uint2*>(tile + ((size_t)r * cbx + 4 * lane) * 2);
+    const uint2 u = lds_u2(addr);
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u),
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u));
   }
@@ -383,6 +384,9 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
     const int a0 = a_cta + 8 * warp;
     const bool lane_on = 4 * lane < A.cbx;
     const bool warp_on = a0 < A.dp;
+    const uint32_t smem_base = smem_u32(smem);
+    const uint32_t row_bytes = (uint32_t)A.cbx * (uint32_t)sizeof(TB);
+    const uint32_t lane_off = 4u * (uint32_t)lane * (uint32_t)sizeof(TB);
     float acc[8][4];
 #pragma unroll
     for (int sl = 0; sl < 8; ++sl)
@@ -398,25 +402,27 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
       }
       const int w = w_begin + it;
       if (warp_on && lane_on) {
-        const unsigned char* tile = smem + (size_t)s * A.stage_stride;
-        const int32_t* bp = reinterpret_cast<const int32_t*>(tile + A.wsl_off) + 8 * warp;
-        const int4 lo = *reinterpret_cast<const int4*>(bp);
-        const int4 hi = *reinterpret_cast<const int4*>(bp + 4);
+        // 32-bit shared addresses: entry i of the stage at ent + 8 i; row r of
+        // the tile, this lane's 4 columns, at lane_tile + r * row_bytes
+        const uint32_t tile = smem_base + (uint32_t)s * (uint32_t)A.stage_stride;
+        const uint32_t bp = tile + (uint32_t)A.wsl_off + 32u * (uint32_t)warp;
+        const int4 lo = lds_i4(bp);
+        const int4 hi = lds_i4(bp + 16);
+        const int32_t last = (int32_t)lds_u32(bp + 32);
         const int32_t e_base = hdr[s];
-        const int bnd[9] = {lo.x - e_base, lo.y - e_base, lo.z - e_base, lo.w - e_base, hi.x - e_base,
-                            hi.y - e_base, hi.z - e_base, hi.w - e_base, bp[8] - e_base};
-        const int2* ent = reinterpret_cast<const int2*>(tile + A.ent_off);
-        const int rbase = w * kWinRows;
+        const uint32_t ent = tile + (uint32_t)A.ent_off - 8u * (uint32_t)e_base;
+        const uint32_t row_adj = tile + lane_off - (uint32_t)(w * kWinRows) * row_bytes;
+        const int bnd[9] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w, last};
 #pragma unroll
         for (int sl = 0; sl < 8; ++sl) {
           int e = bnd[sl];
           const int e_end = bnd[sl + 1];
           // two entries per step: independent loads in flight
           for (; e + 1 < e_end; e += 2) {
-            const int2 en0 = ent[e];
-            const int2 en1 = ent[e + 1];
-            const float4 x0 = load_tile4<TB>(tile, en0.x - rbase, A.cbx, lane);
-            const float4 x1 = load_tile4<TB>(tile, en1.x - rbase, A.cbx, lane);
+            const int2 en0 = lds_i2(ent + 8u * (uint32_t)e);
+            const int2 en1 = lds_i2(ent + 8u * (uint32_t)e + 8u);
+            const float4 x0 = tile_load<TB>(row_adj + (uint32_t)en0.x * row_bytes);
+            const float4 x1 = tile_load<TB>(row_adj + (uint32_t)en1.x * row_bytes);
             const float v0 = __int_as_float(en0.y), v1 = __int_as_float(en1.y);
             acc[sl][0] = fmaf(v1, x1.x, fmaf(v0, x0.x, acc[sl][0]));
             acc[sl][1] = fmaf(v1, x1.y, fmaf(v0, x0.y, acc[sl][1]));
@@ -424,8 +430,8 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
             acc[sl][3] = fmaf(v1, x1.w, fmaf(v0, x0.w, acc[sl][3]));
           }
           if (e < e_end) {
-            const int2 en = ent[e];
-            const float4 x = load_tile4<TB>(tile, en.x - rbase, A.cbx, lane);
+            const int2 en = lds_i2(ent + 8u * (uint32_t)e);
+            const float4 x = tile_load<TB>(row_adj + (uint32_t)en.x * row_bytes);
             const float v = __int_as_float(en.y);
             acc[sl][0] = fmaf(v, x.x, acc[sl][0]);
             acc[sl][1] = fmaf(v, x.y, acc[sl][1]);
@@ -823,6 +829,8 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
     // consumers
     int64_t cur_jb = -1;
     bool failed = false;
+    const uint32_t stages_base = smem_u32(stages);
+    const uint32_t vs_lane = smem_u32(vs) + 8u * (uint32_t)lane;
     for (int64_t q = 0; q < nit; ++q) {
       const int64_t item = it0 + q, jb = item / A.n_rt, rt = item % A.n_rt;
       const int64_t j0 = jb * kApplyCols;
@@ -841,9 +849,11 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
         shared_flags[1] = 1;
       }
       if (failed) continue;
-      const unsigned char* st = stages + (size_t)s * A.stage_stride;
-      const int32_t* eidx = reinterpret_cast<const int32_t*>(st + A.tile_bytes);
-      const float* evals = reinterpret_cast<const float*>(st + A.tile_bytes + A.ent_stride);
+      // 32-bit shared addresses: W tile row r at st + r * 64 * esize, entry
+      // arrays after it, V block row a at vs_lane + a * 256
+      const uint32_t st = stages_base + (uint32_t)s * (uint32_t)A.stage_stride;
+      const uint32_t eidx = st + (uint32_t)A.tile_bytes;
+      const uint32_t evals = eidx + (uint32_t)A.ent_stride;
       const int64_t j = j0 + 2 * lane;
       const bool on0 = j < A.n, on1 = j + 1 < A.n;
       const bool vec = A.vec_ok && on1;
@@ -854,35 +864,41 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
         if (i >= A.m) break;
         float w0, w1;
         if (kBf16W) {
-          const uint32_t u = *reinterpret_cast<const uint32_t*>(st + ((size_t)r * kApplyCols + 2 * lane) * 2);
+          const uint32_t u = lds_u32(st + ((uint32_t)r * kApplyCols + 2u * lane) * 2u);
           w0 = __uint_as_float(u << 16);
           w1 = __uint_as_float(u & 0xFFFF0000u);
         } else {
-          const float2 u = *reinterpret_cast<const float2*>(st + ((size_t)r * kApplyCols + 2 * lane) * 4);
+          const float2 u = lds_f2(st + ((uint32_t)r * kApplyCols + 2u * lane) * 4u);
           w0 = u.x;
           w1 = u.y;
         }
         float s0 = 0.0f, s1 = 0.0f;
-        const int32_t* ri = eidx + r * k;
-        const float* rv = evals + r * k;
+        const uint32_t ri = eidx + (uint32_t)(r * k) * 4u;
+        const uint32_t rv = evals + (uint32_t)(r * k) * 4u;
         if ((k & 3) == 0) {
           for (int l = 0; l < k; l += 4) {
-            const int4 a4 = *reinterpret_cast<const int4*>(ri + l);
-            const float4 p4 = *reinterpret_cast<const float4*>(rv + l);
-            const int aa[4] = {a4.x, a4.y, a4.z, a4.w};
-            const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float2 v = *reinterpret_cast<const float2*>(vs + aa[u] * kApplyCols + 2 * lane);
-              s0 = fmaf(pp[u], v.x, s0);
-              s1 = fmaf(pp[u], v.y, s1);
-            }
+            const int4 a4 = lds_i4(ri + 4u * l);
+            const float4 p4 = lds_f4(rv + 4u * l);
+            const float2 v0 = lds_f2(vs_lane + (uint32_t)a4.x * (kApplyCols * 4u));
+            const float2 v1 = lds_f2(vs_lane + (uint32_t)a4.y * (kApplyCols * 4u));
+            const float2 v2 = lds_f2(vs_lane + (uint32_t)a4.z * (kApplyCols * 4u));
+            const float2 v3 = lds_f2(vs_lane + (uint32_t)a4.w * (kApplyCols * 4u));
+            s0 = fmaf(p4.x, v0.x, s0);
+            s1 = fmaf(p4.x, v0.y, s1);
+            s0 = fmaf(p4.y, v1.x, s0);
+            s1 = fmaf(p4.y, v1.y, s1);
+            s0 = fmaf(p4.z, v2.x, s0);
+            s1 = fmaf(p4.z, v2.y, s1);
+            s0 = fmaf(p4.w, v3.x, s0);
+            s1 = fmaf(p4.w, v3.y, s1);
           }
         } else {
           for (int l = 0; l < k; ++l) {
-            const float2 v = *reinterpret_cast<const float2*>(vs + ri[l] * kApplyCols + 2 * lane);
-            s0 = fmaf(rv[l], v.x, s0);
-            s1 = fmaf(rv[l], v.y, s1);
+            const int a = (int)lds_u32(ri + 4u * l);
+            const float p = __uint_as_float(lds_u32(rv + 4u * l));
+            const float2 v = lds_f2(vs_lane + (uint32_t)a * (kApplyCols * 4u));
+            s0 = fmaf(p, v.x, s0);
+            s1 = fmaf(p, v.y, s1);
           }
         }
         const float n0 = w0 - s0, n1 = w1 - s1;
