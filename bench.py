@@ -273,6 +273,42 @@ def run_resident(args, world):
                 launches=args.steps * n_layers, clocks=clk.summary(), layer_params=synth.layer_numel(synth.OPT13_LAYER))
 
 
+def link_probe(nbytes=2 << 30, reps=5):
+    """Raw host<->device copy bandwidth with pinned buffers: each direction alone, then both at once."""
+    import torch
+    h_a = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_b = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t0) / reps
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_a, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            h_b.copy_(d_b, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+    h2d(); d2h(); torch.cuda.synchronize()
+    t_h2d, t_d2h, t_both = timed(h2d), timed(d2h), timed(both)
+    out = {"bytes": nbytes, "h2d_GBps": nbytes / t_h2d / 1e9, "d2h_GBps": nbytes / t_d2h / 1e9,
+           "bidir_each_GBps": nbytes / t_both / 1e9}
+    del h_a, h_b, d_a, d_b
+    return out
+
+
 def run_e2e(args, world):
     """Same step through the window engine with the layers in pinned host memory."""
     import torch
@@ -359,6 +395,32 @@ def run_lsp(args, matrices=None):
         if it >= args.warmup:
             for m, n, e in row:
                 per.append((m, n, e[0].elapsed_time(e[1]), e[1].elapsed_time(e[2]), e[2].elapsed_time(e[3])))
+    # the same chain for all matrices captured once in a CUDA graph and
+    # replayed: no host gaps between the launches
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g, stream=cap):
+            cs = torch.cuda.current_stream()
+            for (name, m, n, P, Q, G, W, (S, mm, vv, dS), ws, wsb) in mats:
+                native.lsp_compress(P, Q, G, native.SF_FP32, m, n, S, ws, wsb, cs)
+                native.lsp_adamw_compressed(S, mm, vv, dS, d * d, hp, args.warmup + reps + 1, cs)
+                native.lsp_decompress_apply(P, Q, dS, W, native.SF_BF16, None, m, n, ws, wsb, cs)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ga, gb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ga.record(stream)
+        for _ in range(reps):
+            g.replay()
+        gb.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = ga.elapsed_time(gb) / reps
+        del g
+    except Exception as ex:  # recorded on the line, eager numbers still stand
+        graph_ms = f"graph capture failed: {str(ex)[:120]}"
     n_params = sum(m * n for (_, m, n, *_r) in mats)
     comp_t = sum(p[2] for p in per) / reps
     ad_t = sum(p[3] for p in per) / reps
@@ -374,7 +436,13 @@ def run_lsp(args, matrices=None):
         "adamw_compressed": {"ms": ad_t},
         "decompress_apply": {"ms": dec_t, "GBps": dec_bytes / dec_t / 1e6, "frac": dec_bytes / dec_t / 1e6 / peak},
         "peak_GBps": peak, "peak_kind": kind,
+        "ms_per_chain_all7_graph": graph_ms,
     }
+    if isinstance(graph_ms, float):
+        out["params_updated_per_s_graph"] = n_params / (graph_ms / 1e3)
+        all_bytes = comp_bytes + dec_bytes + 24 * d * d * len(mats)
+        out["chain_GBps_graph"] = all_bytes / graph_ms / 1e6
+        out["chain_frac_graph"] = all_bytes / graph_ms / 1e6 / peak
     for x in mats:
         x[3].close()
         x[4].close()
@@ -431,6 +499,10 @@ def main_ours(args, rank, world):
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "path": "sf_slide_window_step: 24 pinned host layers, 2 device slots, 3 streams",
                        "link_GBps_each_way": e["h2d"] * args.steps / wall / 1e9}
+        try:
+            line["e2e"]["link_probe"] = link_probe()
+        except Exception as ex:
+            line["e2e"]["link_probe"] = {"error": str(ex)[:200]}
     if not args.no_lsp and rank == 0:
         try:
             line["lsp"] = run_lsp(args)

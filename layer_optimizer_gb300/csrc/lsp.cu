@@ -857,12 +857,8 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
       const int64_t j = j0 + 2 * lane;
       const bool on0 = j < A.n, on1 = j + 1 < A.n;
       const bool vec = A.vec_ok && on1;
-#pragma unroll
-      for (int r4 = 0; r4 < 4; ++r4) {
-        const int r = warp * 4 + r4;
-        const int64_t i = rt * kApplyRows + r;
-        if (i >= A.m) break;
-        float w0, w1;
+      // W row r of this tile as two fp32 values
+      auto w_load = [&](int r, float& w0, float& w1) {
         if (kBf16W) {
           const uint32_t u = lds_u32(st + ((uint32_t)r * kApplyCols + 2u * lane) * 2u);
           w0 = __uint_as_float(u << 16);
@@ -872,42 +868,14 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
           w0 = u.x;
           w1 = u.y;
         }
-        float s0 = 0.0f, s1 = 0.0f;
-        const uint32_t ri = eidx + (uint32_t)(r * k) * 4u;
-        const uint32_t rv = evals + (uint32_t)(r * k) * 4u;
-        if ((k & 3) == 0) {
-          for (int l = 0; l < k; l += 4) {
-            const int4 a4 = lds_i4(ri + 4u * l);
-            const float4 p4 = lds_f4(rv + 4u * l);
-            const float2 v0 = lds_f2(vs_lane + (uint32_t)a4.x * (kApplyCols * 4u));
-            const float2 v1 = lds_f2(vs_lane + (uint32_t)a4.y * (kApplyCols * 4u));
-            const float2 v2 = lds_f2(vs_lane + (uint32_t)a4.z * (kApplyCols * 4u));
-            const float2 v3 = lds_f2(vs_lane + (uint32_t)a4.w * (kApplyCols * 4u));
-            s0 = fmaf(p4.x, v0.x, s0);
-            s1 = fmaf(p4.x, v0.y, s1);
-            s0 = fmaf(p4.y, v1.x, s0);
-            s1 = fmaf(p4.y, v1.y, s1);
-            s0 = fmaf(p4.z, v2.x, s0);
-            s1 = fmaf(p4.z, v2.y, s1);
-            s0 = fmaf(p4.w, v3.x, s0);
-            s1 = fmaf(p4.w, v3.y, s1);
-          }
-        } else {
-          for (int l = 0; l < k; ++l) {
-            const int a = (int)lds_u32(ri + 4u * l);
-            const float p = __uint_as_float(lds_u32(rv + 4u * l));
-            const float2 v = lds_f2(vs_lane + (uint32_t)a * (kApplyCols * 4u));
-            s0 = fmaf(p, v.x, s0);
-            s1 = fmaf(p, v.y, s1);
-          }
-        }
-        const float n0 = w0 - s0, n1 = w1 - s1;
+      };
+      auto w_store = [&](int64_t i, float n0, float n1) {
         const int64_t off = i * A.n + j;
         if (kBf16W) {
           uint16_t* Wb = static_cast<uint16_t*>(A.W);
           if (vec) {
-            *reinterpret_cast<uint32_t*>(Wb + off) =
-                (uint32_t)f32_to_bf16_bits(n0) | ((uint32_t)f32_to_bf16_bits(n1) << 16);
+            __nv_bfloat162 h = __floats2bfloat162_rn(n0, n1);
+            *reinterpret_cast<uint32_t*>(Wb + off) = *reinterpret_cast<uint32_t*>(&h);
           } else {
             if (on0) Wb[off] = f32_to_bf16_bits(n0);
             if (on1) Wb[off + 1] = f32_to_bf16_bits(n1);
@@ -916,9 +884,10 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
           float* Wf = static_cast<float*>(A.W);
           if (vec) {
             *reinterpret_cast<float2*>(Wf + off) = make_float2(n0, n1);
-            if (A.mirror)
-              *reinterpret_cast<uint32_t*>(A.mirror + off) =
-                  (uint32_t)f32_to_bf16_bits(n0) | ((uint32_t)f32_to_bf16_bits(n1) << 16);
+            if (A.mirror) {
+              __nv_bfloat162 h = __floats2bfloat162_rn(n0, n1);
+              *reinterpret_cast<uint32_t*>(A.mirror + off) = *reinterpret_cast<uint32_t*>(&h);
+            }
           } else {
             if (on0) {
               Wf[off] = n0;
@@ -929,6 +898,59 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
               if (A.mirror) A.mirror[off + 1] = f32_to_bf16_bits(n1);
             }
           }
+        }
+      };
+      const int64_t i_first = rt * kApplyRows + warp * 4;
+      if (k == 8 && i_first + 3 < A.m) {
+        // two rows at a time, every load issued before the multiply-adds
+#pragma unroll
+        for (int rp = 0; rp < 4; rp += 2) {
+          const int r0 = warp * 4 + rp;
+          const uint32_t e0 = eidx + (uint32_t)r0 * 32u, v0a = evals + (uint32_t)r0 * 32u;
+          const int4 a0 = lds_i4(e0), a1 = lds_i4(e0 + 16), a2 = lds_i4(e0 + 32), a3 = lds_i4(e0 + 48);
+          const float4 p0 = lds_f4(v0a), p1 = lds_f4(v0a + 16), p2 = lds_f4(v0a + 32), p3 = lds_f4(v0a + 48);
+          float wa0, wa1, wb0, wb1;
+          w_load(r0, wa0, wa1);
+          w_load(r0 + 1, wb0, wb1);
+          const int ia[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const int ib[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+          const float pa[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          const float pb[8] = {p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
+          float2 va[8], vb[8];
+#pragma unroll
+          for (int l = 0; l < 8; ++l) {
+            va[l] = lds_f2(vs_lane + (uint32_t)ia[l] * (kApplyCols * 4u));
+            vb[l] = lds_f2(vs_lane + (uint32_t)ib[l] * (kApplyCols * 4u));
+          }
+          float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f;
+#pragma unroll
+          for (int l = 0; l < 8; ++l) {
+            sa0 = fmaf(pa[l], va[l].x, sa0);
+            sa1 = fmaf(pa[l], va[l].y, sa1);
+            sb0 = fmaf(pb[l], vb[l].x, sb0);
+            sb1 = fmaf(pb[l], vb[l].y, sb1);
+          }
+          w_store(i_first + rp, wa0 - sa0, wa1 - sa1);
+          w_store(i_first + rp + 1, wb0 - sb0, wb1 - sb1);
+        }
+      } else {
+        for (int r4 = 0; r4 < 4; ++r4) {
+          const int r = warp * 4 + r4;
+          const int64_t i = rt * kApplyRows + r;
+          if (i >= A.m) break;
+          float w0, w1;
+          w_load(r, w0, w1);
+          float s0 = 0.0f, s1 = 0.0f;
+          const uint32_t ri = eidx + (uint32_t)(r * k) * 4u;
+          const uint32_t rv = evals + (uint32_t)(r * k) * 4u;
+          for (int l = 0; l < k; ++l) {
+            const int a = (int)lds_u32(ri + 4u * l);
+            const float p = __uint_as_float(lds_u32(rv + 4u * l));
+            const float2 v = lds_f2(vs_lane + (uint32_t)a * (kApplyCols * 4u));
+            s0 = fmaf(p, v.x, s0);
+            s1 = fmaf(p, v.y, s1);
+          }
+          w_store(i, w0 - s0, w1 - s1);
         }
       }
       __syncwarp();
