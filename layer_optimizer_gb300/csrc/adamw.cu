@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 
 #include "common.h"
+#include "ptx.cuh"
 
 namespace sf {
 namespace {
@@ -51,6 +52,33 @@ struct LaunchArgs {
   AdamConsts c;
   int32_t nt;
   int32_t total_tiles;
+  int32_t skip_vector;   // vector-mode tensors: only the scalar head and tail (the bulk kernel does the rest)
+};
+
+// Bulk-copy kernel: the 16-byte aligned middle of each tensor, in chunks.
+constexpr int kBulkChunk = 2048;                    // elements per stage (256 threads x 8)
+constexpr int kBulkStages = 6;                      // ring depth: 6 x 28 KB in flight per SM
+constexpr int kBulkConsumerWarps = 8;
+constexpr int kBulkStageBytes = kBulkChunk * 14;    // grad 4 KB, master / m / v 8 KB each
+constexpr int kBulkOffP = kBulkChunk * 2, kBulkOffM = kBulkChunk * 6, kBulkOffV = kBulkChunk * 10;
+constexpr int64_t kBulkMinElems = int64_t(1) << 20; // smaller launches keep the register-staged kernel
+
+struct BulkTensor {
+  const uint16_t* g;    // all pointers already advanced past the scalar head
+  float* p;
+  float* m;
+  float* v;
+  uint16_t* w;          // may be null
+  int64_t len;          // elements of the aligned middle (a multiple of 8)
+  int32_t chunk_begin;
+  int32_t pad;
+};
+
+struct BulkArgs {
+  BulkTensor t[SF_MAX_TENSORS_PER_LAUNCH];
+  AdamConsts c;
+  int32_t nt;
+  int32_t total_chunks;
 };
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t bits16) {
@@ -100,6 +128,12 @@ adamw_multi_tensor_kernel(const __grid_constant__ LaunchArgs L) {
         const int64_t e = e0 + (int64_t)k * kThreads;
         if (e < d.n) scalar_elem(d, e, c);
       }
+      continue;
+    }
+
+    if (L.skip_vector) {
+      if ((int)threadIdx.x < d.head) scalar_elem(d, threadIdx.x, c);
+      if ((int)threadIdx.x < d.tail) scalar_elem(d, d.head + d.nvec * kUnitElems + threadIdx.x, c);
       continue;
     }
 
@@ -158,6 +192,115 @@ adamw_multi_tensor_kernel(const __grid_constant__ LaunchArgs L) {
     if (lt == 0 && (int)threadIdx.x < d.head) scalar_elem(d, threadIdx.x, c);
     if (lt == last && (int)threadIdx.x < d.tail)
       scalar_elem(d, d.head + d.nvec * kUnitElems + threadIdx.x, c);
+  }
+}
+
+// The aligned middle of every tensor, streamed through a ring of shared-memory
+// stages by 1D bulk copies (cp.async.bulk): one producer warp keeps up to
+// kBulkStages chunks (168 KB) of grad / master / m / v in flight per SM
+// without holding them in registers; 8 consumer warps read a chunk from
+// shared memory, update it and store master / m / v / weight straight to
+// global memory with streaming stores.
+__global__ void __launch_bounds__(32 * (kBulkConsumerWarps + 1), 1)
+    adamw_bulk_kernel(const __grid_constant__ BulkArgs B) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBulkStages * kBulkStageBytes);
+  uint64_t* empty = full + kBulkStages;
+  int32_t* flags = reinterpret_cast<int32_t*>(empty + kBulkStages);   // [0] issued, [1] failed
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBulkStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kBulkConsumerWarps);
+    }
+    flags[0] = flags[1] = 0;
+    fence_mbar_init_cluster();
+  }
+  __syncthreads();
+  const int G = gridDim.x;
+  const int n_my = (int)blockIdx.x < B.total_chunks ? (B.total_chunks - (int)blockIdx.x + G - 1) / G : 0;
+
+  if (warp == kBulkConsumerWarps) {
+    if (lane == 0) {
+      int q = 0;
+      for (; q < n_my; ++q) {
+        const int s = q % kBulkStages;
+        if (q >= kBulkStages && !mbar_wait(&empty[s], ((uint32_t)(q / kBulkStages) & 1u) ^ 1u)) {
+          flags[1] = 1;
+          break;
+        }
+        const int c = (int)blockIdx.x + q * G;
+        int ti = 0;
+        while (ti + 1 < B.nt && B.t[ti + 1].chunk_begin <= c) ++ti;
+        const BulkTensor& T = B.t[ti];
+        const int64_t e0 = (int64_t)(c - T.chunk_begin) * kBulkChunk;
+        const uint32_t len = (uint32_t)(T.len - e0 < kBulkChunk ? T.len - e0 : kBulkChunk);
+        unsigned char* st = smem + s * kBulkStageBytes;
+        mbar_arrive_expect_tx(&full[s], len * 14u);
+        bulk_load(st, T.g + e0, len * 2u, &full[s]);
+        bulk_load(st + kBulkOffP, T.p + e0, len * 4u, &full[s]);
+        bulk_load(st + kBulkOffM, T.m + e0, len * 4u, &full[s]);
+        bulk_load(st + kBulkOffV, T.v + e0, len * 4u, &full[s]);
+      }
+      flags[0] = q;
+    }
+  } else {
+    const AdamConsts& c = B.c;
+    const uint32_t base = smem_u32(smem);
+    bool failed = false;
+    for (int q = 0; q < n_my; ++q) {
+      const int s = q % kBulkStages;
+      if (!failed && !mbar_wait(&full[s], (uint32_t)(q / kBulkStages) & 1u)) {
+        failed = true;
+        flags[1] = 1;
+      }
+      if (failed) continue;
+      const int ch = (int)blockIdx.x + q * G;
+      int ti = 0;
+      while (ti + 1 < B.nt && B.t[ti + 1].chunk_begin <= ch) ++ti;
+      const BulkTensor& T = B.t[ti];
+      const int64_t e0 = (int64_t)(ch - T.chunk_begin) * kBulkChunk;
+      const int64_t len = T.len - e0 < kBulkChunk ? T.len - e0 : kBulkChunk;
+      const int t = threadIdx.x;
+      if (8 * t < len) {
+        const uint32_t st = base + (uint32_t)(s * kBulkStageBytes);
+        uint4 g4;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(g4.x), "=r"(g4.y), "=r"(g4.z), "=r"(g4.w)
+                     : "r"(st + 16u * t));
+        float4 p4[2] = {lds_f4(st + kBulkOffP + 32u * t), lds_f4(st + kBulkOffP + 32u * t + 16u)};
+        float4 m4[2] = {lds_f4(st + kBulkOffM + 32u * t), lds_f4(st + kBulkOffM + 32u * t + 16u)};
+        float4 v4[2] = {lds_f4(st + kBulkOffV + 32u * t), lds_f4(st + kBulkOffV + 32u * t + 16u)};
+        const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w};
+        float* pf = reinterpret_cast<float*>(&p4[0]);
+        float* mf = reinterpret_cast<float*>(&m4[0]);
+        float* vf = reinterpret_cast<float*>(&v4[0]);
+        uint32_t wout[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          adam_elem(bf16_to_f32(gw[j] & 0xFFFFu), pf[2 * j], mf[2 * j], vf[2 * j], c);
+          adam_elem(bf16_to_f32(gw[j] >> 16), pf[2 * j + 1], mf[2 * j + 1], vf[2 * j + 1], c);
+          wout[j] = pack_bf16x2(pf[2 * j], pf[2 * j + 1]);
+        }
+        const int64_t o = e0 + 8 * t;
+        __stcs(reinterpret_cast<float4*>(T.p + o), p4[0]);
+        __stcs(reinterpret_cast<float4*>(T.p + o) + 1, p4[1]);
+        __stcs(reinterpret_cast<float4*>(T.m + o), m4[0]);
+        __stcs(reinterpret_cast<float4*>(T.m + o) + 1, m4[1]);
+        __stcs(reinterpret_cast<float4*>(T.v + o), v4[0]);
+        __stcs(reinterpret_cast<float4*>(T.v + o) + 1, v4[1]);
+        if (T.w) __stcs(reinterpret_cast<uint4*>(T.w + o), make_uint4(wout[0], wout[1], wout[2], wout[3]));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(&empty[s]);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && flags[1]) {
+    // a wait ran out: let the copies still in flight land (bounded) before exit
+    const int issued = flags[0];
+    for (int q = issued > kBulkStages ? issued - kBulkStages : 0; q < issued; ++q)
+      mbar_wait(&full[q % kBulkStages], (uint32_t)(q / kBulkStages) & 1u);
   }
 }
 
@@ -259,6 +402,62 @@ sf_status adamw_layer_step_impl(const sf_tensor* tensors, int n_tensors, const s
       tiles += nt;
     }
     if (L.nt == 0) continue;
+    // Large launches: the aligned middles go through the bulk-copy kernel and
+    // the register-staged kernel only does scalar heads / tails and tensors
+    // that are not mutually 16-byte aligned.
+    int64_t vec_elems = 0;
+    for (int t = 0; t < L.nt; ++t)
+      if (L.t[t].vector_mode) vec_elems += L.t[t].nvec * kUnitElems;
+    L.skip_vector = vec_elems >= kBulkMinElems ? 1 : 0;
+    if (L.skip_vector) {
+      BulkArgs B;
+      B.c = c;
+      B.nt = 0;
+      int64_t chunks = 0;
+      bool scalar_work = false;
+      int64_t rtiles = 0;
+      for (int t = 0; t < L.nt; ++t) {
+        TensorDesc& d = L.t[t];
+        d.tile_begin = (int32_t)rtiles;
+        if (!d.vector_mode) {
+          rtiles += tiles_of(d);
+          scalar_work = true;
+          continue;
+        }
+        rtiles += 1;
+        if (d.head || d.tail) scalar_work = true;
+        if (d.nvec == 0) continue;
+        BulkTensor& T = B.t[B.nt++];
+        T.g = d.g + d.head;
+        T.p = d.p + d.head;
+        T.m = d.m + d.head;
+        T.v = d.v + d.head;
+        T.w = d.w ? d.w + d.head : nullptr;
+        T.len = d.nvec * kUnitElems;
+        T.chunk_begin = (int32_t)chunks;
+        T.pad = 0;
+        chunks += ceil_div<int64_t>(T.len, kBulkChunk);
+      }
+      B.total_chunks = (int32_t)chunks;
+      static_assert(sizeof(BulkArgs) <= 4096, "kernel parameter block too large");
+      const size_t smem = (size_t)kBulkStages * kBulkStageBytes + 2 * kBulkStages * 8 + 8;
+      static thread_local bool configured = false;
+      if (!configured) {
+        SF_CUDA_TRY(cudaFuncSetAttribute(adamw_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
+                    "cudaFuncSetAttribute(adamw_bulk_kernel)");
+        configured = true;
+      }
+      if (B.nt > 0) {
+        const int grid = (int)std::min<int64_t>(chunks, sm_count());
+        adamw_bulk_kernel<<<grid, 32 * (kBulkConsumerWarps + 1), smem, stream>>>(B);
+        SF_TRY(check_launch("adamw_bulk_kernel"));
+      }
+      if (!scalar_work) continue;
+      L.total_tiles = (int32_t)rtiles;
+      adamw_multi_tensor_kernel<<<(int)std::min<int64_t>(rtiles, grid_cap), kThreads, 0, stream>>>(L);
+      SF_TRY(check_launch("adamw_multi_tensor_kernel"));
+      continue;
+    }
     L.total_tiles = (int32_t)tiles;
     const int grid = (int)std::min<int64_t>(tiles, grid_cap);
     adamw_multi_tensor_kernel<<<grid, kThreads, 0, stream>>>(L);
@@ -277,6 +476,13 @@ sf_status adamw_compressed_impl(const float* S, float* m, float* v, float* dS, i
   const int64_t blocks = std::min<int64_t>(ceil_div<int64_t>(n, kThreads), (int64_t)sm_count() * 8);
   adamw_compressed_kernel<<<(int)blocks, kThreads, 0, stream>>>(S, m, v, dS, n, c);
   return check_launch("adamw_compressed_kernel");
+}
+
+int read_and_clear_device_error_adamw() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_device_error, &z, sizeof z);
+  return v;
 }
 
 }  // namespace sf

@@ -58,6 +58,7 @@ struct AdamConsts {
 // checks in the kernels set (0 = none; bit 1 = a wait ran out; bit 2 = an
 // out-of-range index was skipped).
 int read_and_clear_device_error();
+int read_and_clear_device_error_adamw();
 
 sf_status make_adam_consts(const sf_adamw_hparams* hp, int64_t step, bool with_decay,
                            AdamConsts* out);

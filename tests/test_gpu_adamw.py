@@ -80,6 +80,18 @@ def test_misaligned_pointers(offset):
     _run_and_check([5000, 33, 70001], steps=2, seed=3, offset=offset)
 
 
+@pytest.mark.parametrize("offset", [0, 3, 4])
+def test_bulk_copy_path_with_heads_tails_and_scalar_tensors(offset):
+    # over 2^20 aligned elements in one launch: the aligned middles go through
+    # the bulk-copy kernel, heads / tails and odd-phase tensors through the
+    # register-staged one
+    _run_and_check([600001, 500007, 33, 9, 2048 * 3], steps=2, seed=11, offset=offset)
+
+
+def test_bulk_copy_path_without_weights():
+    _run_and_check([1 << 20, 4096 + 3], steps=2, seed=12, with_weight=False)
+
+
 def test_no_weight_output():
     _run_and_check([3000, 12345], steps=2, seed=4, with_weight=False)
 
