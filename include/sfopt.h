@@ -68,7 +68,7 @@ typedef enum { SF_BF16 = 0, SF_FP32 = 1 } sf_dtype;
 
 /* AdamW hyper-parameters.  Given in double; the library derives the fp32
  * constants the kernels use (1-beta1, 1-beta2, 1-lr*wd, lr/(1-beta1^t),
- * sqrt(1-beta2^t)) in double and rounds each once. */
+ * 1/sqrt(1-beta2^t)) in double and rounds each once. */
 typedef struct {
   double lr;
   double beta1;

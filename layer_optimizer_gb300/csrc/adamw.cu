@@ -56,9 +56,9 @@ struct LaunchArgs {
 };
 
 // Bulk-copy kernel: the 16-byte aligned middle of each tensor, in chunks.
-constexpr int kBulkChunk = 2048;                    // elements per stage (256 threads x 8)
-constexpr int kBulkStages = 6;                      // ring depth: 6 x 28 KB in flight per SM
-constexpr int kBulkConsumerWarps = 8;
+constexpr int kBulkChunk = 4096;                    // elements per stage (512 threads x 8)
+constexpr int kBulkStages = 3;                      // ring depth: 3 x 56 KB in flight per SM
+constexpr int kBulkConsumerWarps = 16;
 constexpr int kBulkStageBytes = kBulkChunk * 14;    // grad 4 KB, master / m / v 8 KB each
 constexpr int kBulkOffP = kBulkChunk * 2, kBulkOffM = kBulkChunk * 6, kBulkOffV = kBulkChunk * 10;
 constexpr int64_t kBulkMinElems = int64_t(1) << 20; // smaller launches keep the register-staged kernel
@@ -95,7 +95,7 @@ __device__ __forceinline__ void adam_elem(float g, float& p, float& m, float& v,
                                           const AdamConsts& c) {
   m = fmaf(c.beta1, m, c.one_minus_beta1 * g);
   v = fmaf(c.beta2, v, c.one_minus_beta2 * (g * g));
-  const float denom = sqrtf(v) / c.sqrt_bc2 + c.eps;
+  const float denom = sqrtf(v) * c.inv_sqrt_bc2 + c.eps;
   p = fmaf(-c.step_size, m / denom, p * c.decay);
 }
 
@@ -198,7 +198,7 @@ adamw_multi_tensor_kernel(const __grid_constant__ LaunchArgs L) {
 // The aligned middle of every tensor, streamed through a ring of shared-memory
 // stages by 1D bulk copies (cp.async.bulk): one producer warp keeps up to
 // kBulkStages chunks (168 KB) of grad / master / m / v in flight per SM
-// without holding them in registers; 8 consumer warps read a chunk from
+// without holding them in registers; 16 consumer warps read a chunk from
 // shared memory, update it and store master / m / v / weight straight to
 // global memory with streaming stores.
 __global__ void __launch_bounds__(32 * (kBulkConsumerWarps + 1), 1)
@@ -314,7 +314,7 @@ adamw_compressed_kernel(const float* __restrict__ S, float* __restrict__ m, floa
     float mm = m[e], vv = v[e];
     mm = fmaf(c.beta1, mm, c.one_minus_beta1 * g);
     vv = fmaf(c.beta2, vv, c.one_minus_beta2 * (g * g));
-    const float denom = sqrtf(vv) / c.sqrt_bc2 + c.eps;
+    const float denom = sqrtf(vv) * c.inv_sqrt_bc2 + c.eps;
     m[e] = mm;
     v[e] = vv;
     dS[e] = c.step_size * (mm / denom);

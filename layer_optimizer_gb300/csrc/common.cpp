@@ -97,6 +97,7 @@ sf_status make_adam_consts(const sf_adamw_hparams* hp, int64_t step, bool with_d
   out->decay = static_cast<float>(with_decay ? 1.0 - hp->lr * hp->weight_decay : 1.0);
   out->step_size = static_cast<float>(hp->lr / bc1);
   out->sqrt_bc2 = static_cast<float>(std::sqrt(bc2));
+  out->inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
   out->eps = static_cast<float>(hp->eps);
   return SF_OK;
 }

@@ -51,6 +51,7 @@ struct AdamConsts {
   float decay;          // 1 - lr * weight_decay
   float step_size;      // lr / (1 - beta1^t)
   float sqrt_bc2;       // sqrt(1 - beta2^t)
+  float inv_sqrt_bc2;   // 1 / sqrt(1 - beta2^t), rounded once from double
   float eps;
 };
 
