@@ -57,6 +57,9 @@ def parse():
     ap.add_argument("--no-lsp", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--layers", type=int, default=24, help="OPT-1.3B layers (24 = the full stack)")
+    ap.add_argument("--workload", default="opt-1.3b", choices=["opt-1.3b", "llama2-7b", "mistral-window"],
+                    help="opt-1.3b: the headline stack; llama2-7b: the full LLaMA-2-7B step resident in HBM; "
+                         "mistral-window: four Mistral-Large layers in pinned host memory through 2 device slots")
     ap.add_argument("--profile-small", action="store_true",
                     help="1 layer, 1 warm-up + 1 timed step, no extras: a small case for ncu captures")
     ap.add_argument("--profile-lsp", action="store_true",
@@ -206,30 +209,38 @@ def oracle_params_per_s(budget_s=12.0, chunk=1 << 21, max_steps=None):
 
 # ------------------------------------------------------------------ ours ---
 
-def make_stack(n_layers, seed=0):
+def make_groups(groups, seed=0):
+    """Device buffers for a list of tensor groups (one group = one launch)."""
     import torch
 
     from layer_optimizer_gb300 import synth
-    layers = []
-    for li in range(n_layers):
+    out = []
+    for li, grp in enumerate(groups):
         ts = []
-        for ti, (_, n) in enumerate(synth.OPT13_LAYER):
+        for ti, (_, n) in enumerate(grp):
             g = synth.fill_normal_(torch.empty(n, dtype=torch.bfloat16, device="cuda"), 1e-3,
                                    synth.sub_seed(seed, 1, li, ti))
             p = synth.fill_normal_(torch.empty(n, device="cuda"), 0.02, synth.sub_seed(seed, 2, li, ti))
             ts.append([g, p, torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda"),
                        torch.empty(n, dtype=torch.bfloat16, device="cuda")])
-        layers.append(ts)
-    return layers
+        out.append(ts)
+    return out
+
+
+def workload_groups(args):
+    from layer_optimizer_gb300 import synth
+    if args.workload == "llama2-7b":
+        return synth.llama7_step_order()
+    return [synth.OPT13_LAYER] * args.layers
 
 
 def run_resident(args, world):
     import torch
 
     from layer_optimizer_gb300 import native, synth
-    n_layers = args.layers
-    layers = make_stack(n_layers)
-    params_per_step = n_layers * synth.layer_numel(synth.OPT13_LAYER)
+    groups = workload_groups(args)
+    layers = make_groups(groups)
+    params_per_step = sum(synth.layer_numel(g) for g in groups)
     hp = native.hparams(**HP)
     descs = [[native.make_tensor(*t) for t in L] for L in layers]
     arrs = [native.tensor_array(d) for d in descs]
@@ -237,6 +248,7 @@ def run_resident(args, world):
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
     step = [0]
+    n_groups = len(groups)
 
     def one_step(evs=None):
         step[0] += 1
@@ -252,7 +264,7 @@ def run_resident(args, world):
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_layers)]
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_groups)]
            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -267,10 +279,11 @@ def run_resident(args, world):
     barrier(world)
     total_ms = t0.elapsed_time(t1)
     launch_ms = [a.elapsed_time(b) for row in evs for (a, b) in row]
+    group_params = [synth.layer_numel(g) for g in groups] * args.steps
     del layers
     torch.cuda.empty_cache()
-    return dict(total_ms=total_ms, launch_ms=launch_ms, params_per_step=params_per_step,
-                launches=args.steps * n_layers, clocks=clk.summary(), layer_params=synth.layer_numel(synth.OPT13_LAYER))
+    return dict(total_ms=total_ms, launch_ms=launch_ms, params_per_step=params_per_step, group_params=group_params,
+                launches=args.steps * n_groups, clocks=clk.summary())
 
 
 def link_probe(nbytes=2 << 30, reps=5):
@@ -451,6 +464,136 @@ def run_lsp(args, matrices=None):
     return out
 
 
+def run_mistral_window(args, world):
+    """Four Mistral-Large layers in pinned host memory streamed through 2 device slots, 88 visits."""
+    import torch
+
+    from layer_optimizer_gb300 import native, synth
+    layer = synth.MISTRAL_LAYER
+    n_phys, n_visits = 4, 88
+    caps = [n for _, n in layer]
+    chunk = 1 << 28
+    tmp = torch.empty(chunk, device="cuda")
+    tmpb = torch.empty(chunk, dtype=torch.bfloat16, device="cuda")
+    zero = torch.zeros(chunk, device="cuda")
+
+    def fill_pinned(t, std, seed):
+        flat = t.view(-1)
+        for ci, s0 in enumerate(range(0, flat.numel(), chunk)):
+            e = min(flat.numel(), s0 + chunk)
+            if std is None:
+                flat[s0:e].copy_(zero[:e - s0])
+            elif t.dtype == torch.float32:
+                synth.fill_normal_(tmp[:e - s0], std, synth.sub_seed(seed, ci))
+                flat[s0:e].copy_(tmp[:e - s0])
+            else:
+                synth.fill_normal_(tmpb[:e - s0], std, synth.sub_seed(seed, ci))
+                flat[s0:e].copy_(tmpb[:e - s0])
+        torch.cuda.synchronize()
+        return t
+
+    t_alloc = time.perf_counter()
+    host = []
+    for li in range(n_phys):
+        ts = []
+        for ti, n in enumerate(caps):
+            g = fill_pinned(torch.empty(n, dtype=torch.bfloat16, pin_memory=True), 1e-3, synth.sub_seed(5, li, ti, 0))
+            p = fill_pinned(torch.empty(n, pin_memory=True), 0.02, synth.sub_seed(5, li, ti, 1))
+            m = fill_pinned(torch.empty(n, pin_memory=True), None, 0)
+            v = fill_pinned(torch.empty(n, pin_memory=True), None, 0)
+            w = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
+            ts.append([g, p, m, v, w])
+        host.append(ts)
+    del tmp, tmpb, zero
+    slots = [[[torch.empty(c, dtype=torch.bfloat16, device="cuda"), torch.empty(c, device="cuda"),
+               torch.empty(c, device="cuda"), torch.empty(c, device="cuda"),
+               torch.empty(c, dtype=torch.bfloat16, device="cuda")] for c in caps] for _ in range(2)]
+    setup_s = time.perf_counter() - t_alloc
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = native.sf_window_create([[native.make_tensor(*t) for t in s_] for s_ in slots], *streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in host])
+    steps = (ctypes.c_int64 * n_phys)()
+    hp = native.hparams(**HP)
+    # warm-up: one visit per physical layer
+    native.sf_slide_window_step(win, hl, list(range(n_phys)), hp, steps)
+    win.sync()
+    # stage times of one visit, each alone (for the overlap efficiency)
+    L0, S0 = host[0], slots[0]
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+    e[0].record(streams[0])
+    with torch.cuda.stream(streams[0]):
+        for h, d in zip(L0, S0):
+            for k in range(4):
+                d[k].copy_(h[k], non_blocking=True)
+    e[1].record(streams[0])
+    torch.cuda.synchronize()
+    e[2].record(streams[1])
+    native.sf_adamw_layer_step([native.make_tensor(*d) for d in S0], hp, 1, streams[1])
+    e[3].record(streams[1])
+    torch.cuda.synchronize()
+    e[4].record(streams[2])
+    with torch.cuda.stream(streams[2]):
+        for h, d in zip(L0, S0):
+            for k in (1, 2, 3, 4):
+                h[k].copy_(d[k], non_blocking=True)
+    e[5].record(streams[2])
+    torch.cuda.synchronize()
+    t_h2d, t_upd, t_d2h = e[0].elapsed_time(e[1]), e[2].elapsed_time(e[3]), e[4].elapsed_time(e[5])
+    order = [v % n_phys for v in range(n_visits)]
+    barrier(world)
+    clk = Clocks(bus_id_of_current_device())
+    with clk:
+        t0 = time.perf_counter()
+        native.sf_slide_window_step(win, hl, order, hp, steps)
+        win.sync()
+        wall = time.perf_counter() - t0
+    barrier(world)
+    per_layer = synth.layer_numel(layer)
+    win.close()
+    del host, slots
+    torch.cuda.empty_cache()
+    return dict(wall_s=wall, visits=n_visits, params_per_visit=per_layer, setup_s=setup_s,
+                t_h2d_ms=t_h2d, t_update_ms=t_upd, t_d2h_ms=t_d2h, clocks=clk.summary(), steps=list(steps))
+
+
+def main_window(args, rank, world):
+    import torch
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    from layer_optimizer_gb300 import native
+    native.load()
+    r = run_mistral_window(args, world)
+    wall = max_over_ranks(r["wall_s"], world)
+    params = world * r["params_per_visit"] * r["visits"]
+    link_bytes = 14 * r["params_per_visit"] * r["visits"]
+    bound = max(r["t_h2d_ms"], r["t_update_ms"], r["t_d2h_ms"])
+    peak, kind = measured_peak_hbm()
+    upd_gbs = ADAM_BYTES_PER_PARAM * r["params_per_visit"] / (r["t_update_ms"] / 1e3) / 1e9
+    line = {
+        "metric": "params updated/s (layer-sliding window, Mistral-Large-123B layer)",
+        "value": params / wall, "unit": "params/s", "n_gpus": world, "steps": 1, "warmup": 1,
+        "ms_per_step": wall * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (bf16 grad in, bf16 weight out)",
+        "data": "synthetic (seeded N(0,1e-3) bf16 grads fixed in the host slots, N(0,0.02) fp32 masters)",
+        "config": {"workload": "Mistral-Large-123B layer (hidden 12288, 96 q / 8 kv heads of 128, SwiGLU FFN 28672; "
+                               "1,384,144,896 params); 4 layers in pinned host memory (88.6 GB), 2 device slots, "
+                               "88 visits cycling layers 0..3 (22 updates per layer); 3 streams",
+                   "step": "one 88-visit sweep", "warm-up": "one visit per layer",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "gpu_launches": r["visits"],
+        "e2e": {"value": params / wall, "unit": "params/s", "h2d_bytes_per_step": link_bytes,
+                "d2h_bytes_per_step": link_bytes, "path": "sf_slide_window_step (the measured path itself)"},
+        "link": {"h2d_GBps": link_bytes / wall / 1e9, "d2h_GBps": link_bytes / wall / 1e9,
+                 "one_visit_alone_ms": {"h2d": r["t_h2d_ms"], "update": r["t_update_ms"], "d2h": r["t_d2h_ms"]},
+                 "overlap_efficiency": r["visits"] * bound / 1e3 / wall},
+        "roofline": {"bound": "host link", "kernel": "adamw_bulk_kernel (in the window)",
+                     "update_alone_GBps": upd_gbs, "update_frac_of_hbm_peak": upd_gbs / peak,
+                     "peak": peak, "peak_kind": kind},
+        "clocks": r["clocks"], "setup_s": r["setup_s"], "steps_per_layer": r["steps"],
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main_ours(args, rank, world):
     import torch
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
@@ -462,14 +605,30 @@ def main_ours(args, rank, world):
     value = world * res["params_per_step"] * args.steps / (total_ms / 1e3)
     lm = res["launch_ms"]
     avg_launch_ms = sum(lm) / len(lm)
-    bytes_per_launch = ADAM_BYTES_PER_PARAM * res["layer_params"]
-    achieved = bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
+    bytes_per_launch = ADAM_BYTES_PER_PARAM * sum(res["group_params"]) / len(res["group_params"])
+    # algorithmic bytes of all launches over their summed durations
+    achieved = ADAM_BYTES_PER_PARAM * sum(res["group_params"]) / (sum(lm) / 1e3) / 1e9
     peak, kind = measured_peak_hbm()
     # layers above 2^20 aligned elements run the bulk-copy kernel (one launch per layer)
     kname = "adamw_bulk_kernel"
     traffic = kernel_traffic(kname)
+    if args.workload == "llama2-7b":
+        metric = "params updated/s (fused AdamW, LLaMA-2-7B full step)"
+        cfg = {"workload": "LLaMA-2-7B: 32 layers (hidden 4096, SwiGLU FFN 11008) + embedding + LM head "
+                           "(vocab 32000) + final norm = 6,738,415,616 params resident in HBM, one fused AdamW "
+                           "launch per group in sliding order (head, norm, layers 31..0, embedding)",
+               "groups": len(workload_groups(args)), "params_per_step": res["params_per_step"],
+               "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+               "l2": "inputs larger than L2"}
+    else:
+        metric = "params updated/s (fused AdamW, OPT-1.3B stack)"
+        cfg = {"workload": "OPT-1.3B stack: 24 layers x 50,339,840 params (hidden 2048, FFN 8192, "
+                           "QKV/O/FC1/FC2 + 2 LayerNorms), one fused AdamW launch per layer",
+               "layers": args.layers, "params_per_step": res["params_per_step"],
+               "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+               "l2": "inputs larger than L2 (1.41 GB per launch)"}
     line = {
-        "metric": "params updated/s (fused AdamW, OPT-1.3B stack)",
+        "metric": metric,
         "value": value,
         "unit": "params/s",
         "n_gpus": world,
@@ -481,11 +640,7 @@ def main_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": "f32 (bf16 grad in, bf16 weight out)",
         "data": "synthetic (seeded N(0,1e-3) bf16 grads, N(0,0.02) fp32 masters)",
-        "config": {"workload": "OPT-1.3B stack: 24 layers x 50,339,840 params (hidden 2048, FFN 8192, "
-                               "QKV/O/FC1/FC2 + 2 LayerNorms), one fused AdamW launch per layer",
-                   "layers": args.layers, "params_per_step": res["params_per_step"],
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (1.41 GB per launch)"},
+        "config": cfg,
         "gpu_launches": res["launches"],
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -494,7 +649,7 @@ def main_ours(args, rank, world):
                      "traffic": traffic["bytes_per_launch"] if traffic else None},
         "clocks": res["clocks"],
     }
-    if not args.no_e2e:
+    if not args.no_e2e and args.workload == "opt-1.3b":
         e = run_e2e(args, world)
         wall = max_over_ranks(e["wall_s"], world)
         line["e2e"] = {"value": world * e["params_per_step"] * args.steps / wall, "unit": "params/s",
@@ -505,7 +660,7 @@ def main_ours(args, rank, world):
             line["e2e"]["link_probe"] = link_probe()
         except Exception as ex:
             line["e2e"]["link_probe"] = {"error": str(ex)[:200]}
-    if not args.no_lsp and rank == 0:
+    if not args.no_lsp and rank == 0 and args.workload == "opt-1.3b":
         try:
             line["lsp"] = run_lsp(args)
         except Exception as ex:  # the line still prints; the failure is recorded on it
@@ -559,6 +714,8 @@ def main():
     rank, world = dist_init(args)
     if args.impl == "reference":
         main_reference(args, rank, world)
+    elif args.workload == "mistral-window":
+        main_window(args, rank, world)
     else:
         main_ours(args, rank, world)
     if world > 1:
