@@ -512,21 +512,29 @@ __global__ void k_reduce_splits(const float* __restrict__ part, int splits, int6
 // Decompress kernels
 // ----------------------------------------------------------------------------
 
+constexpr int kVMaxK = 8;            // k_v keeps 32 x k entries per warp in shared memory
+
 __host__ __device__ __forceinline__ size_t v_ebuf_offset(int d) { return ((size_t)d * 65 * 4 + 15) / 16 * 16; }
+__host__ __device__ __forceinline__ size_t v_obuf_offset(int d) {
+  return v_ebuf_offset(d) + (size_t)8 * 32 * kVMaxK * 8;
+}
+__host__ __device__ __forceinline__ size_t v_smem_bytes(int d) { return v_obuf_offset(d) + (size_t)8 * 64 * 33 * 4; }
 
 // V[a][j] = sum_l q_{j,l} dS[a][c_{j,l}] for a in a 64-row block, j in 32-column tiles.
 // dS^T of the block sits in shared memory (st[c * 65 + aa], padded: the
 // transposing fill and the lane-along-a reads are both conflict-free); the
 // k entries of the tile's 32 Q rows are fetched with coalesced loads into a
-// per-warp buffer and read back as warp-uniform broadcasts.
+// per-warp buffer and read back as warp-uniform broadcasts; the 64 x 32
+// result tile goes through a padded per-warp buffer so that V is written
+// as coalesced 128-byte row segments.
 __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, const int32_t* __restrict__ qidx,
                                            const float* __restrict__ qval, int k, int64_t n,
                                            float* __restrict__ V, int tiles_per_warp) {
   extern __shared__ float st[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
-  // entry buffers start at the first 16-byte boundary after the tile (d * 65 floats)
-  int2* ebuf = reinterpret_cast<int2*>(reinterpret_cast<unsigned char*>(st) + v_ebuf_offset(d)) +
-               (size_t)warp * 32 * k;
+  unsigned char* sbytes = reinterpret_cast<unsigned char*>(st);
+  int2* ebuf = reinterpret_cast<int2*>(sbytes + v_ebuf_offset(d)) + (size_t)warp * 32 * kVMaxK;
+  float* obuf = reinterpret_cast<float*>(sbytes + v_obuf_offset(d)) + (size_t)warp * 64 * 33;
   const int a0 = blockIdx.x * kVRows;
   if ((d & 3) == 0 && (reinterpret_cast<uintptr_t>(dS) & 15) == 0) {
     // lanes along a (one dS row each), warps along 4-column groups: 16-byte
@@ -563,7 +571,6 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
   }
   __syncthreads();
   const int64_t n_tiles = (n + 31) / 32;
-  const bool vec = (n % 4) == 0 && (reinterpret_cast<uintptr_t>(V) % 16) == 0;
   for (int q = 0; q < tiles_per_warp; ++q) {
     const int64_t t = ((int64_t)blockIdx.y * nwarps + warp) * tiles_per_warp + q;
     if (t >= n_tiles) break;
@@ -574,37 +581,21 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
     for (int e = lane; e < ne; e += 32)
       ebuf[e] = make_int2(qidx[j0 * k + e], __float_as_int(qval[j0 * k + e]));
     __syncwarp();
-    float acc0[32], acc1[32];
-#pragma unroll
-    for (int jj = 0; jj < 32; ++jj) {
-      acc0[jj] = 0.0f;
-      acc1[jj] = 0.0f;
-      if (jj < rows_here) {
-        for (int l = 0; l < k; ++l) {
-          const int2 en = ebuf[jj * k + l];
-          const float qv = __int_as_float(en.y);
-          acc0[jj] = fmaf(qv, st[en.x * 65 + lane], acc0[jj]);
-          acc1[jj] = fmaf(qv, st[en.x * 65 + lane + 32], acc1[jj]);
-        }
+    for (int jj = 0; jj < rows_here; ++jj) {
+      float s0 = 0.0f, s1 = 0.0f;
+      for (int l = 0; l < k; ++l) {
+        const int2 en = ebuf[jj * k + l];
+        const float qv = __int_as_float(en.y);
+        s0 = fmaf(qv, st[en.x * 65 + lane], s0);
+        s1 = fmaf(qv, st[en.x * 65 + lane + 32], s1);
       }
+      obuf[lane * 33 + jj] = s0;
+      obuf[(lane + 32) * 33 + jj] = s1;
     }
-    const bool full_tile = rows_here == 32;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int a = a0 + lane + 32 * h;
-      if (a >= d) continue;
-      const float* acc = h ? acc1 : acc0;
-      float* o = V + (int64_t)a * n + j0;
-      if (vec && full_tile) {
-#pragma unroll
-        for (int jj = 0; jj < 32; jj += 4)
-          *reinterpret_cast<float4*>(o + jj) = make_float4(acc[jj], acc[jj + 1], acc[jj + 2], acc[jj + 3]);
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj)
-          if (jj < rows_here) o[jj] = acc[jj];
-      }
-    }
+    __syncwarp();
+    const int64_t j = j0 + lane;
+    if (lane < rows_here)
+      for (int aa = 0; aa < kVRows && a0 + aa < d; ++aa) V[(int64_t)(a0 + aa) * n + j] = obuf[aa * 33 + lane];
   }
 }
 
@@ -1414,17 +1405,23 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
     const int warps = 8;
     const int tpw = (int)std::max<int64_t>(1, (int64_t)n_ab * n_tiles / ((int64_t)warps * sf::kTargetCtas));
     const int64_t gy = ceil_div<int64_t>(n_tiles, (int64_t)warps * tpw);
-    const size_t smem_v = sf::v_ebuf_offset(d) + (size_t)warps * 32 * Q->k * 8;
-    static thread_local bool v_cfg = false;
-    if (!v_cfg) {
-      SF_CUDA_TRY(cudaFuncSetAttribute(sf::k_v, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)(sf::v_ebuf_offset(sf::kMaxFastD) + 8 * 32 * 32 * 8)),
-                  "cudaFuncSetAttribute(k_v)");
-      v_cfg = true;
+    if (Q->k <= sf::kVMaxK) {
+      const size_t smem_v = sf::v_smem_bytes(d);
+      static thread_local bool v_cfg = false;
+      if (!v_cfg) {
+        SF_CUDA_TRY(cudaFuncSetAttribute(sf::k_v, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sf::v_smem_bytes(sf::kMaxFastD)),
+                    "cudaFuncSetAttribute(k_v)");
+        v_cfg = true;
+      }
+      sf::k_v<<<dim3((unsigned)n_ab, (unsigned)gy), 32 * warps, smem_v, s>>>(dS, d, Q->ell_idx, Q->ell_val, Q->k, n,
+                                                                            V, tpw);
+      SF_TRY(sf::check_launch("k_v"));
+    } else {
+      const int64_t nv = (int64_t)d * n;
+      sf::k_v_generic<<<(unsigned)ceil_div<int64_t>(nv, 256), 256, 0, s>>>(dS, d, Q->ell_idx, Q->ell_val, Q->k, n, V);
+      SF_TRY(sf::check_launch("k_v_generic"));
     }
-    sf::k_v<<<dim3((unsigned)n_ab, (unsigned)gy), 32 * warps, smem_v, s>>>(dS, d, Q->ell_idx, Q->ell_val, Q->k, n, V,
-                                                                          tpw);
-    SF_TRY(sf::check_launch("k_v"));
 
     const size_t smem_a = (size_t)d * sf::kApplyCols * 4 + 16 * 32 * 8;
     const int64_t n_jb = ceil_div<int64_t>(n, sf::kApplyCols);

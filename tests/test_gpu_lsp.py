@@ -155,6 +155,7 @@ def test_compressed_adamw_three_steps():
 DECOMPRESS_CASES = [
     (1, 1, 1, 1), (7, 33, 8, 2), (64, 128, 16, 2), (100, 130, 8, 3), (1000, 1000, 64, 4),
     (333, 264, 512, 8), (129, 63, 12, 3), (40, 50, 600, 4),   # d > 512: generic path
+    (64, 96, 64, 16), (100, 72, 40, 12),                       # k > 8: generic V, fast apply
 ]
 
 
