@@ -94,6 +94,11 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
+def job_value(world, units_per_step_per_rank, steps, slowest_ms):
+    """Whole-job throughput: units all ranks processed over the slowest rank's time."""
+    return world * units_per_step_per_rank * steps / (slowest_ms / 1e3)
+
+
 def measured_peak_hbm():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -602,7 +607,7 @@ def main_ours(args, rank, world):
     res = run_resident(args, world)
     total_ms = max_over_ranks(res["total_ms"], world)
     ms_per_step = total_ms / args.steps
-    value = world * res["params_per_step"] * args.steps / (total_ms / 1e3)
+    value = job_value(world, res["params_per_step"], args.steps, total_ms)
     lm = res["launch_ms"]
     avg_launch_ms = sum(lm) / len(lm)
     bytes_per_launch = ADAM_BYTES_PER_PARAM * sum(res["group_params"]) / len(res["group_params"])
