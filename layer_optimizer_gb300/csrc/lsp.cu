@@ -359,10 +359,11 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
     if (lane == 0) {
       const int2* gd_row = A.gdesc + (int64_t)blockIdx.y * A.n_win;
       int it = 0;
+      int s = 0;                 // stage of window it, and the phase parity of its ring pass
+      uint32_t pass = 0;
       int2 gd = nw > 0 ? gd_row[w_begin] : make_int2(0, 0);
       for (; it < nw; ++it) {
-        const int s = it % S;
-        if (it >= S && !mbar_wait(&empty[s], ((uint32_t)(it / S) & 1u) ^ 1u)) {
+        if (it >= S && !mbar_wait(&empty[s], pass ^ 1u)) {
           flags[1] = 1;
           break;
         }
@@ -377,6 +378,10 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
         bulk_load(st + A.wsl_off, A.wptr + (int64_t)w * A.dp + a_cta, (uint32_t)A.wbytes, &full[s]);
         if (gd.y > 0) bulk_load(st + A.ent_off, A.went + gd.x, (uint32_t)gd.y, &full[s]);
         if (it + 1 < nw) gd = gd_row[w + 1];
+        if (++s == S) {
+          s = 0;
+          pass ^= 1u;
+        }
       }
       flags[0] = it;
     }
@@ -393,9 +398,10 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[sl][j] = 0.0f;
     bool failed = false;
+    int s = 0;
+    uint32_t pass = 0;
     for (int it = 0; it < nw; ++it) {
-      const int s = it % S;
-      if (!mbar_wait(&full[s], (uint32_t)(it / S) & 1u)) {
+      if (!mbar_wait(&full[s], pass)) {
         failed = true;
         flags[1] = 1;
         break;
@@ -447,6 +453,10 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
         } else {
           mbar_arrive_local(&empty[s]);
         }
+      }
+      if (++s == S) {
+        s = 0;
+        pass ^= 1u;
       }
     }
 
@@ -799,13 +809,14 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
     // producer
     if (lane == 0) {
       int64_t q = 0;
+      int s = 0;                 // stage and ring-pass parity, advanced without divisions
+      uint32_t pass = 0;
+      int64_t jb = it0 / A.n_rt, rt = it0 % A.n_rt;
       for (; q < nit; ++q) {
-        const int s = (int)(q % S);
-        if (q >= S && !mbar_wait(&empty[s], (uint32_t)((q / S) & 1) ^ 1u)) {
+        if (q >= S && !mbar_wait(&empty[s], pass ^ 1u)) {
           shared_flags[1] = 1;
           break;
         }
-        const int64_t item = it0 + q, jb = item / A.n_rt, rt = item % A.n_rt;
         const int rows_here = (int)imin64(kApplyRows, A.m - rt * kApplyRows);
         const uint32_t eb = (uint32_t)((rows_here * k * 4 + 15) / 16 * 16);
         unsigned char* st = stages + (size_t)s * A.stage_stride;
@@ -813,6 +824,14 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
         tma_load_2d(st, &wmap, &full[s], (int)(jb * kApplyCols), (int)(rt * kApplyRows));
         bulk_load(st + A.tile_bytes, A.pidx + rt * kApplyRows * k, eb, &full[s]);
         bulk_load(st + A.tile_bytes + A.ent_stride, A.pval + rt * kApplyRows * k, eb, &full[s]);
+        if (++s == S) {
+          s = 0;
+          pass ^= 1u;
+        }
+        if (++rt == A.n_rt) {
+          rt = 0;
+          ++jb;
+        }
       }
       shared_flags[0] = (int32_t)q;
     }
@@ -822,8 +841,14 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
     bool failed = false;
     const uint32_t stages_base = smem_u32(stages);
     const uint32_t vs_lane = smem_u32(vs) + 8u * (uint32_t)lane;
+    int s = 0;
+    uint32_t pass = 0;
+    int64_t jb = it0 / A.n_rt, rt = it0 % A.n_rt;
     for (int64_t q = 0; q < nit; ++q) {
-      const int64_t item = it0 + q, jb = item / A.n_rt, rt = item % A.n_rt;
+      if (q > 0 && ++rt == A.n_rt) {
+        rt = 0;
+        ++jb;
+      }
       const int64_t j0 = jb * kApplyCols;
       if (jb != cur_jb) {
         named_bar_sync(1, 32 * kApplyConsumerWarps);
@@ -834,15 +859,20 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
         named_bar_sync(1, 32 * kApplyConsumerWarps);
         cur_jb = jb;
       }
-      const int s = (int)(q % S);
-      if (!failed && !mbar_wait(&full[s], (uint32_t)(q / S) & 1u)) {
+      const int cur_s = s;
+      const uint32_t cur_pass = pass;
+      if (++s == S) {
+        s = 0;
+        pass ^= 1u;
+      }
+      if (!failed && !mbar_wait(&full[cur_s], cur_pass)) {
         failed = true;
         shared_flags[1] = 1;
       }
       if (failed) continue;
       // 32-bit shared addresses: W tile row r at st + r * 64 * esize, entry
       // arrays after it, V block row a at vs_lane + a * 256
-      const uint32_t st = stages_base + (uint32_t)s * (uint32_t)A.stage_stride;
+      const uint32_t st = stages_base + (uint32_t)cur_s * (uint32_t)A.stage_stride;
       const uint32_t eidx = st + (uint32_t)A.tile_bytes;
       const uint32_t evals = eidx + (uint32_t)A.ent_stride;
       const int64_t j = j0 + 2 * lane;
@@ -945,7 +975,7 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_local(&empty[s]);
+      if (lane == 0) mbar_arrive_local(&empty[cur_s]);
     }
   }
   __syncthreads();
