@@ -217,6 +217,8 @@ __global__ void __launch_bounds__(32 * (kBulkConsumerWarps + 1), 1)
     fence_mbar_init_cluster();
   }
   __syncthreads();
+  griddep_launch_dependents();
+  griddep_wait();                // every thread: loads and stores below touch caller memory
   const int G = gridDim.x;
   const int n_my = (int)blockIdx.x < B.total_chunks ? (B.total_chunks - (int)blockIdx.x + G - 1) / G : 0;
 
@@ -308,6 +310,8 @@ __global__ void __launch_bounds__(32 * (kBulkConsumerWarps + 1), 1)
 __global__ void __launch_bounds__(kThreads)
 adamw_compressed_kernel(const float* __restrict__ S, float* __restrict__ m, float* __restrict__ v,
                         float* __restrict__ dS, int64_t n, AdamConsts c) {
+  griddep_launch_dependents();
+  griddep_wait();                // S comes from the compress kernels
   for (int64_t e = (int64_t)blockIdx.x * kThreads + threadIdx.x; e < n;
        e += (int64_t)gridDim.x * kThreads) {
     const float g = S[e];
@@ -449,8 +453,8 @@ sf_status adamw_layer_step_impl(const sf_tensor* tensors, int n_tensors, const s
       }
       if (B.nt > 0) {
         const int grid = (int)std::min<int64_t>(chunks, sm_count());
-        adamw_bulk_kernel<<<grid, 32 * (kBulkConsumerWarps + 1), smem, stream>>>(B);
-        SF_TRY(check_launch("adamw_bulk_kernel"));
+        SF_CUDA_TRY(launch_pdl(adamw_bulk_kernel, dim3(grid), dim3(32 * (kBulkConsumerWarps + 1)), smem, stream, B),
+                    "launch adamw_bulk_kernel");
       }
       if (!scalar_work) continue;
       L.total_tiles = (int32_t)rtiles;
@@ -474,8 +478,9 @@ sf_status adamw_compressed_impl(const float* S, float* m, float* v, float* dS, i
   SF_TRY(make_adam_consts(hp, step, false, &c));
   if (n == 0) return SF_OK;
   const int64_t blocks = std::min<int64_t>(ceil_div<int64_t>(n, kThreads), (int64_t)sm_count() * 8);
-  adamw_compressed_kernel<<<(int)blocks, kThreads, 0, stream>>>(S, m, v, dS, n, c);
-  return check_launch("adamw_compressed_kernel");
+  SF_CUDA_TRY(launch_pdl(adamw_compressed_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, S, m, v, dS, n, c),
+              "launch adamw_compressed_kernel");
+  return SF_OK;
 }
 
 int read_and_clear_device_error_adamw() {

@@ -44,6 +44,25 @@ inline sf_status check_launch(const char* what) {
   return e == cudaSuccess ? SF_OK : cuda_fail(e, what);
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled
+// while the previous kernel in the stream drains; it must call
+// griddepcontrol.wait before touching memory that kernel may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // fp32 constants of one AdamW step, derived in double and rounded once.
 struct AdamConsts {
   float beta1, one_minus_beta1;

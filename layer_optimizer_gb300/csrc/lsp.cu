@@ -350,6 +350,7 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
     fence_mbar_init_cluster();
   }
   if (C > 1) cluster_sync(); else __syncthreads();
+  griddep_launch_dependents();
 
   if (warp == ncw) {
     // Producer: one stage = the B tile of a window (rows split over the
@@ -358,6 +359,7 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
     // CTA in the cluster has released it.
     if (lane == 0) {
       const int2* gd_row = A.gdesc + (int64_t)blockIdx.y * A.n_win;
+      griddep_wait();            // B may be the previous kernel's output
       int it = 0;
       int s = 0;                 // stage of window it, and the phase parity of its ring pass
       uint32_t pass = 0;
@@ -511,6 +513,8 @@ __global__ void k_gather_generic(const TB* __restrict__ B, int64_t ldb, int64_t 
 // out[e] = sum over splits s = 0, 1, ... of part[s][e], in that order.
 __global__ void k_reduce_splits(const float* __restrict__ part, int splits, int64_t stride, int64_t n,
                                 float* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
     float s = 0.0f;
     for (int k = 0; k < splits; ++k) s += part[k * stride + e];
@@ -546,6 +550,8 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
   int2* ebuf = reinterpret_cast<int2*>(sbytes + v_ebuf_offset(d)) + (size_t)warp * 32 * kVMaxK;
   float* obuf = reinterpret_cast<float*>(sbytes + v_obuf_offset(d)) + (size_t)warp * 64 * 33;
   const int a0 = blockIdx.x * kVRows;
+  griddep_launch_dependents();
+  griddep_wait();                // dS comes from the compressed step
   if ((d & 3) == 0 && (reinterpret_cast<uintptr_t>(dS) & 15) == 0) {
     // lanes along a (one dS row each), warps along 4-column groups: 16-byte
     // loads, 8 in flight per thread; the transposing stores hit 32 distinct banks
@@ -801,6 +807,8 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
     fence_mbar_init_cluster();
   }
   __syncthreads();
+  griddep_launch_dependents();
+  griddep_wait();                // V, W and P may be written by earlier kernels in the stream
   const int64_t it0 = (int64_t)blockIdx.x * A.per_cta;
   const int64_t nit = imax64(0, imin64(A.total, it0 + A.per_cta) - it0);
   const int k = A.k;
@@ -1141,19 +1149,23 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   cfg.blockDim = dim3(32 * (p.warps + 1));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = (unsigned)p.cluster;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gather_t<TB>, map, A), "launch k_gather_t");
   if (p.splits > 1) {
     const int64_t n_out = ncols * d;
     const int blocks = (int)std::min<int64_t>(ceil_div<int64_t>(n_out, 256), (int64_t)sm_count() * 4);
-    k_reduce_splits<<<blocks, 256, 0, stream>>>(yt_partial, p.splits, n_out, n_out, yt_final);
-    return check_launch("k_reduce_splits");
+    SF_CUDA_TRY(launch_pdl(k_reduce_splits, dim3(blocks), dim3(256), 0, stream, yt_partial, p.splits, n_out, n_out,
+                           yt_final),
+                "launch k_reduce_splits");
+    return SF_OK;
   }
   return SF_OK;
 }
@@ -1444,9 +1456,9 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
                     "cudaFuncSetAttribute(k_v)");
         v_cfg = true;
       }
-      sf::k_v<<<dim3((unsigned)n_ab, (unsigned)gy), 32 * warps, smem_v, s>>>(dS, d, Q->ell_idx, Q->ell_val, Q->k, n,
-                                                                            V, tpw);
-      SF_TRY(sf::check_launch("k_v"));
+      SF_CUDA_TRY(sf::launch_pdl(sf::k_v, dim3((unsigned)n_ab, (unsigned)gy), dim3(32 * warps), smem_v, s, dS, d,
+                                 Q->ell_idx, Q->ell_val, Q->k, n, V, tpw),
+                  "launch k_v");
     } else {
       const int64_t nv = (int64_t)d * n;
       sf::k_v_generic<<<(unsigned)ceil_div<int64_t>(nv, 256), 256, 0, s>>>(dS, d, Q->ell_idx, Q->ell_val, Q->k, n, V);
@@ -1515,8 +1527,10 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
                       "cudaFuncSetAttribute(k_apply_tma)");
           t_cfg[bf16w] = true;
         }
-        kt<<<(unsigned)ceil_div<int64_t>(A.total, A.per_cta), 32 * (sf::kApplyConsumerWarps + 1), smem2, s>>>(wmap, A);
-        return sf::check_launch("k_apply_tma");
+        SF_CUDA_TRY(sf::launch_pdl(kt, dim3((unsigned)ceil_div<int64_t>(A.total, A.per_cta)),
+                                   dim3(32 * (sf::kApplyConsumerWarps + 1)), smem2, s, wmap, A),
+                    "launch k_apply_tma");
+        return SF_OK;
       }
     }
     const int R = std::min(sf::kApplyMaxR, 32 / P->k);

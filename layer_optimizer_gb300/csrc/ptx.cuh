@@ -148,6 +148,15 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
   return v;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue once every CTA of this one has passed this point ...
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// ... and, in that next kernel, wait until the previous one has completed and
+// its memory is visible.  Both are no-ops for a normal launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
