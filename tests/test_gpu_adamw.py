@@ -192,3 +192,35 @@ def test_opt13_stack_sampled():
             check_close("v", b[3][ix], st.v, st.v_abs, TOL_STATE)
             check_bf16("w", bits(b[4][ix]), st.theta)
         del bufs
+
+
+def test_checkpoint_resume_bitwise():
+    """Three steps uninterrupted equal: one step, save to host, reload into new buffers, two steps."""
+    n = 200003
+    grads = [synth.normal((n,), 1e-3, synth.sub_seed(21, t), dtype=torch.bfloat16) for t in (1, 2, 3)]
+    hp = native.hparams(**HP)
+
+    def fresh(theta, m=None, v=None):
+        return [torch.empty(n, dtype=torch.bfloat16, device=DEV), theta.to(DEV).clone(),
+                (torch.zeros(n) if m is None else m).to(DEV).clone(),
+                (torch.zeros(n) if v is None else v).to(DEV).clone(),
+                torch.empty(n, dtype=torch.bfloat16, device=DEV)]
+
+    theta0 = synth.normal((n,), 0.02, 22)
+    a = fresh(theta0)
+    for t in (1, 2, 3):
+        a[0].copy_(grads[t - 1])
+        native.sf_adamw_layer_step([native.make_tensor(*a)], hp, t)
+    b = fresh(theta0)
+    b[0].copy_(grads[0])
+    native.sf_adamw_layer_step([native.make_tensor(*b)], hp, 1)
+    saved = [x.cpu().clone() for x in b[1:4]]            # the caller-owned state: master, m, v (and t = 1)
+    del b
+    c = fresh(*saved)
+    for t in (2, 3):
+        c[0].copy_(grads[t - 1])
+        native.sf_adamw_layer_step([native.make_tensor(*c)], hp, t)
+    torch.cuda.synchronize()
+    for x, y in zip(a[1:4], c[1:4]):
+        assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+    assert torch.equal(a[4].view(torch.int16), c[4].view(torch.int16))

@@ -1,0 +1,96 @@
+"""The oracle's pins catch plausible mistakes (CPU only).
+
+Each test plants one mistake in a copy of the oracle's arithmetic, on the
+CPU, and checks that a pin that holds for the real oracle fails for the
+broken one.  Nothing here touches the CUDA path.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from layer_optimizer_gb300 import synth
+from oracle import adamw as oa
+from oracle import lsp as ol
+
+HP = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
+
+
+def _torch_adamw_theta(th, grads):
+    p = torch.nn.Parameter(torch.from_numpy(th.copy()))
+    opt = torch.optim.AdamW([p], lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"],
+                            weight_decay=HP["weight_decay"], foreach=False)
+    for g in grads:
+        p.grad = torch.from_numpy(g.copy())
+        opt.step()
+    return p.detach().numpy()
+
+
+def _broken_step(kind):
+    def step(state, g, t, lr, beta1, beta2, eps, weight_decay):
+        g = np.asarray(g, dtype=np.float64)
+        bc1, bc2 = 1 - beta1 ** t, 1 - beta2 ** t
+        if kind == "no_bias_correction":
+            bc1 = bc2 = 1.0
+        if kind == "eps_inside_sqrt":
+            m = beta1 * state.m + (1 - beta1) * g
+            v = beta2 * state.v + (1 - beta2) * g * g
+            state.theta = state.theta * (1 - lr * weight_decay) - lr * (m / bc1) / np.sqrt(v / bc2 + eps)
+            state.m, state.v = m, v
+            return
+        if kind == "coupled_decay":
+            g = g + weight_decay * state.theta
+            decay = 1.0
+        else:
+            decay = 1 - lr * weight_decay
+        m = beta1 * state.m + (1 - beta1) * g
+        v = beta2 * state.v + (1 - beta2) * (g if kind == "v_not_squared" else g * g)
+        state.theta = state.theta * decay - lr * (m / bc1) / (np.sqrt(v / bc2) + eps)
+        state.m, state.v = m, v
+    return step
+
+
+@pytest.mark.parametrize("kind", ["no_bias_correction", "eps_inside_sqrt", "coupled_decay", "v_not_squared"])
+def test_planted_adamw_mistakes_fail_a_pin(kind):
+    rng = np.random.default_rng(3)
+    th = rng.standard_normal(2000) * 0.02
+    grads = [np.abs(rng.standard_normal(2000)) * 1e-3 + 1e-4 for _ in range(3)]
+    ref = _torch_adamw_theta(th, grads)
+    good, bad = oa.AdamWState(th), oa.AdamWState(th)
+    for t, g in enumerate(grads, start=1):
+        oa.adamw_step(good, g, t, **HP)
+        _broken_step(kind)(bad, g, t, **HP)
+    assert np.allclose(good.theta, ref, rtol=1e-12, atol=1e-18)
+    assert not np.allclose(bad.theta, ref, rtol=1e-9, atol=1e-15)
+
+
+def _brute(P, Q, G):
+    S = np.zeros((P.d, Q.d))
+    for i in range(G.shape[0]):
+        for li in range(P.k):
+            for j in range(G.shape[1]):
+                for lj in range(Q.k):
+                    S[P.idx[i, li], Q.idx[j, lj]] += P.val[i, li] * G[i, j] * Q.val[j, lj]
+    return S
+
+
+@pytest.mark.parametrize("kind", ["transposed_G", "Q_for_P", "dropped_value", "wrong_sign"])
+def test_planted_compress_mistakes_fail_brute_force(kind):
+    rng = np.random.default_rng(4)
+    m = n = 12
+    d, k = 6, 2
+    Pi, Pv = synth.projector(m, d, k, 1)
+    Qi, Qv = synth.projector(n, d, k, 2)
+    P, Q = ol.Projector(Pi, Pv, d), ol.Projector(Qi, Qv, d)
+    G = rng.standard_normal((m, n))
+    Pd, Qd = P.dense(), Q.dense()
+    broken = {
+        "transposed_G": Pd.T @ G.T @ Qd,
+        "Q_for_P": Qd.T @ G @ Qd,
+        "dropped_value": (Pd != 0).T.astype(float) @ G @ Qd,
+        "wrong_sign": -(Pd.T @ G @ Qd),
+    }[kind]
+    want = _brute(P, Q, G)
+    S, _ = ol.compress(P, Q, G)
+    assert np.allclose(S, want, rtol=1e-12, atol=1e-12)
+    assert not np.allclose(broken, want, rtol=1e-6, atol=1e-9)
