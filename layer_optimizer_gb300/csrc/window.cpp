@@ -11,9 +11,14 @@
 // window for the update step: a visit copies one layer into a free slot
 // (h2d stream), updates it (compute stream), and copies it back (d2h
 // stream).  Visits to different slots run concurrently, so the copy
-// engines in both directions and the HBM-bound kernel overlap.  It does no
-// arithmetic of its own; dependencies are CUDA events only, and the host
-// never blocks while enqueueing.
+// engines in both directions and the HBM-bound kernel overlap.  Inside a
+// visit the layer moves in groups of consecutive tensors (at least
+// kGroupParams parameters each, or the rest of the layer): a group's update
+// starts as soon as that group has arrived, its write-back as soon as it is
+// updated, and the next visit to the slot may overwrite a tensor as soon as
+// that tensor's write-back has ended.  It does no arithmetic of its own;
+// dependencies are CUDA events only, and the host never blocks while
+// enqueueing.
 #include <algorithm>
 #include <new>
 #include <vector>
@@ -31,6 +36,8 @@ struct sf_window_s {
   int n_tensors = 0;
   std::vector<std::vector<sf_tensor>> slots;
   cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  // per (slot, tensor): copies of the group starting at that tensor landed /
+  // its update ended / that tensor's write-back ended
   std::vector<cudaEvent_t> ev_in, ev_done, ev_free;
   std::vector<bool> slot_used;
   std::vector<cudaEvent_t> ev_layer;   // write-back of a host layer has landed
@@ -39,6 +46,8 @@ struct sf_window_s {
 };
 
 namespace {
+
+constexpr int64_t kGroupParams = int64_t(16) << 20;
 
 // Test hook: the n-th copy enqueue (1-based) fails once; 0 = off.
 int64_t g_fail_copy_at = 0;
@@ -118,14 +127,15 @@ sf_status sf_window_create(int n_slots, const sf_tensor* const* device_slots, in
     }
     w->slots.emplace_back(device_slots[s], device_slots[s] + n_tensors_per_slot);
   }
-  w->ev_in.assign(n_slots, nullptr);
-  w->ev_done.assign(n_slots, nullptr);
-  w->ev_free.assign(n_slots, nullptr);
+  const int ne = n_slots * std::max(1, n_tensors_per_slot);
+  w->ev_in.assign(ne, nullptr);
+  w->ev_done.assign(ne, nullptr);
+  w->ev_free.assign(ne, nullptr);
   w->slot_used.assign(n_slots, false);
-  for (int s = 0; s < n_slots; ++s) {
+  for (int e = 0; e < ne; ++e) {
     sf_status st = SF_OK;
-    if ((st = new_event(&w->ev_in[s])) != SF_OK || (st = new_event(&w->ev_done[s])) != SF_OK ||
-        (st = new_event(&w->ev_free[s])) != SF_OK) {
+    if ((st = new_event(&w->ev_in[e])) != SF_OK || (st = new_event(&w->ev_done[e])) != SF_OK ||
+        (st = new_event(&w->ev_free[e])) != SF_OK) {
       destroy_events(w);
       delete w;
       return st;
@@ -165,46 +175,60 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
     const int s = (int)(w->visits % w->n_slots);
     const sf_host_layer& L = layers[l];
     const std::vector<sf_tensor>& slot = w->slots[s];
+    const int eb = s * w->n_tensors;          // this slot's events
+    const int64_t step = steps[l] + 1;
 
-    // h2d: slot free, previous write-back of this layer landed, then copy in.
-    if (w->slot_used[s]) SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_free[s], 0), "wait slot free");
+    // the previous write-back of this layer must have landed before it is read again
     if (w->layer_pending[l])
       SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_layer[l], 0), "wait layer write-back");
-    for (int t = 0; t < L.n_tensors; ++t) {
-      const sf_tensor& h = L.tensors[t];
-      const size_t n = (size_t)h.numel;
-      SF_TRY(copy_async(const_cast<void*>(slot[t].grad), h.grad, 2 * n, cudaMemcpyHostToDevice, w->h2d, "h2d grad"));
-      SF_TRY(copy_async(slot[t].master, h.master, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d master"));
-      SF_TRY(copy_async(slot[t].exp_avg, h.exp_avg, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg"));
-      SF_TRY(copy_async(slot[t].exp_avg_sq, h.exp_avg_sq, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg_sq"));
+    int t0 = 0;
+    while (t0 < L.n_tensors) {
+      int t1 = t0;
+      int64_t params = 0;
+      while (t1 < L.n_tensors && (params < kGroupParams || t1 == t0)) params += L.tensors[t1++].numel;
+
+      // h2d: the slot's tensors of this group are free, then copy in
+      if (w->slot_used[s])
+        for (int t = t0; t < t1; ++t)
+          SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_free[eb + t], 0), "wait slot tensor free");
+      for (int t = t0; t < t1; ++t) {
+        const sf_tensor& h = L.tensors[t];
+        const size_t n = (size_t)h.numel;
+        SF_TRY(copy_async(const_cast<void*>(slot[t].grad), h.grad, 2 * n, cudaMemcpyHostToDevice, w->h2d, "h2d grad"));
+        SF_TRY(copy_async(slot[t].master, h.master, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d master"));
+        SF_TRY(copy_async(slot[t].exp_avg, h.exp_avg, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg"));
+        SF_TRY(copy_async(slot[t].exp_avg_sq, h.exp_avg_sq, 4 * n, cudaMemcpyHostToDevice, w->h2d,
+                          "h2d exp_avg_sq"));
+      }
+      SF_CUDA_TRY(cudaEventRecord(w->ev_in[eb + t0], w->h2d), "record ev_in");
+
+      // compute: the fused update of the group
+      SF_CUDA_TRY(cudaStreamWaitEvent(w->comp, w->ev_in[eb + t0], 0), "wait ev_in");
+      for (int t = t0; t < t1; ++t) {
+        dev[t] = slot[t];
+        dev[t].numel = L.tensors[t].numel;
+        if (!L.tensors[t].weight) dev[t].weight = nullptr;
+      }
+      SF_TRY(sf::adamw_layer_step_impl(dev.data() + t0, t1 - t0, hp, step, w->comp));
+      SF_CUDA_TRY(cudaEventRecord(w->ev_done[eb + t0], w->comp), "record ev_done");
+
+      // d2h: write the group back; each tensor of the slot is free when its copies end
+      SF_CUDA_TRY(cudaStreamWaitEvent(w->d2h, w->ev_done[eb + t0], 0), "wait ev_done");
+      for (int t = t0; t < t1; ++t) {
+        const sf_tensor& h = L.tensors[t];
+        const size_t n = (size_t)h.numel;
+        SF_TRY(copy_async(h.master, slot[t].master, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h master"));
+        SF_TRY(copy_async(h.exp_avg, slot[t].exp_avg, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg"));
+        SF_TRY(copy_async(h.exp_avg_sq, slot[t].exp_avg_sq, 4 * n, cudaMemcpyDeviceToHost, w->d2h,
+                          "d2h exp_avg_sq"));
+        if (h.weight)
+          SF_TRY(copy_async(h.weight, slot[t].weight, 2 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h weight"));
+        SF_CUDA_TRY(cudaEventRecord(w->ev_free[eb + t], w->d2h), "record ev_free");
+      }
+      t0 = t1;
     }
-    SF_CUDA_TRY(cudaEventRecord(w->ev_in[s], w->h2d), "record ev_in");
     w->slot_used[s] = true;
-
-    // compute: the fused update on the slot.
-    SF_CUDA_TRY(cudaStreamWaitEvent(w->comp, w->ev_in[s], 0), "wait ev_in");
-    for (int t = 0; t < L.n_tensors; ++t) {
-      dev[t] = slot[t];
-      dev[t].numel = L.tensors[t].numel;
-      if (!L.tensors[t].weight) dev[t].weight = nullptr;
-    }
-    const int64_t step = steps[l] + 1;
-    SF_TRY(sf::adamw_layer_step_impl(dev.data(), L.n_tensors, hp, step, w->comp));
     steps[l] = step;
-    SF_CUDA_TRY(cudaEventRecord(w->ev_done[s], w->comp), "record ev_done");
-
-    // d2h: write the layer back; the slot is free when these copies end.
-    SF_CUDA_TRY(cudaStreamWaitEvent(w->d2h, w->ev_done[s], 0), "wait ev_done");
-    for (int t = 0; t < L.n_tensors; ++t) {
-      const sf_tensor& h = L.tensors[t];
-      const size_t n = (size_t)h.numel;
-      SF_TRY(copy_async(h.master, slot[t].master, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h master"));
-      SF_TRY(copy_async(h.exp_avg, slot[t].exp_avg, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg"));
-      SF_TRY(copy_async(h.exp_avg_sq, slot[t].exp_avg_sq, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg_sq"));
-      if (h.weight)
-        SF_TRY(copy_async(h.weight, slot[t].weight, 2 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h weight"));
-    }
-    SF_CUDA_TRY(cudaEventRecord(w->ev_free[s], w->d2h), "record ev_free");
     SF_CUDA_TRY(cudaEventRecord(w->ev_layer[l], w->d2h), "record ev_layer");
     w->layer_pending[l] = true;
     ++w->visits;
