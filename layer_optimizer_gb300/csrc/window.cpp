@@ -36,9 +36,12 @@ struct sf_window_s {
   int n_tensors = 0;
   std::vector<std::vector<sf_tensor>> slots;
   cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
-  // per (slot, tensor): copies of the group starting at that tensor landed /
-  // its update ended / that tensor's write-back ended
+  // per (slot, tensor): events of the group that starts at that tensor:
+  // its copies landed / its update ended / its write-back ended
   std::vector<cudaEvent_t> ev_in, ev_done, ev_free;
+  // per (slot, tensor): index (into ev_free) of the write-back event of the
+  // group that last held that tensor of the slot; -1 = never used
+  std::vector<int> free_ev;
   std::vector<bool> slot_used;
   std::vector<cudaEvent_t> ev_layer;   // write-back of a host layer has landed
   std::vector<bool> layer_pending;
@@ -47,7 +50,7 @@ struct sf_window_s {
 
 namespace {
 
-constexpr int64_t kGroupParams = int64_t(16) << 20;
+constexpr int64_t kGroupParams = int64_t(64) << 20;
 
 // Test hook: the n-th copy enqueue (1-based) fails once; 0 = off.
 int64_t g_fail_copy_at = 0;
@@ -132,6 +135,7 @@ sf_status sf_window_create(int n_slots, const sf_tensor* const* device_slots, in
   w->ev_done.assign(ne, nullptr);
   w->ev_free.assign(ne, nullptr);
   w->slot_used.assign(n_slots, false);
+  w->free_ev.assign(ne, -1);
   for (int e = 0; e < ne; ++e) {
     sf_status st = SF_OK;
     if ((st = new_event(&w->ev_in[e])) != SF_OK || (st = new_event(&w->ev_done[e])) != SF_OK ||
@@ -187,10 +191,14 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
       int64_t params = 0;
       while (t1 < L.n_tensors && (params < kGroupParams || t1 == t0)) params += L.tensors[t1++].numel;
 
-      // h2d: the slot's tensors of this group are free, then copy in
-      if (w->slot_used[s])
-        for (int t = t0; t < t1; ++t)
-          SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_free[eb + t], 0), "wait slot tensor free");
+      // h2d: the slot's tensors of this group are free (one wait per distinct
+      // earlier group that held them), then copy in
+      int last = -2;
+      for (int t = t0; t < t1; ++t) {
+        const int e = w->free_ev[eb + t];
+        if (e >= 0 && e != last) SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_free[e], 0), "wait slot tensor free");
+        last = e;
+      }
       for (int t = t0; t < t1; ++t) {
         const sf_tensor& h = L.tensors[t];
         const size_t n = (size_t)h.numel;
@@ -223,8 +231,9 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
                           "d2h exp_avg_sq"));
         if (h.weight)
           SF_TRY(copy_async(h.weight, slot[t].weight, 2 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h weight"));
-        SF_CUDA_TRY(cudaEventRecord(w->ev_free[eb + t], w->d2h), "record ev_free");
       }
+      SF_CUDA_TRY(cudaEventRecord(w->ev_free[eb + t0], w->d2h), "record ev_free");
+      for (int t = t0; t < t1; ++t) w->free_ev[eb + t] = eb + t0;
       t0 = t1;
     }
     w->slot_used[s] = true;
