@@ -359,6 +359,22 @@ def run_e2e(args, world):
     for _ in range(max(1, args.warmup)):
         native.sf_slide_window_step(win, hl, order, hp, steps)
     win.sync()
+    # the same pinned buffers copied with plain bidirectional copies (no
+    # engine, no kernel, no events): the link rate these buffers allow
+    torch.cuda.synchronize()
+    tr = time.perf_counter()
+    for li, L in enumerate(host):
+        sl = slots[li % 2]
+        with torch.cuda.stream(streams[0]):
+            for h, dv in zip(L, sl):
+                for k in range(4):
+                    dv[k][:h[k].numel()].copy_(h[k], non_blocking=True)
+        with torch.cuda.stream(streams[2]):
+            for h, dv in zip(L, slots[(li + 1) % 2]):
+                for k in (1, 2, 3, 4):
+                    h[k].copy_(dv[k][:h[k].numel()], non_blocking=True)
+    torch.cuda.synchronize()
+    raw_s = time.perf_counter() - tr
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(args.steps):
@@ -370,7 +386,8 @@ def run_e2e(args, world):
     win.close()
     del host, slots
     torch.cuda.empty_cache()
-    return dict(wall_s=wall, params_per_step=params, h2d=14 * params, d2h=14 * params)
+    return dict(wall_s=wall, params_per_step=params, h2d=14 * params, d2h=14 * params,
+                raw_copy_GBps_each_way=14 * params / raw_s / 1e9)
 
 
 def run_lsp(args, matrices=None):
@@ -694,7 +711,8 @@ def main_ours(args, rank, world):
         line["e2e"] = {"value": world * e["params_per_step"] * args.steps / wall, "unit": "params/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
                        "path": "sf_slide_window_step: 24 pinned host layers, 2 device slots, 3 streams",
-                       "link_GBps_each_way": e["h2d"] * args.steps / wall / 1e9}
+                       "link_GBps_each_way": e["h2d"] * args.steps / wall / 1e9,
+                       "same_buffers_plain_copies_GBps_each_way": e["raw_copy_GBps_each_way"]}
         try:
             line["e2e"]["link_probe"] = link_probe()
         except Exception as ex:
