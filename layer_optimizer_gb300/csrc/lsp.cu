@@ -597,7 +597,28 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
     for (int e = lane; e < ne; e += 32)
       ebuf[e] = make_int2(qidx[j0 * k + e], __float_as_int(qval[j0 * k + e]));
     __syncwarp();
-    for (int jj = 0; jj < rows_here; ++jj) {
+    // four columns at a time: four independent load-multiply chains per warp
+    int jj = 0;
+    for (; jj + 4 <= rows_here; jj += 4) {
+      float s[4][2];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) s[u][0] = s[u][1] = 0.0f;
+      for (int l = 0; l < k; ++l) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int2 en = ebuf[(jj + u) * k + l];
+          const float qv = __int_as_float(en.y);
+          s[u][0] = fmaf(qv, st[en.x * 65 + lane], s[u][0]);
+          s[u][1] = fmaf(qv, st[en.x * 65 + lane + 32], s[u][1]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        obuf[lane * 33 + jj + u] = s[u][0];
+        obuf[(lane + 32) * 33 + jj + u] = s[u][1];
+      }
+    }
+    for (; jj < rows_here; ++jj) {
       float s0 = 0.0f, s1 = 0.0f;
       for (int l = 0; l < k; ++l) {
         const int2 en = ebuf[jj * k + l];
