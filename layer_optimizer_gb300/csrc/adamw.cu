@@ -11,14 +11,18 @@
 // 4 B read and written, 2 B weight) and does ~15 flops, one sqrt and one
 // divide, so HBM bandwidth bounds it.
 //
-// Kernel shape: a persistent grid (SMs x resident blocks) walks "tiles" of
-// 4096 elements (256 threads x 2 units x 8 elements).  Each unit is one
-// 16-byte grad load (8 bf16), two 16-byte loads each of master, m and v,
-// the same stores, and one 16-byte bf16 weight store.  All loads of a
-// thread are issued before any math so that ~220 bytes per thread are in
-// flight.  Tensors whose arrays are not mutually 16-byte aligned fall back
-// to a scalar loop; the (< 8 element) unaligned head and the tail of an
-// aligned tensor are done by scalar code in the tensor's first/last tile.
+// Two kernels share the element update (adam_elem):
+//  - adamw_bulk_kernel, for launches with at least 2^20 16-byte aligned
+//    elements: one CTA per SM, a producer warp streams grad / master / m / v
+//    in 4096-element chunks into a 3-stage shared-memory ring with 1D bulk
+//    copies (cp.async.bulk, mbarrier completion), 16 consumer warps update
+//    from shared memory and store straight to global memory.  It keeps
+//    ~168 KB per SM in flight without register staging.
+//  - adamw_multi_tensor_kernel, for small launches, for the (< 8 element)
+//    unaligned head and tail of each tensor, and for tensors whose arrays
+//    are not mutually 16-byte aligned: a persistent grid walks 4096-element
+//    tiles with 128-bit loads issued before the math (~220 bytes in flight
+//    per thread), or a scalar loop.
 #include <cuda_bf16.h>
 
 #include "common.h"
@@ -497,12 +501,14 @@ extern "C" {
 sf_status sf_adamw_layer_step(const sf_tensor* tensors, int n_tensors, const sf_adamw_hparams* hp,
                               int64_t step, void* stream) {
   sf::clear_error();
+  sf::NvtxRange nvtx_range("sf_adamw_layer_step");
   return sf::adamw_layer_step_impl(tensors, n_tensors, hp, step, sf::as_stream(stream));
 }
 
 sf_status lsp_adamw_compressed(const float* S, float* m, float* v, float* dS, int64_t d2,
                                const sf_adamw_hparams* hp, int64_t step, void* stream) {
   sf::clear_error();
+  sf::NvtxRange nvtx_range("lsp_adamw_compressed");
   return sf::adamw_compressed_impl(S, m, v, dS, d2, hp, step, sf::as_stream(stream));
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 #include <cstdarg>
@@ -12,6 +13,15 @@
 #include "sfopt.h"
 
 namespace sf {
+
+// NVTX range around one ABI call, so profiler timelines show library calls
+// by name (header-only NVTX; a no-op unless a tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Records a message for sf_last_error() (thread-local) and returns `st`.
 sf_status fail(sf_status st, const char* fmt, ...);

@@ -1220,6 +1220,7 @@ extern "C" {
 sf_status lsp_projector_create(int64_t rows, int32_t d, int32_t k, const int32_t* d_col_idx, const float* d_val,
                                int validate, void* stream_, lsp_projector* out) {
   sf::clear_error();
+  sf::NvtxRange nvtx_range("lsp_projector_create");
   if (!out) return fail(SF_ERR_INVALID, "out is NULL");
   *out = nullptr;
   if (rows < 1 || d < 1 || d > 1024 || k < 1 || k > 64)
@@ -1348,6 +1349,7 @@ size_t lsp_workspace_bytes(int64_t m, int64_t n, int32_t d) {
 sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G, sf_dtype g_dtype, int64_t m, int64_t n,
                        float* S, void* ws, size_t ws_bytes, void* stream_) {
   sf::clear_error();
+  sf::NvtxRange nvtx_range("lsp_compress");
   SF_TRY(sf::check_proj(P, "P"));
   SF_TRY(sf::check_proj(Q, "Q"));
   if (!G || !S) return fail(SF_ERR_INVALID, "G or S is NULL");
@@ -1423,6 +1425,7 @@ extern "C" {
 sf_status lsp_compress_noalloc(lsp_projector P, lsp_projector Q, const void* G, sf_dtype g_dtype, int64_t m, int64_t n,
                                float* S, void* stream) {
   sf::clear_error();
+  sf::NvtxRange nvtx_range("lsp_compress_noalloc");
   SF_TRY(sf::check_proj(P, "P"));
   SF_TRY(sf::check_proj(Q, "Q"));
   if (P->rows != m || Q->rows != n)
@@ -1445,6 +1448,7 @@ sf_status lsp_compress_noalloc(lsp_projector P, lsp_projector Q, const void* G, 
 sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS, void* W, sf_dtype w_dtype,
                                void* w_bf16_mirror, int64_t m, int64_t n, void* ws, size_t ws_bytes, void* stream_) {
   sf::clear_error();
+  sf::NvtxRange nvtx_range("lsp_decompress_apply");
   SF_TRY(sf::check_proj(P, "P"));
   SF_TRY(sf::check_proj(Q, "Q"));
   if (!dS || !W) return fail(SF_ERR_INVALID, "dS or W is NULL");

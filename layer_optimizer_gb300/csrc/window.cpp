@@ -42,7 +42,6 @@ struct sf_window_s {
   // per (slot, tensor): index (into ev_free) of the write-back event of the
   // group that last held that tensor of the slot; -1 = never used
   std::vector<int> free_ev;
-  std::vector<bool> slot_used;
   std::vector<cudaEvent_t> ev_layer;   // write-back of a host layer has landed
   std::vector<bool> layer_pending;
   int64_t visits = 0;                  // running visit counter (slot rotation)
@@ -134,7 +133,6 @@ sf_status sf_window_create(int n_slots, const sf_tensor* const* device_slots, in
   w->ev_in.assign(ne, nullptr);
   w->ev_done.assign(ne, nullptr);
   w->ev_free.assign(ne, nullptr);
-  w->slot_used.assign(n_slots, false);
   w->free_ev.assign(ne, -1);
   for (int e = 0; e < ne; ++e) {
     sf_status st = SF_OK;
@@ -153,6 +151,7 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
                                const int32_t* order, int n_order, const sf_adamw_hparams* hp,
                                int64_t* steps) {
   sf::clear_error();
+  sf::NvtxRange nvtx_range("sf_slide_window_step");
   if (!w) return sf::fail(SF_ERR_INVALID, "window is NULL");
   if (n_order < 0 || n_layers < 0) return sf::fail(SF_ERR_INVALID, "negative count");
   if (n_order == 0) return SF_OK;
@@ -236,7 +235,6 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
       for (int t = t0; t < t1; ++t) w->free_ev[eb + t] = eb + t0;
       t0 = t1;
     }
-    w->slot_used[s] = true;
     steps[l] = step;
     SF_CUDA_TRY(cudaEventRecord(w->ev_layer[l], w->d2h), "record ev_layer");
     w->layer_pending[l] = true;
@@ -247,6 +245,7 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
 
 sf_status sf_window_sync(sf_window w, int64_t timeout_ms) {
   sf::clear_error();
+  sf::NvtxRange nvtx_range("sf_window_sync");
   if (!w) return sf::fail(SF_ERR_INVALID, "window is NULL");
   SF_TRY(sf::bounded_wait_stream(w->h2d, timeout_ms, "window h2d stream"));
   SF_TRY(sf::bounded_wait_stream(w->comp, timeout_ms, "window compute stream"));
