@@ -486,6 +486,34 @@ def run_lsp(args, matrices=None):
         del g2
     except Exception as ex:
         graph_ms_streams = f"multi-stream graph failed: {str(ex)[:120]}"
+    # the same chain with the compressed moments in pinned host memory,
+    # through the layer-wise window (2 device slots, 3 streams)
+    host_ms = None
+    try:
+        items = []
+        for (name, m, n, P, Q, G, W, (S, mm, vv, dS), ws, wsb) in mats:
+            items.append(dict(P=P, Q=Q, G=G, g_dtype=native.SF_FP32, W=W, w_dtype=native.SF_BF16, m=m, n=n,
+                              m_host=torch.zeros(d, d).pin_memory(), v_host=torch.zeros(d, d).pin_memory()))
+        wsb_max = max(x[9] for x in mats)
+        slots = [tuple(torch.zeros(d, d, device="cuda") for _ in range(4)) +
+                 (torch.empty(wsb_max, dtype=torch.uint8, device="cuda"), wsb_max) for _ in range(2)]
+        wstreams = [torch.cuda.Stream() for _ in range(3)]
+        lw = native.lsp_window_create(slots, d, *wstreams)
+        lay = native.lsp_layers(items)
+        lsteps = (ctypes.c_int64 * len(items))()
+        order = list(range(len(items)))
+        for _ in range(args.warmup):
+            native.lsp_slide_window_step(lw, lay, order, hp, lsteps)
+        lw.sync()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            native.lsp_slide_window_step(lw, lay, order, hp, lsteps)
+        lw.sync()
+        host_ms = (time.perf_counter() - t0) / reps * 1e3
+        lw.close()
+        del slots, items
+    except Exception as ex:
+        host_ms = f"host-moment window failed: {str(ex)[:120]}"
     n_params = sum(m * n for (_, m, n, *_r) in mats)
     comp_t = sum(p[2] for p in per) / reps
     ad_t = sum(p[3] for p in per) / reps
@@ -509,6 +537,9 @@ def run_lsp(args, matrices=None):
         out["chain_GBps_graph"] = all_bytes / graph_ms / 1e6
         out["chain_frac_graph"] = all_bytes / graph_ms / 1e6 / peak
     out["ms_per_chain_all7_graph_streams"] = graph_ms_streams
+    out["ms_per_chain_all7_host_moments_window"] = host_ms
+    if isinstance(host_ms, float):
+        out["params_updated_per_s_host_moments_window"] = n_params / (host_ms / 1e3)
     if isinstance(graph_ms_streams, float):
         out["params_updated_per_s_graph_streams"] = n_params / (graph_ms_streams / 1e3)
         out["chain_frac_graph_streams"] = all_bytes / graph_ms_streams / 1e6 / peak

@@ -271,6 +271,66 @@ sf_status sf_window_sync(sf_window w, int64_t timeout_ms);
 sf_status sf_window_destroy(sf_window w);
 
 /* ------------------------------------------------------------------------
+ * (b') Learned sparse projectors with the compressed optimizer state in
+ * pinned host memory, layer by layer.
+ *
+ * LSP-Offload ("Practical offloading for fine-tuning LLM on commodity GPU
+ * via learned sparse projectors", abstract: "layer-wise communication
+ * schedule") keeps only compressed d x d quantities on the host and
+ * overlaps their transfers with the compute of neighbouring layers.  Here
+ * each layer's compressed moments m~, v~ (fp32 [d][d]) live in pinned host
+ * memory; lsp_slide_window_step enqueues, for every entry l = order[v]
+ * (slot s = running visit count mod n_slots):
+ *   compute: lsp_compress(P, Q, G) -> slot S           (device)
+ *   h2d:     wait until slot s is free and layer l's previous write-back has
+ *            landed; copy m~, v~ of layer l into the slot
+ *   compute: lsp_adamw_compressed(S, m~, v~ -> dS, step = ++steps[l]);
+ *            lsp_decompress_apply(P, Q, dS, W)
+ *   d2h:     copy m~, v~ back to layer l; the slot is free again when these
+ *            copies have ended.
+ * Results are bitwise those of the same calls with device-resident moments.
+ * Slots are caller-allocated device buffers; the window owns only events.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  float* S;       /* device fp32 [d][d] */
+  float* m;       /* device fp32 [d][d] */
+  float* v;       /* device fp32 [d][d] */
+  float* dS;      /* device fp32 [d][d] */
+  void* ws;       /* device workspace (256-byte aligned) */
+  size_t ws_bytes;
+} lsp_slot;
+
+typedef struct {
+  lsp_projector P;      /* rows = m */
+  lsp_projector Q;      /* rows = n, same d as P */
+  const void* G;        /* device [m][n], dtype g_dtype */
+  sf_dtype g_dtype;
+  void* W;              /* device [m][n], dtype w_dtype */
+  sf_dtype w_dtype;
+  void* w_bf16_mirror;  /* NULL or device bf16 [m][n] (w_dtype = SF_FP32) */
+  int64_t m, n;
+  float* m_host;        /* pinned host fp32 [d][d]: compressed first moment */
+  float* v_host;        /* pinned host fp32 [d][d]: compressed second moment */
+} lsp_layer;
+
+typedef struct lsp_window_s* lsp_window;
+
+/* n_slots >= 1 slots of dimension d; every slot's ws must cover every layer
+ * that passes through (lsp_workspace_bytes). */
+sf_status lsp_window_create(int n_slots, const lsp_slot* slots, int32_t d,
+                            void* h2d_stream, void* compute_stream,
+                            void* d2h_stream, lsp_window* out);
+
+sf_status lsp_slide_window_step(lsp_window w, const lsp_layer* layers,
+                                int n_layers, const int32_t* order, int n_order,
+                                const sf_adamw_hparams* hp, int64_t* steps);
+
+/* Bounded wait (as sf_window_sync) for everything the window enqueued. */
+sf_status lsp_window_sync(lsp_window w, int64_t timeout_ms);
+
+sf_status lsp_window_destroy(lsp_window w);
+
+/* ------------------------------------------------------------------------
  * Utilities.
  * ---------------------------------------------------------------------- */
 

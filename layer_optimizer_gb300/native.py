@@ -25,6 +25,7 @@ EXPORTS = [
     "lsp_decompress_apply", "sf_window_create", "sf_slide_window_step", "sf_window_sync",
     "sf_window_destroy", "sf_sync_status", "sf_last_error", "sf_version",
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
+    "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
 ]
 
 
@@ -46,6 +47,18 @@ class sf_tensor(ctypes.Structure):
 
 class sf_host_layer(ctypes.Structure):
     _fields_ = [("tensors", ctypes.POINTER(sf_tensor)), ("n_tensors", ctypes.c_int)]
+
+
+class lsp_slot(ctypes.Structure):
+    _fields_ = [("S", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dS", ctypes.c_void_p),
+                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+
+
+class lsp_layer(ctypes.Structure):
+    _fields_ = [("P", ctypes.c_void_p), ("Q", ctypes.c_void_p), ("G", ctypes.c_void_p), ("g_dtype", ctypes.c_int),
+                ("W", ctypes.c_void_p), ("w_dtype", ctypes.c_int), ("w_bf16_mirror", ctypes.c_void_p),
+                ("m", ctypes.c_int64), ("n", ctypes.c_int64), ("m_host", ctypes.c_void_p),
+                ("v_host", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -76,6 +89,11 @@ _SIGS = {
     "sf_last_error": (ctypes.c_char_p, []),
     "sf_version": (ctypes.c_char_p, []),
     "sf_test_fail_copy_after": (None, [_I64]),
+    "lsp_window_create": (_ST, [_INT, ctypes.POINTER(lsp_slot), _I32, _P, _P, _P, ctypes.POINTER(_P)]),
+    "lsp_slide_window_step": (_ST, [_P, ctypes.POINTER(lsp_layer), _INT, ctypes.POINTER(_I32), _INT,
+                                    ctypes.POINTER(sf_adamw_hparams), ctypes.POINTER(_I64)]),
+    "lsp_window_sync": (_ST, [_P, _I64]),
+    "lsp_window_destroy": (_ST, [_P]),
 }
 
 _lib = None
@@ -274,6 +292,61 @@ def sf_slide_window_step(window, layers, order, hp, steps):
     order_arr = (ctypes.c_int32 * max(1, len(order)))(*order)
     _check(load().sf_slide_window_step(window.handle, hl, n_layers, order_arr, len(order), ctypes.byref(hp),
                                        steps))
+
+
+# ----------------------------------------------------------------- (b') ----
+
+class LspWindow:
+    """Owning wrapper of an lsp_window handle; keeps its slot array alive."""
+
+    def __init__(self, handle, keep):
+        self.handle = handle
+        self._keep = keep
+
+    def sync(self, timeout_ms=0):
+        _check(load().lsp_window_sync(self.handle, timeout_ms))
+
+    def close(self):
+        if self.handle:
+            st = load().lsp_window_destroy(self.handle)
+            self.handle = None
+            _check(st)
+
+    def __del__(self):
+        try:
+            if self.handle:
+                load().lsp_window_destroy(self.handle)
+        except Exception:
+            pass
+
+
+def lsp_window_create(slots, d, h2d_stream, compute_stream, d2h_stream):
+    """``slots``: list of (S, m, v, dS, ws, ws_bytes) device buffers."""
+    arr = (lsp_slot * max(1, len(slots)))()
+    for i, (S, m, v, dS, ws, wsb) in enumerate(slots):
+        arr[i] = lsp_slot(_addr(S), _addr(m), _addr(v), _addr(dS), _addr(ws), wsb)
+    h = ctypes.c_void_p()
+    _check(load().lsp_window_create(len(slots), arr, d, _stream(h2d_stream), _stream(compute_stream),
+                                    _stream(d2h_stream), ctypes.byref(h)))
+    return LspWindow(h.value, arr)
+
+
+def lsp_layers(items):
+    """``items``: list of dicts with P, Q, G, g_dtype, W, w_dtype, mirror, m, n, m_host, v_host."""
+    arr = (lsp_layer * max(1, len(items)))()
+    for i, it in enumerate(items):
+        arr[i] = lsp_layer(it["P"].handle, it["Q"].handle, _addr(it["G"]), it["g_dtype"], _addr(it["W"]),
+                           it["w_dtype"], _addr(it.get("mirror")), it["m"], it["n"], _addr(it["m_host"]),
+                           _addr(it["v_host"]))
+    return arr, items
+
+
+def lsp_slide_window_step(window, layers, order, hp, steps):
+    """``layers`` from ``lsp_layers``; ``steps`` a ctypes int64 array (updated)."""
+    arr, items = layers
+    order_arr = (ctypes.c_int32 * max(1, len(order)))(*order)
+    _check(load().lsp_slide_window_step(window.handle, arr, len(items), order_arr, len(order), ctypes.byref(hp),
+                                        steps))
 
 
 def sf_sync_status(stream=None):
