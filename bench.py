@@ -551,6 +551,29 @@ def run_lsp(args, matrices=None):
     return out
 
 
+def host_update_rate(steps=3):
+    """The same AdamW step on all host cores (sf_adamw_host_step), one OPT-1.3B layer in host memory."""
+    import torch
+
+    from layer_optimizer_gb300 import native, synth
+    layer = []
+    for ti, (_, n) in enumerate(synth.OPT13_LAYER):
+        layer.append([synth.normal((n,), 1e-3, synth.sub_seed(11, ti), dtype=torch.bfloat16),
+                      synth.normal((n,), 0.02, synth.sub_seed(12, ti)), torch.zeros(n), torch.zeros(n),
+                      torch.empty(n, dtype=torch.bfloat16)])
+    ts = [native.make_tensor(*t) for t in layer]
+    hp = native.hparams(**HP)
+    native.sf_adamw_host_step(ts, hp, 1)
+    t0 = time.perf_counter()
+    for k in range(steps):
+        native.sf_adamw_host_step(ts, hp, k + 2)
+    el = (time.perf_counter() - t0) / steps
+    n = synth.layer_numel(synth.OPT13_LAYER)
+    return {"params_per_s": n / el, "GBps": ADAM_BYTES_PER_PARAM * n / el / 1e9, "threads": os.cpu_count(),
+            "sample": f"one OPT-1.3B layer ({n} params) in host memory, {steps} steps",
+            "note": "SlideFormer's own placement of the update (host cores), same arithmetic and bits as the GPU"}
+
+
 def run_mistral_window(args, world):
     """Four Mistral-Large layers in pinned host memory streamed through 2 device slots, 88 visits."""
     import torch
@@ -753,6 +776,8 @@ def main_ours(args, rank, world):
             line["lsp"] = run_lsp(args)
         except Exception as ex:  # the line still prints; the failure is recorded on it
             line["lsp"] = {"error": str(ex)[:300]}
+    if not args.no_cpu and rank == 0 and args.workload == "opt-1.3b":
+        line["host_update"] = host_update_rate()
     if not args.no_cpu and rank == 0:
         v, done, el = oracle_params_per_s()
         line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",

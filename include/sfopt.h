@@ -116,6 +116,18 @@ sf_status sf_adamw_layer_step(const sf_tensor* tensors, int n_tensors,
                               const sf_adamw_hparams* hp, int64_t step,
                               void* stream);
 
+/* The same AdamW layer step on the host CPU cores, for layers whose arrays
+ * are in host memory (any host memory; pinned is not required): SlideFormer's
+ * own placement of the update (technical summary section 2.A, "the CPU
+ * updates the parameters of layer L_i"), kept as a comparison point for the
+ * device kernels.  Identical arithmetic to sf_adamw_layer_step (no
+ * floating-point contraction, the same fused multiply-adds), so IEEE hosts
+ * produce the same bits as the GPU for finite inputs.  n_threads <= 0 uses
+ * every hardware thread.  Synchronous: returns when the update is done. */
+sf_status sf_adamw_host_step(const sf_tensor* tensors, int n_tensors,
+                             const sf_adamw_hparams* hp, int64_t step,
+                             int n_threads);
+
 /* ------------------------------------------------------------------------
  * (b) Learned sparse projectors.
  *

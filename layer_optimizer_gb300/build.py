@@ -55,7 +55,13 @@ def _stamp(src, flags):
     return h.hexdigest()
 
 
+# Per-file extra flags: the host AdamW must not contract a*b+c into an FMA
+# where the device kernel does not, so both give the same bits.
+FILE_FLAGS = {"host_adamw.cpp": ["-Xcompiler", "-ffp-contract=off"]}
+
+
 def _compile(nvcc, src, flags, verbose):
+    flags = list(flags) + FILE_FLAGS.get(os.path.basename(src), [])
     obj = os.path.join(BUILD, os.path.basename(src) + ".o")
     stamp_file = obj + ".stamp"
     stamp = _stamp(src, flags)

@@ -26,6 +26,7 @@ EXPORTS = [
     "sf_window_destroy", "sf_sync_status", "sf_last_error", "sf_version",
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
+    "sf_adamw_host_step",
 ]
 
 
@@ -89,6 +90,7 @@ _SIGS = {
     "sf_last_error": (ctypes.c_char_p, []),
     "sf_version": (ctypes.c_char_p, []),
     "sf_test_fail_copy_after": (None, [_I64]),
+    "sf_adamw_host_step": (_ST, [ctypes.POINTER(sf_tensor), _INT, ctypes.POINTER(sf_adamw_hparams), _I64, _INT]),
     "lsp_window_create": (_ST, [_INT, ctypes.POINTER(lsp_slot), _I32, _P, _P, _P, ctypes.POINTER(_P)]),
     "lsp_slide_window_step": (_ST, [_P, ctypes.POINTER(lsp_layer), _INT, ctypes.POINTER(_I32), _INT,
                                     ctypes.POINTER(sf_adamw_hparams), ctypes.POINTER(_I64)]),
@@ -164,6 +166,12 @@ def tensor_array(items):
 def sf_adamw_layer_step(tensors, hp, step, stream=None):
     arr = tensor_array(tensors)
     _check(load().sf_adamw_layer_step(arr, len(tensors), ctypes.byref(hp), step, _stream(stream)))
+
+
+def sf_adamw_host_step(tensors, hp, step, n_threads=0):
+    """The same update on the host cores; tensors hold host (CPU) arrays."""
+    arr = tensor_array(tensors)
+    _check(load().sf_adamw_host_step(arr, len(tensors), ctypes.byref(hp), step, n_threads))
 
 
 # ------------------------------------------------------------------ (b) ----

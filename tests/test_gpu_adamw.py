@@ -224,3 +224,23 @@ def test_checkpoint_resume_bitwise():
     for x, y in zip(a[1:4], c[1:4]):
         assert torch.equal(x.view(torch.int32), y.view(torch.int32))
     assert torch.equal(a[4].view(torch.int16), c[4].view(torch.int16))
+
+
+def test_host_step_bitwise_equals_device_step():
+    """The host-core update and the device kernels give the same bits (finite inputs)."""
+    sizes = [1 << 20, 4097, 33, 600001]
+    dev = _layer(sizes, 31)
+    host = [[x.cpu().clone() for x in t] for t in dev]
+    hp = native.hparams(**HP)
+    for t in (1, 2):
+        for i, n in enumerate(sizes):
+            g = synth.normal((n,), 1e-3, synth.sub_seed(31, 9, i, t), dtype=torch.bfloat16)
+            dev[i][0].copy_(g)
+            host[i][0].copy_(g)
+        native.sf_adamw_layer_step([native.make_tensor(*x) for x in dev], hp, t)
+        native.sf_adamw_host_step([native.make_tensor(*x) for x in host], hp, t)
+    torch.cuda.synchronize()
+    for d_, h_ in zip(dev, host):
+        for k in (1, 2, 3):
+            assert torch.equal(d_[k].cpu().view(torch.int32), h_[k].view(torch.int32))
+        assert torch.equal(d_[4].cpu().view(torch.int16), h_[4].view(torch.int16))
