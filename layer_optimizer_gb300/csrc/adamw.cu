@@ -99,7 +99,7 @@ __device__ __forceinline__ void adam_elem(float g, float& p, float& m, float& v,
                                           const AdamConsts& c) {
   m = fmaf(c.beta1, m, c.one_minus_beta1 * g);
   v = fmaf(c.beta2, v, c.one_minus_beta2 * (g * g));
-  const float denom = sqrtf(v) * c.inv_sqrt_bc2 + c.eps;
+  const float denom = fmaf(sqrtf(v), c.inv_sqrt_bc2, c.eps);   // one explicit rounding
   p = fmaf(-c.step_size, m / denom, p * c.decay);
 }
 
@@ -322,7 +322,7 @@ adamw_compressed_kernel(const float* __restrict__ S, float* __restrict__ m, floa
     float mm = m[e], vv = v[e];
     mm = fmaf(c.beta1, mm, c.one_minus_beta1 * g);
     vv = fmaf(c.beta2, vv, c.one_minus_beta2 * (g * g));
-    const float denom = sqrtf(vv) * c.inv_sqrt_bc2 + c.eps;
+    const float denom = fmaf(sqrtf(vv), c.inv_sqrt_bc2, c.eps);
     m[e] = mm;
     v[e] = vv;
     dS[e] = c.step_size * (mm / denom);

@@ -50,7 +50,7 @@ void update_range(const sf_tensor& t, int64_t b, int64_t e, const sf::AdamConsts
     const float gi = bf16_to_f32(g[i]);
     const float m = std::fmaf(c.beta1, M[i], c.one_minus_beta1 * gi);
     const float v = std::fmaf(c.beta2, V[i], c.one_minus_beta2 * (gi * gi));
-    const float denom = std::sqrt(v) * c.inv_sqrt_bc2 + c.eps;
+    const float denom = std::fmaf(std::sqrt(v), c.inv_sqrt_bc2, c.eps);
     const float p = std::fmaf(-c.step_size, m / denom, P[i] * c.decay);
     M[i] = m;
     V[i] = v;
