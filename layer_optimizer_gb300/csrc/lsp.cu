@@ -526,29 +526,31 @@ __global__ void k_reduce_splits(const float* __restrict__ part, int splits, int6
 // Decompress kernels
 // ----------------------------------------------------------------------------
 
-constexpr int kVMaxK = 8;            // k_v keeps 32 x k entries per warp in shared memory
+constexpr int kVMaxK = 8;            // k_v keeps 8 x k entries per warp in shared memory
+constexpr int kVWarps = 16;          // warps of a k_v CTA
+constexpr int kVGroup = 8;           // V columns a warp computes at a time (one 32-byte sector per row)
 
 __host__ __device__ __forceinline__ size_t v_ebuf_offset(int d) { return ((size_t)d * 65 * 4 + 15) / 16 * 16; }
-__host__ __device__ __forceinline__ size_t v_obuf_offset(int d) {
-  return v_ebuf_offset(d) + (size_t)8 * 32 * kVMaxK * 8;
+__host__ __device__ __forceinline__ size_t v_smem_bytes(int d) {
+  return v_ebuf_offset(d) + (size_t)kVWarps * kVGroup * kVMaxK * 8;
 }
-__host__ __device__ __forceinline__ size_t v_smem_bytes(int d) { return v_obuf_offset(d) + (size_t)8 * 64 * 33 * 4; }
 
-// V[a][j] = sum_l q_{j,l} dS[a][c_{j,l}] for a in a 64-row block, j in 32-column tiles.
-// dS^T of the block sits in shared memory (st[c * 65 + aa], padded: the
-// transposing fill and the lane-along-a reads are both conflict-free); the
-// k entries of the tile's 32 Q rows are fetched with coalesced loads into a
-// per-warp buffer and read back as warp-uniform broadcasts; the 64 x 32
-// result tile goes through a padded per-warp buffer so that V is written
-// as coalesced 128-byte row segments.
-__global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, const int32_t* __restrict__ qidx,
-                                           const float* __restrict__ qval, int k, int64_t n,
-                                           float* __restrict__ V, int tiles_per_warp) {
+// V[a][j] = sum_l q_{j,l} dS[a][c_{j,l}] for a in a 64-row block and the
+// CTA's range of columns j.  dS^T of the block sits in shared memory
+// (st[c * 65 + aa], padded: the transposing fill and the lane-along-a reads
+// are both conflict-free).  A warp takes 8 columns at a time: their 8 x k Q
+// entries go through a small per-warp buffer and are read back as
+// warp-uniform broadcasts; each lane keeps rows a0 + lane and a0 + lane + 32
+// of the 8 columns in registers and writes them as two 32-byte row segments.
+__global__ void __launch_bounds__(32 * kVWarps) k_v(const float* __restrict__ dS, int d,
+                                                    const int32_t* __restrict__ qidx,
+                                                    const float* __restrict__ qval, int k, int64_t n,
+                                                    float* __restrict__ V, int64_t cols_per_cta) {
   extern __shared__ float st[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   unsigned char* sbytes = reinterpret_cast<unsigned char*>(st);
-  int2* ebuf = reinterpret_cast<int2*>(sbytes + v_ebuf_offset(d)) + (size_t)warp * 32 * kVMaxK;
-  float* obuf = reinterpret_cast<float*>(sbytes + v_obuf_offset(d)) + (size_t)warp * 64 * 33;
+  int2* ebuf = reinterpret_cast<int2*>(sbytes + v_ebuf_offset(d)) + (size_t)warp * kVGroup * kVMaxK;
+  const uint32_t ebuf_a = smem_u32(ebuf);
   const int a0 = blockIdx.x * kVRows;
   griddep_launch_dependents();
   griddep_wait();                // dS comes from the compressed step
@@ -586,53 +588,67 @@ __global__ void __launch_bounds__(256) k_v(const float* __restrict__ dS, int d, 
     }
   }
   __syncthreads();
-  const int64_t n_tiles = (n + 31) / 32;
-  for (int q = 0; q < tiles_per_warp; ++q) {
-    const int64_t t = ((int64_t)blockIdx.y * nwarps + warp) * tiles_per_warp + q;
-    if (t >= n_tiles) break;
-    const int64_t j0 = t * 32;
-    const int rows_here = (int)(n - j0 < 32 ? n - j0 : 32);
-    const int ne = rows_here * k;
+  const uint32_t st_lo = smem_u32(st) + 4u * (uint32_t)lane;   // st[c * 65 + lane] at st_lo + 260 c
+  const bool on_lo = a0 + lane < d, on_hi = a0 + lane + 32 < d;
+  float* v_lo = V + (int64_t)(a0 + lane) * n;
+  float* v_hi = V + (int64_t)(a0 + lane + 32) * n;
+  const bool vec = (n & 3) == 0 && (reinterpret_cast<uintptr_t>(V) & 15) == 0;
+  const int64_t j_begin = (int64_t)blockIdx.y * cols_per_cta;
+  const int64_t j_end = imin64(n, j_begin + cols_per_cta);
+  for (int64_t j0 = j_begin + kVGroup * warp; j0 < j_end; j0 += (int64_t)kVGroup * nwarps) {
+    const int cols = (int)imin64(kVGroup, j_end - j0);
+    const int ne = cols * k;
     __syncwarp();
     for (int e = lane; e < ne; e += 32)
       ebuf[e] = make_int2(qidx[j0 * k + e], __float_as_int(qval[j0 * k + e]));
     __syncwarp();
-    // four columns at a time: four independent load-multiply chains per warp
-    int jj = 0;
-    for (; jj + 4 <= rows_here; jj += 4) {
-      float s[4][2];
+    float s_lo[kVGroup], s_hi[kVGroup];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) s[u][0] = s[u][1] = 0.0f;
-      for (int l = 0; l < k; ++l) {
+    for (int u = 0; u < kVGroup; ++u) s_lo[u] = s_hi[u] = 0.0f;
+    if (k == kVMaxK && cols == kVGroup) {
+      // every load of the group is independent: fully unrolled
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int2 en = ebuf[(jj + u) * k + l];
+      for (int l = 0; l < kVMaxK; ++l) {
+#pragma unroll
+        for (int u = 0; u < kVGroup; ++u) {
+          const int2 en = lds_i2(ebuf_a + 8u * (uint32_t)(u * kVMaxK + l));
           const float qv = __int_as_float(en.y);
-          s[u][0] = fmaf(qv, st[en.x * 65 + lane], s[u][0]);
-          s[u][1] = fmaf(qv, st[en.x * 65 + lane + 32], s[u][1]);
+          const uint32_t sa = st_lo + 260u * (uint32_t)en.x;
+          s_lo[u] = fmaf(qv, __uint_as_float(lds_u32(sa)), s_lo[u]);
+          s_hi[u] = fmaf(qv, __uint_as_float(lds_u32(sa + 128u)), s_hi[u]);
         }
       }
+    } else {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        obuf[lane * 33 + jj + u] = s[u][0];
-        obuf[(lane + 32) * 33 + jj + u] = s[u][1];
+      for (int u = 0; u < kVGroup; ++u) {
+        if (u >= cols) break;
+        for (int l = 0; l < k; ++l) {
+          const int2 en = lds_i2(ebuf_a + 8u * (uint32_t)(u * k + l));
+          const float qv = __int_as_float(en.y);
+          const uint32_t sa = st_lo + 260u * (uint32_t)en.x;
+          s_lo[u] = fmaf(qv, __uint_as_float(lds_u32(sa)), s_lo[u]);
+          s_hi[u] = fmaf(qv, __uint_as_float(lds_u32(sa + 128u)), s_hi[u]);
+        }
       }
     }
-    for (; jj < rows_here; ++jj) {
-      float s0 = 0.0f, s1 = 0.0f;
-      for (int l = 0; l < k; ++l) {
-        const int2 en = ebuf[jj * k + l];
-        const float qv = __int_as_float(en.y);
-        s0 = fmaf(qv, st[en.x * 65 + lane], s0);
-        s1 = fmaf(qv, st[en.x * 65 + lane + 32], s1);
+    if (vec && cols == kVGroup) {
+      if (on_lo) {
+        *reinterpret_cast<float4*>(v_lo + j0) = make_float4(s_lo[0], s_lo[1], s_lo[2], s_lo[3]);
+        *reinterpret_cast<float4*>(v_lo + j0 + 4) = make_float4(s_lo[4], s_lo[5], s_lo[6], s_lo[7]);
       }
-      obuf[lane * 33 + jj] = s0;
-      obuf[(lane + 32) * 33 + jj] = s1;
+      if (on_hi) {
+        *reinterpret_cast<float4*>(v_hi + j0) = make_float4(s_hi[0], s_hi[1], s_hi[2], s_hi[3]);
+        *reinterpret_cast<float4*>(v_hi + j0 + 4) = make_float4(s_hi[4], s_hi[5], s_hi[6], s_hi[7]);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kVGroup; ++u) {
+        if (u < cols) {
+          if (on_lo) v_lo[j0 + u] = s_lo[u];
+          if (on_hi) v_hi[j0 + u] = s_hi[u];
+        }
+      }
     }
-    __syncwarp();
-    const int64_t j = j0 + lane;
-    if (lane < rows_here)
-      for (int aa = 0; aa < kVRows && a0 + aa < d; ++aa) V[(int64_t)(a0 + aa) * n + j] = obuf[aa * 33 + lane];
   }
 }
 
@@ -802,6 +818,7 @@ struct ApplyArgs {
   int32_t stages;
   int32_t vs_bytes;      // bytes of the V block (1024-aligned)
   int32_t vec_ok;
+  int32_t v_vec;         // V rows can be read as float4 (n % 4 == 0, 16-byte aligned V)
 };
 
 template <bool kBf16W>
@@ -881,9 +898,29 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
       const int64_t j0 = jb * kApplyCols;
       if (jb != cur_jb) {
         named_bar_sync(1, 32 * kApplyConsumerWarps);
-        for (int e = threadIdx.x; e < A.d * kApplyCols; e += 32 * kApplyConsumerWarps) {
-          const int a = e / kApplyCols, jj = e % kApplyCols;
-          vs[e] = (j0 + jj < A.n) ? A.V[(int64_t)a * A.n + j0 + jj] : 0.0f;
+        if (A.v_vec && j0 + kApplyCols <= A.n) {
+          // 16-byte loads, 8 in flight per thread before their stores
+          constexpr int kQuads = kApplyCols / 4;               // float4 per V row of the block
+          const int total4 = A.d * kQuads;
+          for (int e0 = threadIdx.x; e0 < total4; e0 += 8 * 32 * kApplyConsumerWarps) {
+            float4 t[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int e = e0 + u * 32 * kApplyConsumerWarps;
+              if (e < total4)
+                t[u] = *reinterpret_cast<const float4*>(A.V + (int64_t)(e / kQuads) * A.n + j0 + 4 * (e % kQuads));
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int e = e0 + u * 32 * kApplyConsumerWarps;
+              if (e < total4) reinterpret_cast<float4*>(vs)[e] = t[u];
+            }
+          }
+        } else {
+          for (int e = threadIdx.x; e < A.d * kApplyCols; e += 32 * kApplyConsumerWarps) {
+            const int a = e / kApplyCols, jj = e % kApplyCols;
+            vs[e] = (j0 + jj < A.n) ? A.V[(int64_t)a * A.n + j0 + jj] : 0.0f;
+          }
         }
         named_bar_sync(1, 32 * kApplyConsumerWarps);
         cur_jb = jb;
@@ -951,7 +988,43 @@ __global__ void __launch_bounds__(32 * (kApplyConsumerWarps + 1), 1)
         }
       };
       const int64_t i_first = rt * kApplyRows + warp * 4;
-      if (k == 8 && i_first + 3 < A.m) {
+      if (kBf16W && k == 8 && i_first + 3 < A.m && A.vec_ok && j0 + kApplyCols <= A.n) {
+        // bf16 W, whole tile row in range: two rows at a time, every load
+        // issued before the multiply-adds, both columns of a lane as one
+        // packed pair (fused multiply-add, subtraction and rounding to bf16
+        // on the pair), one 4-byte store per lane and row
+        uint32_t* wrow = reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(A.W) + i_first * A.n + j);
+        const int64_t wstride = A.n / 2;   // 32-bit words per W row
+#pragma unroll
+        for (int rp = 0; rp < 4; rp += 2) {
+          const int r0 = warp * 4 + rp;
+          const uint32_t e0 = eidx + (uint32_t)r0 * 32u, v0a = evals + (uint32_t)r0 * 32u;
+          const int4 a0 = lds_i4(e0), a1 = lds_i4(e0 + 16), a2 = lds_i4(e0 + 32), a3 = lds_i4(e0 + 48);
+          const float4 p0 = lds_f4(v0a), p1 = lds_f4(v0a + 16), p2 = lds_f4(v0a + 32), p3 = lds_f4(v0a + 48);
+          const uint32_t ua = lds_u32(st + ((uint32_t)r0 * kApplyCols + 2u * lane) * 2u);
+          const uint32_t ub = lds_u32(st + ((uint32_t)(r0 + 1) * kApplyCols + 2u * lane) * 2u);
+          const int ia[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+          const int ib[8] = {a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+          const float pa[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+          const float pb[8] = {p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
+          uint64_t va[8], vb[8];
+#pragma unroll
+          for (int l = 0; l < 8; ++l) {
+            va[l] = lds_u64(vs_lane + (uint32_t)ia[l] * (kApplyCols * 4u));
+            vb[l] = lds_u64(vs_lane + (uint32_t)ib[l] * (kApplyCols * 4u));
+          }
+          uint64_t sa = 0ull, sb = 0ull;
+#pragma unroll
+          for (int l = 0; l < 8; ++l) {
+            ffma2(sa, va[l], pack_f2(pa[l], pa[l]));
+            ffma2(sb, vb[l], pack_f2(pb[l], pb[l]));
+          }
+          const uint64_t wa = pack_f2(__uint_as_float(ua << 16), __uint_as_float(ua & 0xFFFF0000u));
+          const uint64_t wb = pack_f2(__uint_as_float(ub << 16), __uint_as_float(ub & 0xFFFF0000u));
+          wrow[rp * wstride] = bf16x2_rn(fsub2(wa, sa));
+          wrow[(rp + 1) * wstride] = bf16x2_rn(fsub2(wb, sb));
+        }
+      } else if (k == 8 && i_first + 3 < A.m) {
         // two rows at a time, every load issued before the multiply-adds
 #pragma unroll
         for (int rp = 0; rp < 4; rp += 2) {
@@ -1468,10 +1541,12 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
   uint16_t* mirror = static_cast<uint16_t*>(w_bf16_mirror);
   if (d <= sf::kMaxFastD && P->k <= 32 && Q->k <= 32) {
     const int n_ab = (int)ceil_div(d, sf::kVRows);
-    const int64_t n_tiles = ceil_div<int64_t>(n, 32);
-    const int warps = 8;
-    const int tpw = (int)std::max<int64_t>(1, (int64_t)n_ab * n_tiles / ((int64_t)warps * sf::kTargetCtas));
-    const int64_t gy = ceil_div<int64_t>(n_tiles, (int64_t)warps * tpw);
+    // one wave: about one CTA per SM, each with a column range that is a
+    // multiple of the 8-column group
+    const int64_t n_groups = ceil_div<int64_t>(n, sf::kVGroup);
+    const int64_t gy = std::max<int64_t>(1, std::min<int64_t>(n_groups, nsm / n_ab));
+    const int64_t cols_per_cta = ceil_div<int64_t>(n_groups, gy) * sf::kVGroup;
+    const int64_t gy_used = ceil_div<int64_t>(n, cols_per_cta);
     if (Q->k <= sf::kVMaxK) {
       const size_t smem_v = sf::v_smem_bytes(d);
       static thread_local bool v_cfg = false;
@@ -1481,8 +1556,8 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
                     "cudaFuncSetAttribute(k_v)");
         v_cfg = true;
       }
-      SF_CUDA_TRY(sf::launch_pdl(sf::k_v, dim3((unsigned)n_ab, (unsigned)gy), dim3(32 * warps), smem_v, s, dS, d,
-                                 Q->ell_idx, Q->ell_val, Q->k, n, V, tpw),
+      SF_CUDA_TRY(sf::launch_pdl(sf::k_v, dim3((unsigned)n_ab, (unsigned)gy_used), dim3(32 * sf::kVWarps), smem_v, s,
+                                 dS, d, Q->ell_idx, Q->ell_val, Q->k, n, V, cols_per_cta),
                   "launch k_v");
     } else {
       const int64_t nv = (int64_t)d * n;
@@ -1532,6 +1607,7 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
       A.stages = (int)std::min<size_t>(sf::kApplyMaxStages, (220 * 1024 - fixed) / A.stage_stride);
       if (A.stages >= 2) {
         A.vec_ok = vec_ok;
+        A.v_vec = (n % 4 == 0) && (reinterpret_cast<uintptr_t>(V) % 16 == 0) ? 1 : 0;
         const int64_t grid2 = std::min<int64_t>(nsm, A.total);
         A.per_cta = ceil_div<int64_t>(A.total, grid2);
         const size_t smem2 = fixed + (size_t)A.stages * A.stage_stride;
