@@ -94,3 +94,38 @@ def test_planted_compress_mistakes_fail_brute_force(kind):
     S, _ = ol.compress(P, Q, G)
     assert np.allclose(S, want, rtol=1e-12, atol=1e-12)
     assert not np.allclose(broken, want, rtol=1e-6, atol=1e-9)
+
+
+def _broken_fit_grads(kind, G, P, Q):
+    Pd, Qd = P.dense(), Q.dense()
+    S = Pd.T @ G @ Qd
+    E = G - Pd @ S @ Qd.T
+    if kind == "dropped_term":
+        gPd = -2.0 * (E @ Qd @ S.T)
+    elif kind == "transposed_S":
+        gPd = -2.0 * (E @ Qd @ S + G @ Qd @ Qd.T @ E.T @ Pd)
+    else:  # wrong sign of the second term
+        gPd = -2.0 * (E @ Qd @ S.T - G @ Qd @ Qd.T @ E.T @ Pd)
+    return gPd[np.repeat(np.arange(P.rows), P.k).reshape(P.rows, P.k), P.idx]
+
+
+@pytest.mark.parametrize("kind", ["dropped_term", "transposed_S", "wrong_sign"])
+def test_planted_fit_gradient_mistakes_fail_finite_differences(kind):
+    from oracle.lsp_fit import fit_loss, fit_step
+    rng = np.random.default_rng(11)
+    m, n, d, k = 9, 7, 4, 2
+    G = rng.normal(size=(m, n))
+    P = ol.Projector(np.stack([rng.choice(d, k, replace=False) for _ in range(m)]), rng.normal(size=(m, k)), d)
+    Q = ol.Projector(np.stack([rng.choice(d, k, replace=False) for _ in range(n)]), rng.normal(size=(n, k)), d)
+    h = 1e-6
+    fd = np.zeros((m, k))
+    for r in range(m):
+        for t in range(k):
+            vp, vm = P.val.copy(), P.val.copy()
+            vp[r, t] += h
+            vm[r, t] -= h
+            fd[r, t] = (fit_loss(G, ol.Projector(P.idx, vp, d), Q) - fit_loss(G, ol.Projector(P.idx, vm, d), Q)) / (2 * h)
+    good = fit_step(G, P, Q, 0.0)["gP"]
+    bad = _broken_fit_grads(kind, G, P, Q)
+    assert np.allclose(good, fd, rtol=1e-5, atol=1e-5)
+    assert not np.allclose(bad, fd, rtol=1e-3, atol=1e-3)
