@@ -232,6 +232,45 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
                                int64_t m, int64_t n, void* ws, size_t ws_bytes,
                                void* stream);
 
+/* Learning the projectors (LSP-Offload, method section, "key design": the
+ * sparse projectors are fitted by gradient descent to minimise what is lost
+ * by compressing and decompressing).  The pages give no loss or schedule;
+ * this is one plain gradient step on the stored values of P and Q (their
+ * column ids stay fixed) for the squared reconstruction error of a gradient
+ * sample G:
+ *
+ *   S = P^T G Q,   L = || G - P S Q^T ||_F^2,
+ *   dL/dP = -2 (E Q S^T + G Q Q^T E^T P),  dL/dQ = -2 (E^T P S + G^T P P^T E Q),
+ *   E = G - P S Q^T,   val <- val - lr * dL/dval   (P and Q together, both
+ *   gradients at the values before the step).
+ *
+ *   P, Q   : projectors with rows m and n, the same d; must be different
+ *            handles, and neither may have had out-of-range column ids at
+ *            creation (SF_ERR_INVALID otherwise).  Their values are updated
+ *            in place, in every layout the library keeps, so later
+ *            compress / decompress calls and exports see the new values.
+ *   G      : device, [m][n] row-major, SF_BF16 or SF_FP32.
+ *   lr     : step size (rounded once to fp32); lr = 0 evaluates only.
+ *   loss   : device double [1], receives L before the step; may be NULL.
+ *   grad_P : device fp32 [m * k_P], receives dL/dval of P in ELL order (row
+ *            i, entry t at i * k_P + t); may be NULL.  grad_Q likewise
+ *            [n * k_Q].
+ *   ws     : device scratch of ws_bytes >= lsp_fit_workspace_bytes(m, n, d,
+ *            g_dtype), 256-byte aligned.
+ * fp32 arithmetic (the loss assembled in fp64 from fp32 partial sums); no
+ * atomics; stream-ordered like every other call. */
+size_t lsp_fit_workspace_bytes(int64_t m, int64_t n, int32_t d, sf_dtype g_dtype);
+
+sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G,
+                                 sf_dtype g_dtype, int64_t m, int64_t n, double lr,
+                                 double* loss, float* grad_P, float* grad_Q,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* Copy a projector's current values, ELL order [rows * k] fp32, to device
+ * memory `val` (after lsp_projector_fit_step they differ from the values
+ * the projector was created with).  Out-of-range ids read as 0. */
+sf_status lsp_projector_export_values(lsp_projector p, float* val, void* stream);
+
 /* ------------------------------------------------------------------------
  * (c) Layer-sliding window.
  *

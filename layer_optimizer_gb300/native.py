@@ -26,7 +26,7 @@ EXPORTS = [
     "sf_window_destroy", "sf_sync_status", "sf_last_error", "sf_version",
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
-    "sf_adamw_host_step",
+    "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
 ]
 
 
@@ -96,6 +96,10 @@ _SIGS = {
                                     ctypes.POINTER(sf_adamw_hparams), ctypes.POINTER(_I64)]),
     "lsp_window_sync": (_ST, [_P, _I64]),
     "lsp_window_destroy": (_ST, [_P]),
+    "lsp_fit_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I32, _INT]),
+    "lsp_projector_fit_step": (_ST, [_P, _P, _P, _INT, _I64, _I64, ctypes.c_double, _P, _P, _P, _P,
+                                     ctypes.c_size_t, _P]),
+    "lsp_projector_export_values": (_ST, [_P, _P, _P]),
 }
 
 _lib = None
@@ -243,6 +247,19 @@ def lsp_adamw_compressed(S, m, v, dS, d2, hp, step, stream=None):
 def lsp_decompress_apply(P, Q, dS, W, w_dtype, w_bf16_mirror, m, n, ws, ws_bytes, stream=None):
     _check(load().lsp_decompress_apply(P.handle, Q.handle, _addr(dS), _addr(W), w_dtype,
                                        _addr(w_bf16_mirror), m, n, _addr(ws), ws_bytes, _stream(stream)))
+
+
+def lsp_fit_workspace_bytes(m, n, d, g_dtype):
+    return load().lsp_fit_workspace_bytes(m, n, d, g_dtype)
+
+
+def lsp_projector_fit_step(P, Q, G, g_dtype, m, n, lr, loss, grad_P, grad_Q, ws, ws_bytes, stream=None):
+    _check(load().lsp_projector_fit_step(P.handle, Q.handle, _addr(G), g_dtype, m, n, float(lr), _addr(loss),
+                                         _addr(grad_P), _addr(grad_Q), _addr(ws), ws_bytes, _stream(stream)))
+
+
+def lsp_projector_export_values(p, val, stream=None):
+    _check(load().lsp_projector_export_values(p.handle, _addr(val), _stream(stream)))
 
 
 # ------------------------------------------------------------------ (c) ----
