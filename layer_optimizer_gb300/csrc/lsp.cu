@@ -1682,17 +1682,19 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
 namespace sf {
 namespace {
 
-// out[j][i] = in[i][j] (in m x n, out n x m) through a padded 32 x 32 tile,
-// with this block's sum of in^2 (fp32 within the block, one double out).
+// out[j][i] = in[i][j] (in m x n, out n x m) through a padded 64 x 64 tile
+// (16 loads in flight per thread), with this block's sum of in^2 (fp32
+// within the block, one double out).
 template <typename TB>
 __global__ void __launch_bounds__(256) k_transpose_sumsq(const TB* __restrict__ in, int64_t m, int64_t n,
                                                          TB* __restrict__ out, double* __restrict__ partial) {
-  __shared__ TB tile[32][33];
+  __shared__ TB tile[64][65];
   __shared__ float red[8];
-  const int64_t i0 = (int64_t)blockIdx.y * 32, j0 = (int64_t)blockIdx.x * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int64_t i0 = (int64_t)blockIdx.y * 64, j0 = (int64_t)blockIdx.x * 64;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
   float sq = 0.0f;
-  for (int r = ty; r < 32; r += 8) {
+#pragma unroll 4
+  for (int r = ty; r < 64; r += 4) {
     const int64_t i = i0 + r, j = j0 + tx;
     if (i < m && j < n) {
       const TB v = in[i * n + j];
@@ -1704,13 +1706,14 @@ __global__ void __launch_bounds__(256) k_transpose_sumsq(const TB* __restrict__ 
     }
   }
   __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
+#pragma unroll 4
+  for (int r = ty; r < 64; r += 4) {
     const int64_t j = j0 + r, i = i0 + tx;
     if (j < n && i < m) out[j * m + i] = tile[tx][r];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-  if (tx == 0) red[ty] = sq;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = sq;
   __syncthreads();
   if (threadIdx.x == 0) {
     float b = 0.0f;
@@ -1719,24 +1722,14 @@ __global__ void __launch_bounds__(256) k_transpose_sumsq(const TB* __restrict__ 
   }
 }
 
-// A[a][b] = sum_i P[i][a] P[i][b] (the Gram matrix P^T P), one thread per
-// (a, b): the rows of column a in CSC order, each row's k entries scanned
-// for id b (a repeated id adds up, as in the projector itself).
-__global__ void k_gram(const int32_t* __restrict__ col_ptr, const int32_t* __restrict__ row_idx,
-                       const float* __restrict__ csc_val, const int32_t* __restrict__ ell_idx,
-                       const float* __restrict__ ell_val, int k, int d, float* __restrict__ A) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= (int64_t)d * d) return;
-  const int a = (int)(t / d), b = (int)(t % d);
-  float acc = 0.0f;
-  for (int e = col_ptr[a]; e < col_ptr[a + 1]; ++e) {
-    const int64_t i = row_idx[e];
-    float pb = 0.0f;
-    for (int u = 0; u < k; ++u)
-      if (ell_idx[i * k + u] == b) pb += ell_val[i * k + u];
-    acc = fmaf(csc_val[e], pb, acc);
-  }
-  A[t] = acc;
+// Dense copy of a projector, out[i][c] = sum of row i's values with id c
+// (entries in ELL order; `out` zero-filled beforehand).  The Gram matrix
+// P^T P is then the gather of this m x d matrix with P itself.
+__global__ void k_densify(const int32_t* __restrict__ ell_idx, const float* __restrict__ ell_val, int64_t rows,
+                          int k, int d, float* __restrict__ out) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= rows) return;
+  for (int t = 0; t < k; ++t) out[i * d + ell_idx[i * k + t]] += ell_val[i * k + t];
 }
 
 // C = op(A) op(B) for d x d fp32 row-major matrices, op = identity or
@@ -1804,6 +1797,83 @@ __global__ void __launch_bounds__(256) k_gemm_dd(const __grid_constant__ DdBatch
     }
 }
 
+// The same products when d is a multiple of 64: the k-slab of 32 of op(A)
+// and op(B) is staged k-major in shared memory from 16-byte global loads
+// (the next slab's loads in flight while the current one is used), and each
+// thread reads its 4 rows and 4 columns with one 16-byte load each per k.
+// Same order of the sums as k_gemm_dd.
+__global__ void __launch_bounds__(256) k_gemm_dd64(const __grid_constant__ DdBatch bt) {
+  const DdJob J = bt.job[blockIdx.z];
+  const int d = bt.d;
+  __shared__ __align__(16) float As[32][64];
+  __shared__ __align__(16) float Bs[32][64];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
+  // slab loads: 64 x 32 floats of each operand = 512 float4, two per thread
+  float4 ra[2], rb[2];
+  auto load = [&](int k0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = tid + 256 * h;
+      // op(A)[i][l]: plain A is read along l (8 float4 per row), a transposed one along i
+      ra[h] = J.ta ? *reinterpret_cast<const float4*>(J.A + (int64_t)(k0 + (q >> 4)) * d + i0 + 4 * (q & 15))
+                   : *reinterpret_cast<const float4*>(J.A + (int64_t)(i0 + (q >> 3)) * d + k0 + 4 * (q & 7));
+      rb[h] = J.tb ? *reinterpret_cast<const float4*>(J.B + (int64_t)(j0 + (q >> 3)) * d + k0 + 4 * (q & 7))
+                   : *reinterpret_cast<const float4*>(J.B + (int64_t)(k0 + (q >> 4)) * d + j0 + 4 * (q & 15));
+    }
+  };
+  auto store = [&]() {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int q = tid + 256 * h;
+      if (J.ta) {
+        *reinterpret_cast<float4*>(&As[q >> 4][4 * (q & 15)]) = ra[h];
+      } else {
+        const int ii = q >> 3, kk = 4 * (q & 7);
+        As[kk][ii] = ra[h].x;
+        As[kk + 1][ii] = ra[h].y;
+        As[kk + 2][ii] = ra[h].z;
+        As[kk + 3][ii] = ra[h].w;
+      }
+      if (J.tb) {
+        const int jj = q >> 3, kk = 4 * (q & 7);
+        Bs[kk][jj] = rb[h].x;
+        Bs[kk + 1][jj] = rb[h].y;
+        Bs[kk + 2][jj] = rb[h].z;
+        Bs[kk + 3][jj] = rb[h].w;
+      } else {
+        *reinterpret_cast<float4*>(&Bs[q >> 4][4 * (q & 15)]) = rb[h];
+      }
+    }
+  };
+  float acc[4][4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0.0f;
+  load(0);
+  for (int k0 = 0; k0 < d; k0 += 32) {
+    __syncthreads();
+    store();
+    __syncthreads();
+    if (k0 + 32 < d) load(k0 + 32);
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[kk][4 * ty]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][4 * tx]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+    *reinterpret_cast<float4*>(J.C + (int64_t)(i0 + 4 * ty + r) * d + j0 + 4 * tx) =
+        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+}
+
 // H_P = 2 S - X (= S + C with C = S - X, X = A_P S A_Q), H_Q = H_P^T, and
 // this block's partial sums of S * S and W1 * W2 (W1 = S A_Q, W2 = A_P S).
 __global__ void __launch_bounds__(256) k_fit_combine(const float* __restrict__ S, const float* __restrict__ X,
@@ -1844,8 +1914,9 @@ __global__ void __launch_bounds__(256) k_fit_combine(const float* __restrict__ S
 }
 
 // g[r k + s] = -2 (<X[r, :], H[c_s, :]> - sum_t v_t K[c_t][c_s]) for the k
-// stored entries (c_t, v_t) of row r; one warp per row, fixed lane order and
-// a fixed butterfly for every sum.
+// stored entries (c_t, v_t) of row r; one warp per row, the lanes along d.
+// For k <= 8 the k dot products share each load of X[r, :] and are summed
+// side by side; every sum has a fixed lane order and a fixed butterfly.
 __global__ void __launch_bounds__(256) k_fit_rowgrad(const float* __restrict__ X, int64_t rows, int d,
                                                      const int32_t* __restrict__ idx, const float* __restrict__ val,
                                                      int k, const float* __restrict__ H, const float* __restrict__ K,
@@ -1856,6 +1927,35 @@ __global__ void __launch_bounds__(256) k_fit_rowgrad(const float* __restrict__ X
   const float* x = X + r * d;
   const int32_t* ir = idx + r * k;
   const float* vr = val + r * k;
+  if (k <= 8) {
+    int c[8];
+    float p[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      c[s] = s < k ? ir[s] : 0;
+      p[s] = 0.0f;
+    }
+    for (int u = lane; u < d; u += 32) {
+      const float xu = x[u];
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (s < k) p[s] = fmaf(xu, H[(int64_t)c[s] * d + u], p[s]);
+    }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (s >= k) break;
+      float kt = 0.0f;
+      if (lane < k) kt = vr[lane] * K[(int64_t)ir[lane] * d + c[s]];
+      float ps = p[s];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        ps += __shfl_xor_sync(0xffffffffu, ps, o);
+        kt += __shfl_xor_sync(0xffffffffu, kt, o);
+      }
+      if (lane == 0) g[r * k + s] = -2.0f * (ps - kt);
+    }
+    return;
+  }
   for (int s = 0; s < k; ++s) {
     const int c = ir[s];
     const float* h = H + (int64_t)c * d;
@@ -1874,9 +1974,10 @@ __global__ void __launch_bounds__(256) k_fit_rowgrad(const float* __restrict__ X
 
 // L = sum(G^2) - 2 sum(S^2) + sum(W1 W2), from the block partials, in fp64
 // and in a fixed order.
-__global__ void k_fit_loss(const double* __restrict__ g2, int64_t n_g2, const double* __restrict__ part, int n_part,
-                           double* __restrict__ loss) {
-  __shared__ double red[3][256];
+__global__ void __launch_bounds__(1024) k_fit_loss(const double* __restrict__ g2, int64_t n_g2,
+                                                   const double* __restrict__ part, int n_part,
+                                                   double* __restrict__ loss) {
+  __shared__ double red[3][1024];
   double a = 0.0, b = 0.0, c = 0.0;
   for (int64_t i = threadIdx.x; i < n_g2; i += blockDim.x) a += g2[i];
   for (int i = threadIdx.x; i < n_part; i += blockDim.x) {
@@ -1913,8 +2014,8 @@ constexpr int kCombineBlocks = 128;
 
 struct FitPlan {
   CompressPlan cp;
-  GatherPlan gt;
-  size_t off_gt, off_t, off_tp, off_dd, off_gp, off_gq, off_g2, off_part, bytes;
+  GatherPlan gt, gram_p, gram_q;
+  size_t off_gt, off_t, off_tp, off_dd, off_gp, off_gq, off_g2, off_part, off_dense, off_gramp, bytes;
   int64_t n_g2;
 };
 
@@ -1935,11 +2036,17 @@ FitPlan plan_fit(int64_t m, int64_t n, int d, size_t es, int kP, int kQ) {
   off = align_up(off + (size_t)m * kP * 4, 256);
   f.off_gq = off;
   off = align_up(off + (size_t)n * kQ * 4, 256);
-  f.n_g2 = ceil_div<int64_t>(m, 32) * ceil_div<int64_t>(n, 32);
+  f.n_g2 = ceil_div<int64_t>(m, 64) * ceil_div<int64_t>(n, 64);
   f.off_g2 = off;
   off = align_up(off + (size_t)f.n_g2 * 8, 256);
   f.off_part = off;
   off = align_up(off + (size_t)kCombineBlocks * 2 * 8, 256);
+  f.gram_p = plan_gather(m, d, d);
+  f.gram_q = plan_gather(n, d, d);
+  f.off_dense = off;
+  off = align_up(off + (size_t)std::max(m, n) * d * 4, 256);
+  f.off_gramp = off;
+  off = align_up(off + (size_t)std::max(f.gram_p.splits, f.gram_q.splits) * d * d * 4, 256);
   f.bytes = off;
   return f;
 }
@@ -1995,7 +2102,7 @@ sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G
   double* part = reinterpret_cast<double*>(w + f.off_part);
 
   // U = G^T P and S = P^T G Q (the compress pair); G^T with the sum of G^2; T = G Q
-  const dim3 tgrid((unsigned)ceil_div<int64_t>(n, 32), (unsigned)ceil_div<int64_t>(m, 32));
+  const dim3 tgrid((unsigned)ceil_div<int64_t>(n, 64), (unsigned)ceil_div<int64_t>(m, 64));
   if (tgrid.y > 65535u) return fail(SF_ERR_UNSUPPORTED, "m = %lld is too large for the fit step", (long long)m);
   if (g_dtype == SF_FP32) {
     const float* Gf = static_cast<const float*>(G);
@@ -2012,23 +2119,33 @@ sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G
   }
   SF_TRY(sf::launch_gather<float>(Q, U, d, d, f.cp.g2, S, Sp, s));
 
-  // Gram matrices and the five d x d products
-  const unsigned gb = (unsigned)ceil_div<int64_t>((int64_t)dd1, 256);
-  sf::k_gram<<<gb, 256, 0, s>>>(P->col_ptr, P->row_idx, P->csc_val, P->ell_idx, P->ell_val, P->k, d, AP);
-  sf::k_gram<<<gb, 256, 0, s>>>(Q->col_ptr, Q->row_idx, Q->csc_val, Q->ell_idx, Q->ell_val, Q->k, d, AQ);
-  SF_TRY(sf::check_launch("k_gram"));
+  // Gram matrices (P^T P as the gather of a dense copy of P with P; same for
+  // Q, reusing the buffer) and the five d x d products
+  float* dense = reinterpret_cast<float*>(w + f.off_dense);
+  float* gram_part = reinterpret_cast<float*>(w + f.off_gramp);
+  SF_CUDA_TRY(cudaMemsetAsync(dense, 0, (size_t)m * d * 4, s), "clear dense P");
+  sf::k_densify<<<(unsigned)ceil_div<int64_t>(m, 256), 256, 0, s>>>(P->ell_idx, P->ell_val, m, P->k, d, dense);
+  SF_TRY(sf::check_launch("k_densify"));
+  SF_TRY(sf::launch_gather<float>(P, dense, d, d, f.gram_p, AP, gram_part, s));
+  SF_CUDA_TRY(cudaMemsetAsync(dense, 0, (size_t)n * d * 4, s), "clear dense Q");
+  sf::k_densify<<<(unsigned)ceil_div<int64_t>(n, 256), 256, 0, s>>>(Q->ell_idx, Q->ell_val, n, Q->k, d, dense);
+  SF_TRY(sf::check_launch("k_densify"));
+  SF_TRY(sf::launch_gather<float>(Q, dense, d, d, f.gram_q, AQ, gram_part, s));
   const unsigned tiles = (unsigned)ceil_div(d, 64);
   sf::DdBatch b1{};
   b1.d = d;
   b1.job[0] = {S, AQ, W1, 0, 0};   // W1 = S A_Q
   b1.job[1] = {AP, S, W2, 0, 0};   // W2 = A_P S
-  sf::k_gemm_dd<<<dim3(tiles, tiles, 2), 256, 0, s>>>(b1);
+  const bool dd64 = d % 64 == 0;
+  if (dd64) sf::k_gemm_dd64<<<dim3(tiles, tiles, 2), 256, 0, s>>>(b1);
+  else sf::k_gemm_dd<<<dim3(tiles, tiles, 2), 256, 0, s>>>(b1);
   sf::DdBatch b2{};
   b2.d = d;
   b2.job[0] = {W2, AQ, X, 0, 0};   // X = A_P S A_Q
   b2.job[1] = {W1, S, K1, 0, 1};   // K1 = S A_Q S^T
   b2.job[2] = {S, W2, K2, 1, 0};   // K2 = S^T A_P S
-  sf::k_gemm_dd<<<dim3(tiles, tiles, 3), 256, 0, s>>>(b2);
+  if (dd64) sf::k_gemm_dd64<<<dim3(tiles, tiles, 3), 256, 0, s>>>(b2);
+  else sf::k_gemm_dd<<<dim3(tiles, tiles, 3), 256, 0, s>>>(b2);
   SF_TRY(sf::check_launch("k_gemm_dd"));
   sf::k_fit_combine<<<sf::kCombineBlocks, 256, 0, s>>>(S, X, W1, W2, d, HP, HQ, part);
   SF_TRY(sf::check_launch("k_fit_combine"));
@@ -2040,7 +2157,7 @@ sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G
                                                                       gQ);
   SF_TRY(sf::check_launch("k_fit_rowgrad"));
   if (loss) {
-    sf::k_fit_loss<<<1, 256, 0, s>>>(g2, f.n_g2, part, sf::kCombineBlocks, loss);
+    sf::k_fit_loss<<<1, 1024, 0, s>>>(g2, f.n_g2, part, sf::kCombineBlocks, loss);
     SF_TRY(sf::check_launch("k_fit_loss"));
   }
   const float lr32 = (float)lr;
