@@ -266,6 +266,23 @@ sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G
                                  double* loss, float* grad_P, float* grad_Q,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Dense products on the tensor cores (building block of the fused linear
+ * cross-entropy below; usable on its own).
+ *
+ * C = alpha * A * B^T            (accumulate = 0)
+ * C = C + alpha * A * B^T        (accumulate = 1)
+ *   A : device bf16 [M][lda], row-major, the first K columns used.
+ *   B : device bf16 [N][ldb], row-major, the first K columns used.
+ *   C : device fp32 [M][ldc], row-major.
+ * bf16 products accumulated in fp32 on the tensor cores (tcgen05.mma).
+ * A and B need 16-byte aligned bases and lda, ldb multiples of 8
+ * (SF_ERR_UNSUPPORTED otherwise); M, N, K >= 1; no other shape limits.
+ * Deterministic for a given shape. */
+sf_status sf_gemm_abt_bf16(const void* A, const void* B, float* C, int64_t M,
+                           int64_t N, int64_t K, int64_t lda, int64_t ldb,
+                           int64_t ldc, float alpha, int accumulate, void* stream);
+
 /* Copy a projector's current values, ELL order [rows * k] fp32, to device
  * memory `val` (after lsp_projector_fit_step they differ from the values
  * the projector was created with).  Out-of-range ids read as 0. */

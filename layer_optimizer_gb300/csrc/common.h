@@ -2,6 +2,8 @@
 // error-message plumbing, argument checks, small integer utilities.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
@@ -39,6 +41,20 @@ constexpr T ceil_div(T a, T b) { return (a + b - 1) / b; }
 
 // Number of SMs of the current device (cached per device).
 int sm_count();
+
+// cuTensorMapEncodeTiled from the driver (looked up once), or null.
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
+  return fn;
+}
 
 // Default bound for host waits, in milliseconds (SF_TIMEOUT_MS or 600 s).
 int64_t default_timeout_ms();
@@ -89,6 +105,12 @@ struct AdamConsts {
 // out-of-range index was skipped).
 int read_and_clear_device_error();
 int read_and_clear_device_error_adamw();
+int read_and_clear_device_error_gemm();
+
+// C = alpha A B^T (+ C) on the tensor cores (tc_gemm.cu): A [M][K] and
+// B [N][K] bf16 row-major, C fp32 [M][ldc].
+sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                      int64_t ldb, int64_t ldc, float alpha, bool accumulate, cudaStream_t s);
 
 sf_status make_adam_consts(const sf_adamw_hparams* hp, int64_t step, bool with_decay,
                            AdamConsts* out);

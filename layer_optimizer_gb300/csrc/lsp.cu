@@ -1120,19 +1120,6 @@ __global__ void k_apply_generic(const float* __restrict__ V, int64_t n, int64_t 
 // Host side
 // ----------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // Launch geometry of one gather (pure function of the sizes).
 struct GatherPlan {
   int warps, n_ar, cluster, n_cb, n_win, splits, win_per_split;

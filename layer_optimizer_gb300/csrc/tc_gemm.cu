@@ -1,0 +1,301 @@
+// Tensor-core GEMM on the 5th-generation tensor cores: C (fp32) = alpha A B^T
+// (+ C), A [M][K] and B [N][K] bf16 row-major (both K-contiguous).
+//
+// The dense products of the fused linear cross-entropy (logits, and the two
+// gradient products) are real dense contractions, so they run here rather
+// than on CUDA cores.  One CTA computes a 128 x 256 tile of C:
+//   warp 0       TMA producer: 64-wide K slabs of A (128 x 64) and B
+//                (256 x 64) into a 4-stage shared-memory ring, 128-byte
+//                swizzled, completion on an mbarrier per stage;
+//   warp 1       allocates 256 TMEM columns (the 128 x 256 fp32
+//                accumulator) and one elected thread issues tcgen05.mma
+//                (M 128, N 256, K 16, bf16 in, fp32 accumulate), four per
+//                slab; tcgen05.commit frees a stage when its MMAs are done
+//                and, after the last slab, signals the epilogue;
+//   warps 2..5   epilogue: each reads its 32 TMEM lanes (rows) with
+//                tcgen05.ld and writes (or adds into) C.
+// Every wait is bounded: a wait that runs out records an error for
+// sf_sync_status, and the CTA still releases its TMEM before it exits.
+// Sums over K run in slab order on the tensor cores; results are
+// deterministic for a given shape.
+#include <cuda_bf16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace sf {
+namespace {
+
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kStageA = kBM * kBK * 2;         // 16 KB
+constexpr int kStageB = kBN * kBK * 2;         // 32 KB
+constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kTmemCols = 256;
+constexpr int kGemmThreads = 192;
+constexpr size_t kGemmSmem = (size_t)kStages * kStageBytes + 1024 + 256;
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator
+// (bits 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), both K-major
+// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
+                            ((uint32_t)(kBM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with 128-byte swizzling: rows of 128 bytes (64 bf16 of K), 8-row atoms of
+// 1024 bytes (stride-dimension offset), descriptor version 1, layout type 2.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+  uint64_t d = (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading-dimension offset (unused when swizzled)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride-dimension offset: 1024 bytes
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A B^T for one K-16 step; accumulate = 0 overwrites D.
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `mbar` once every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+struct TcGemmArgs {
+  float* C;
+  int64_t ldc;
+  int32_t M, N, K;
+  float alpha;
+  int32_t accumulate;    // 1: C += alpha A B^T, 0: C = alpha A B^T
+  int32_t vec;           // C rows 16-byte aligned (float4 epilogue)
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+              const TcGemmArgs g) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* accum = empty + kStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t full_a = smem_u32(full), empty_a = smem_u32(empty), accum_a = smem_u32(accum);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
+  const int nk = (g.K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    prefetch_tensormap(&map_a);
+    prefetch_tensormap(&map_b);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(accum, 1);
+    fence_mbar_init_cluster();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      griddep_wait();
+      int s = 0;
+      uint32_t pass = 0;
+      int kb = 0;
+      for (; kb < nk; ++kb) {
+        if (kb >= kStages && !mbar_wait(&empty[s], pass ^ 1u)) break;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+        unsigned char* st = smem + (size_t)s * kStageBytes;
+        tma_load_2d(st, &map_a, &full[s], kb * kBK, m0);
+        tma_load_2d(st + kStageA, &map_b, &full[s], kb * kBK, n0);
+        if (++s == kStages) {
+          s = 0;
+          pass ^= 1u;
+        }
+      }
+      // the copies of the last stages have landed before the CTA can exit
+      // (immediate when the MMA thread consumed them; bounded otherwise)
+      for (int j = kb > kStages ? kb - kStages : 0; j < kb; ++j)
+        mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int s = 0;
+      uint32_t pass = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait(&full[s], pass)) break;
+        tc_fence_after();
+        const uint32_t a_addr = smem_base + (uint32_t)s * kStageBytes;
+        const uint64_t adesc = umma_desc_sw128(a_addr);
+        const uint64_t bdesc = umma_desc_sw128(a_addr + kStageA);
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)   // 16 bf16 = 32 bytes = 2 descriptor units along K
+          tc_mma(tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+        tc_commit(empty_a + 8u * (uint32_t)s);
+        if (++s == kStages) {
+          s = 0;
+          pass ^= 1u;
+        }
+      }
+      tc_commit(accum_a);
+    }
+  } else {
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = rows of the tile
+    const int quarter = warp & 3;
+    const bool ok = mbar_wait(accum, 0);
+    tc_fence_after();
+    const int row = m0 + 32 * quarter + lane;
+    const bool row_on = ok && row < g.M;
+    float* crow = g.C + (int64_t)row * g.ldc;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)c0, r);
+      tmem_ld_wait();
+      const int col0 = n0 + c0;
+      if (!row_on || col0 >= g.N) continue;
+      if (g.vec && col0 + 32 <= g.N) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          float4 v = make_float4(g.alpha * __uint_as_float(r[j]), g.alpha * __uint_as_float(r[j + 1]),
+                                 g.alpha * __uint_as_float(r[j + 2]), g.alpha * __uint_as_float(r[j + 3]));
+          float4* p = reinterpret_cast<float4*>(crow + col0 + j);
+          if (g.accumulate) {
+            const float4 o = *p;
+            v.x += o.x;
+            v.y += o.y;
+            v.z += o.z;
+            v.w += o.w;
+          }
+          *p = v;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (col0 + j < g.N) {
+            const float v = g.alpha * __uint_as_float(r[j]);
+            crow[col0 + j] = g.accumulate ? crow[col0 + j] + v : v;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+sf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return SF_OK;
+}
+
+}  // namespace
+
+// C = alpha A B^T (+ C); shared with the cross-entropy unit.
+sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                      int64_t ldb, int64_t ldc, float alpha, bool accumulate, cudaStream_t s) {
+  if (!A || !B || !C) return fail(SF_ERR_INVALID, "A, B or C is NULL");
+  if (M < 1 || N < 1 || K < 1) return fail(SF_ERR_INVALID, "M, N, K must be >= 1");
+  if (M > INT32_MAX - kBM || N > INT32_MAX - kBN || K > INT32_MAX - kBK)
+    return fail(SF_ERR_UNSUPPORTED, "M, N, K must be below 2^31");
+  if (lda < K || ldb < K || ldc < N) return fail(SF_ERR_INVALID, "leading dimensions must be >= K (A, B), N (C)");
+  if ((lda * 2) % 16 || (ldb * 2) % 16 || (reinterpret_cast<uintptr_t>(A) % 16) ||
+      (reinterpret_cast<uintptr_t>(B) % 16))
+    return fail(SF_ERR_UNSUPPORTED, "A and B need 16-byte aligned bases and rows (lda, ldb multiples of 8)");
+  if (!tensor_map_encoder()) return fail(SF_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available");
+  if ((M + kBM - 1) / kBM > 65535) return fail(SF_ERR_UNSUPPORTED, "M too large for one launch");
+  CUtensorMap ma, mb;
+  SF_TRY(make_map(&ma, A, M, K, lda, kBM));
+  SF_TRY(make_map(&mb, B, N, K, ldb, kBN));
+  TcGemmArgs g;
+  g.C = C;
+  g.ldc = ldc;
+  g.M = (int32_t)M;
+  g.N = (int32_t)N;
+  g.K = (int32_t)K;
+  g.alpha = alpha;
+  g.accumulate = accumulate ? 1 : 0;
+  g.vec = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0) ? 1 : 0;
+  static thread_local bool configured = false;
+  if (!configured) {
+    SF_CUDA_TRY(cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem),
+                "cudaFuncSetAttribute(k_tc_gemm)");
+    configured = true;
+  }
+  const dim3 grid((unsigned)((N + kBN - 1) / kBN), (unsigned)((M + kBM - 1) / kBM));
+  k_tc_gemm<<<grid, kGemmThreads, kGemmSmem, s>>>(ma, mb, g);
+  return check_launch("k_tc_gemm");
+}
+
+int read_and_clear_device_error_gemm() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_device_error, &z, sizeof z);
+  return v;
+}
+
+}  // namespace sf
+
+extern "C" {
+
+sf_status sf_gemm_abt_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                           int64_t ldb, int64_t ldc, float alpha, int accumulate, void* stream) {
+  sf::clear_error();
+  sf::NvtxRange nvtx_range("sf_gemm_abt_bf16");
+  return sf::tc_gemm_abt(A, B, C, M, N, K, lda, ldb, ldc, alpha, accumulate != 0, sf::as_stream(stream));
+}
+
+}  // extern "C"

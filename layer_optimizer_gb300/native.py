@@ -27,6 +27,7 @@ EXPORTS = [
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
     "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
+    "sf_gemm_abt_bf16",
 ]
 
 
@@ -100,6 +101,7 @@ _SIGS = {
     "lsp_projector_fit_step": (_ST, [_P, _P, _P, _INT, _I64, _I64, ctypes.c_double, _P, _P, _P, _P,
                                      ctypes.c_size_t, _P]),
     "lsp_projector_export_values": (_ST, [_P, _P, _P]),
+    "sf_gemm_abt_bf16": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _INT, _P]),
 }
 
 _lib = None
@@ -260,6 +262,11 @@ def lsp_projector_fit_step(P, Q, G, g_dtype, m, n, lr, loss, grad_P, grad_Q, ws,
 
 def lsp_projector_export_values(p, val, stream=None):
     _check(load().lsp_projector_export_values(p.handle, _addr(val), _stream(stream)))
+
+
+def sf_gemm_abt_bf16(A, B, C, M, N, K, lda, ldb, ldc, alpha=1.0, accumulate=False, stream=None):
+    _check(load().sf_gemm_abt_bf16(_addr(A), _addr(B), _addr(C), M, N, K, lda, ldb, ldc, float(alpha),
+                                   int(bool(accumulate)), _stream(stream)))
 
 
 # ------------------------------------------------------------------ (c) ----
