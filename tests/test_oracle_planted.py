@@ -129,3 +129,29 @@ def test_planted_fit_gradient_mistakes_fail_finite_differences(kind):
     bad = _broken_fit_grads(kind, G, P, Q)
     assert np.allclose(good, fd, rtol=1e-5, atol=1e-5)
     assert not np.allclose(bad, fd, rtol=1e-3, atol=1e-3)
+
+
+@pytest.mark.parametrize("kind", ["divide_by_all_tokens", "no_onehot", "transposed_weight_grad"])
+def test_planted_lce_mistakes_fail_the_torch_pin(kind):
+    rng = np.random.default_rng(12)
+    N, D, V = 10, 6, 9
+    H, W = rng.normal(size=(N, D)), rng.normal(size=(V, D)) * 0.3
+    y = rng.integers(0, V, size=N)
+    y[[1, 4]] = -100
+    Z = H @ W.T
+    P = np.exp(Z - Z.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    valid = y != -100
+    dZ = np.where(valid[:, None], P, 0.0)
+    if kind != "no_onehot":
+        dZ[np.flatnonzero(valid), y[valid]] -= 1.0
+    dZ /= N if kind == "divide_by_all_tokens" else valid.sum()
+    dW = (H.T @ dZ)[:, :V].T if kind == "transposed_weight_grad" and D >= V else dZ.T @ H
+    if kind == "transposed_weight_grad":
+        dW = dW[::-1]                                # rows in the wrong order
+    Ht, Wt = torch.tensor(H, requires_grad=True), torch.tensor(W, requires_grad=True)
+    torch.nn.functional.cross_entropy(Ht @ Wt.T, torch.tensor(y), ignore_index=-100).backward()
+    from oracle.lce import lce
+    good = lce(H, W, y)
+    assert np.allclose(good["dW"], Wt.grad.numpy()) and np.allclose(good["dH"], Ht.grad.numpy())
+    assert not (np.allclose(dZ @ W, Ht.grad.numpy()) and np.allclose(dW, Wt.grad.numpy()))
