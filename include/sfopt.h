@@ -283,6 +283,40 @@ sf_status sf_gemm_abt_bf16(const void* A, const void* B, float* C, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb,
                            int64_t ldc, float alpha, int accumulate, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Fused linear cross-entropy (SlideFormer, "Fused LinearCrossEntropy" in the
+ * summaries' kernel lists: the output projection and the loss fused, the
+ * gradients computed in small blocks so the full logits tensor is never
+ * held).  For hidden states H (N tokens x D) and an output layer W (V x D):
+ *
+ *   z_i  = W h_i,   n = number of tokens whose label != ignore_index
+ *   loss = (1/n) sum_{labelled i} ( logsumexp(z_i) - z_i[label_i] )
+ *   dH   = dZ W,   dW = dZ^T H,   dZ_i = (softmax(z_i) - onehot(label_i)) / n
+ *          (dZ_i = 0 for unlabelled tokens; loss = 0 and no gradient if n = 0)
+ *
+ *   H      : device bf16 [N][D] row-major;  W : device bf16 [V][D] row-major.
+ *   labels : device int32 [N]; a label outside [0, V) that is not
+ *            ignore_index counts as unlabelled and is reported by
+ *            sf_sync_status (SF_ERR_INVALID).
+ *   chunk  : tokens per block (a positive multiple of 8; the call holds one
+ *            chunk of fp32 logits and two of the bf16 gradient).
+ *   loss   : device double [1], written; may be NULL.
+ *   dH     : device fp32 [N][D], written; may be NULL.
+ *   dW     : device fp32 [V][D], written; may be NULL (both NULL: loss only).
+ *   ws     : device scratch of ws_bytes >= lce_workspace_bytes(N, D, V,
+ *            chunk), 256-byte aligned.
+ * Logits: bf16 products summed in fp32 on the tensor cores.  The row
+ * statistics are fp32; dZ is rounded to bf16 (nearest even) before the two
+ * gradient products, which run on the tensor cores with fp32 sums.
+ * D and V must be multiples of 8 and H, W, dH, dW 16-byte aligned
+ * (SF_ERR_UNSUPPORTED otherwise).  Deterministic. */
+size_t lce_workspace_bytes(int64_t n_tokens, int64_t d, int64_t vocab, int64_t chunk);
+
+sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labels,
+                               int64_t N, int64_t D, int64_t V, int64_t chunk,
+                               int32_t ignore_index, double* loss, float* dH,
+                               float* dW, void* ws, size_t ws_bytes, void* stream);
+
 /* Copy a projector's current values, ELL order [rows * k] fp32, to device
  * memory `val` (after lsp_projector_fit_step they differ from the values
  * the projector was created with).  Out-of-range ids read as 0. */

@@ -116,7 +116,7 @@ sf_status sf_sync_status(void* stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return sf::cuda_fail(e, "sf_sync_status");
   const int dev_err = sf::read_and_clear_device_error() | sf::read_and_clear_device_error_adamw() |
-                      sf::read_and_clear_device_error_gemm();
+                      sf::read_and_clear_device_error_gemm() | sf::read_and_clear_device_error_lce();
   if (dev_err & 1) return sf::fail(SF_ERR_TIMEOUT, "a kernel wait ran out of its bound (device error word %d)", dev_err);
   if (dev_err & 2) return sf::fail(SF_ERR_INVALID, "a kernel skipped an out-of-range index (device error word %d)", dev_err);
   return SF_OK;

@@ -106,6 +106,7 @@ struct AdamConsts {
 int read_and_clear_device_error();
 int read_and_clear_device_error_adamw();
 int read_and_clear_device_error_gemm();
+int read_and_clear_device_error_lce();
 
 // C = alpha A B^T (+ C) on the tensor cores (tc_gemm.cu): A [M][K] and
 // B [N][K] bf16 row-major, C fp32 [M][ldc].

@@ -1,0 +1,272 @@
+// Fused linear cross-entropy: loss and gradients of the softmax
+// cross-entropy of a linear output layer, chunked over tokens so that the
+// full logits tensor is never held.
+//
+// SlideFormer ("An Efficient Heterogeneous Co-Design for Fine-Tuning on a
+// Single GPU"; the summaries' kernel lists, "Fused LinearCrossEntropy")
+// fuses the output projection with the loss and computes the gradients in
+// small blocks, so the logits (tokens x vocabulary, larger than every other
+// activation for big vocabularies) never exist in full.  For each chunk of
+// tokens c:
+//   Z_c  = H_c W^T                      tensor cores, fp32 [chunk][V]
+//   lse  = logsumexp over each row of Z_c, and the rows' losses
+//   G_c  = (softmax(Z_c) - onehot(y_c)) / n  rounded to bf16, written both
+//          as [chunk][V] and transposed [V][chunk]
+//   dH_c = G_c W                        tensor cores (W^T made once per call)
+//   dW  += G_c^T H_c                    tensor cores (H_c^T made per chunk)
+// n is the number of tokens whose label is not ignore_index.  The three
+// products run on the tensor-core GEMM (tc_gemm.cu); the row statistics and
+// the gradient tile are fp32 CUDA-core kernels.  Memory: one chunk of
+// logits (fp32) and two of the bf16 gradient instead of N x V.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace sf {
+namespace {
+
+constexpr int kLseThreads = 256;
+
+// out[c][r] = in[r][c] for a rows x cols bf16 matrix (row pitches ld_in,
+// ld_out), through a padded 64 x 64 tile.
+__global__ void __launch_bounds__(256) k_transpose_bf16(const uint16_t* __restrict__ in, int64_t rows,
+                                                        int64_t cols, int64_t ld_in, uint16_t* __restrict__ out,
+                                                        int64_t ld_out) {
+  __shared__ uint16_t tile[64][66];
+  const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  for (int r = ty; r < 64; r += 4)
+    if (r0 + r < rows && c0 + tx < cols) tile[r][tx] = in[(r0 + r) * ld_in + c0 + tx];
+  __syncthreads();
+  for (int c = ty; c < 64; c += 4)
+    if (c0 + c < cols && r0 + tx < rows) out[(c0 + c) * ld_out + r0 + tx] = tile[tx][c];
+}
+
+// Number n of labelled tokens (label != ignore and in [0, V)); a label that
+// is neither is counted as unlabelled and flagged.  inv_n = 1/n (0 if n = 0).
+__global__ void __launch_bounds__(1024) k_lce_count(const int32_t* __restrict__ labels, int64_t N, int64_t V,
+                                                    int32_t ignore, int64_t* __restrict__ n_out,
+                                                    float* __restrict__ inv_n) {
+  __shared__ int64_t red[1024];
+  int64_t c = 0;
+  bool bad = false;
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) {
+    const int32_t y = labels[i];
+    if (y == ignore) continue;
+    if (y < 0 || y >= V) bad = true;
+    else ++c;
+  }
+  if (bad) atomicOr(&g_device_error, kDevErrIndex);
+  red[threadIdx.x] = c;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    *n_out = red[0];
+    *inv_n = red[0] > 0 ? (float)(1.0 / (double)red[0]) : 0.0f;
+  }
+}
+
+__device__ __forceinline__ bool labelled(int32_t y, int32_t ignore, int64_t V) {
+  return y != ignore && y >= 0 && y < V;
+}
+
+// One block per row of the chunk: lse = log sum_j exp(z_j), by a running
+// (max, sum) per thread over a fixed strided set of columns, then a fixed
+// tree; the row's loss lse - z[y] (0 for an unlabelled token).
+__global__ void __launch_bounds__(kLseThreads) k_lce_lse(const float* __restrict__ Z, int64_t V,
+                                                         const int32_t* __restrict__ labels, int32_t ignore,
+                                                         float* __restrict__ lse, float* __restrict__ row_loss) {
+  __shared__ float sm[kLseThreads], ss[kLseThreads];
+  const int64_t r = blockIdx.x;
+  const float* z = Z + r * V;
+  float m = -INFINITY, s = 0.0f;
+  for (int64_t j = threadIdx.x; j < V; j += kLseThreads) {
+    const float x = z[j];
+    if (x > m) {
+      s = s * expf(m - x) + 1.0f;
+      m = x;
+    } else {
+      s += expf(x - m);
+    }
+  }
+  sm[threadIdx.x] = m;
+  ss[threadIdx.x] = s;
+  __syncthreads();
+  for (int st = kLseThreads / 2; st > 0; st >>= 1) {
+    if ((int)threadIdx.x < st) {
+      const float m1 = sm[threadIdx.x], m2 = sm[threadIdx.x + st];
+      const float s1 = ss[threadIdx.x], s2 = ss[threadIdx.x + st];
+      const float mm = fmaxf(m1, m2);
+      const float a = m1 == -INFINITY ? 0.0f : s1 * expf(m1 - mm);
+      const float b = m2 == -INFINITY ? 0.0f : s2 * expf(m2 - mm);
+      sm[threadIdx.x] = mm;
+      ss[threadIdx.x] = a + b;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const float l = sm[0] + logf(ss[0]);
+    lse[r] = l;
+    const int32_t y = labels[r];
+    row_loss[r] = labelled(y, ignore, V) ? l - z[y] : 0.0f;
+  }
+}
+
+// The gradient tile: g = (exp(z - lse) - [j == y]) * inv_n (0 for an
+// unlabelled row), rounded to bf16, written to G [rows][V] and, through
+// shared memory, to Gt [V][ld_gt] (columns = rows of the chunk).
+__global__ void __launch_bounds__(256) k_lce_grad(const float* __restrict__ Z, int64_t rows, int64_t V,
+                                                  const float* __restrict__ lse, const int32_t* __restrict__ labels,
+                                                  int32_t ignore, const float* __restrict__ inv_n,
+                                                  __nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__ Gt,
+                                                  int64_t ld_gt) {
+  __shared__ __nv_bfloat16 tile[64][66];
+  const int64_t r0 = (int64_t)blockIdx.y * 64, j0 = (int64_t)blockIdx.x * 64;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  const float sc = *inv_n;
+  for (int r = ty; r < 64; r += 4) {
+    const int64_t i = r0 + r, j = j0 + tx;
+    if (i < rows && j < V) {
+      const int32_t y = labels[i];
+      float g = 0.0f;
+      if (labelled(y, ignore, V)) g = (expf(Z[i * V + j] - lse[i]) - (j == y ? 1.0f : 0.0f)) * sc;
+      const __nv_bfloat16 b = __float2bfloat16_rn(g);
+      G[i * V + j] = b;
+      tile[r][tx] = b;
+    }
+  }
+  __syncthreads();
+  for (int c = ty; c < 64; c += 4) {
+    const int64_t j = j0 + c, i = r0 + tx;
+    if (j < V && i < rows) Gt[j * ld_gt + i] = tile[tx][c];
+  }
+}
+
+// loss = sum of the rows' losses * inv_n, in fp64 and a fixed order.
+__global__ void __launch_bounds__(1024) k_lce_loss(const float* __restrict__ row_loss, int64_t N,
+                                                   const float* __restrict__ inv_n, double* __restrict__ loss) {
+  __shared__ double red[1024];
+  double a = 0.0;
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) a += (double)row_loss[i];
+  red[threadIdx.x] = a;
+  __syncthreads();
+  for (int s = blockDim.x / 2; s > 0; s >>= 1) {
+    if ((int)threadIdx.x < s) red[threadIdx.x] += red[threadIdx.x + s];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = red[0] * (double)*inv_n;
+}
+
+struct LcePlan {
+  size_t off_z, off_g, off_gt, off_wt, off_ht, off_lse, off_rowloss, off_n, bytes;
+};
+
+LcePlan plan_lce(int64_t N, int64_t D, int64_t V, int64_t chunk) {
+  LcePlan p;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = (off + bytes + 255) / 256 * 256;
+    return o;
+  };
+  p.off_z = take((size_t)chunk * V * 4);
+  p.off_g = take((size_t)chunk * V * 2);
+  p.off_gt = take((size_t)V * chunk * 2);
+  p.off_wt = take((size_t)D * V * 2);
+  p.off_ht = take((size_t)D * chunk * 2);
+  p.off_lse = take((size_t)chunk * 4);
+  p.off_rowloss = take((size_t)N * 4);
+  p.off_n = take(16);
+  p.bytes = off;
+  return p;
+}
+
+}  // namespace
+
+int read_and_clear_device_error_lce() {
+  int v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_device_error, &z, sizeof z);
+  return v;
+}
+
+}  // namespace sf
+
+extern "C" {
+
+size_t lce_workspace_bytes(int64_t n_tokens, int64_t d, int64_t vocab, int64_t chunk) {
+  if (n_tokens < 1 || d < 1 || vocab < 1 || chunk < 1) return 0;
+  return sf::plan_lce(n_tokens, d, vocab, std::min(chunk, (n_tokens + 7) / 8 * 8)).bytes;
+}
+
+sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labels, int64_t N, int64_t D, int64_t V,
+                               int64_t chunk, int32_t ignore_index, double* loss, float* dH, float* dW, void* ws,
+                               size_t ws_bytes, void* stream_) {
+  sf::clear_error();
+  sf::NvtxRange nvtx_range("lce_forward_backward");
+  if (!H || !W || !labels) return sf::fail(SF_ERR_INVALID, "H, W or labels is NULL");
+  if (N < 1 || D < 1 || V < 1) return sf::fail(SF_ERR_INVALID, "N, D, V must be >= 1");
+  if (D % 8 || V % 8) return sf::fail(SF_ERR_UNSUPPORTED, "D and V must be multiples of 8 (16-byte rows)");
+  if (chunk < 8 || chunk % 8) return sf::fail(SF_ERR_INVALID, "chunk must be a positive multiple of 8");
+  if ((reinterpret_cast<uintptr_t>(H) % 16) || (reinterpret_cast<uintptr_t>(W) % 16))
+    return sf::fail(SF_ERR_UNSUPPORTED, "H and W need 16-byte aligned bases");
+  if ((dH && reinterpret_cast<uintptr_t>(dH) % 16) || (dW && reinterpret_cast<uintptr_t>(dW) % 16))
+    return sf::fail(SF_ERR_UNSUPPORTED, "dH and dW need 16-byte aligned bases");
+  chunk = std::min(chunk, (N + 7) / 8 * 8);
+  if ((chunk + 63) / 64 > 65535 || (V + 63) / 64 > (int64_t)INT32_MAX || N > (int64_t)INT32_MAX)
+    return sf::fail(SF_ERR_UNSUPPORTED, "sizes too large");
+  const sf::LcePlan p = sf::plan_lce(N, D, V, chunk);
+  if (!ws || ws_bytes < p.bytes || (reinterpret_cast<uintptr_t>(ws) % 256))
+    return sf::fail(SF_ERR_INVALID, "workspace needs %zu bytes, 256-byte aligned (got %zu)", p.bytes, ws_bytes);
+  cudaStream_t s = sf::as_stream(stream_);
+  char* w = static_cast<char*>(ws);
+  float* Z = reinterpret_cast<float*>(w + p.off_z);
+  __nv_bfloat16* G = reinterpret_cast<__nv_bfloat16*>(w + p.off_g);
+  __nv_bfloat16* Gt = reinterpret_cast<__nv_bfloat16*>(w + p.off_gt);
+  uint16_t* Wt = reinterpret_cast<uint16_t*>(w + p.off_wt);
+  uint16_t* Ht = reinterpret_cast<uint16_t*>(w + p.off_ht);
+  float* lse = reinterpret_cast<float*>(w + p.off_lse);
+  float* row_loss = reinterpret_cast<float*>(w + p.off_rowloss);
+  int64_t* n_valid = reinterpret_cast<int64_t*>(w + p.off_n);
+  float* inv_n = reinterpret_cast<float*>(w + p.off_n + 8);
+  const uint16_t* Hb = static_cast<const uint16_t*>(H);
+  const bool grads = dH || dW;
+
+  sf::k_lce_count<<<1, 1024, 0, s>>>(labels, N, V, ignore_index, n_valid, inv_n);
+  SF_TRY(sf::check_launch("k_lce_count"));
+  if (dH) {
+    sf::k_transpose_bf16<<<dim3((unsigned)sf::ceil_div<int64_t>(D, 64), (unsigned)sf::ceil_div<int64_t>(V, 64)), 256, 0, s>>>(
+        static_cast<const uint16_t*>(W), V, D, D, Wt, V);
+    SF_TRY(sf::check_launch("k_transpose_bf16"));
+  }
+  for (int64_t c0 = 0; c0 < N; c0 += chunk) {
+    const int64_t rows = std::min(chunk, N - c0);
+    SF_TRY(sf::tc_gemm_abt(Hb + c0 * D, W, Z, rows, V, D, D, D, V, 1.0f, false, s));
+    sf::k_lce_lse<<<(unsigned)rows, sf::kLseThreads, 0, s>>>(Z, V, labels + c0, ignore_index, lse, row_loss + c0);
+    SF_TRY(sf::check_launch("k_lce_lse"));
+    if (!grads) continue;
+    sf::k_lce_grad<<<dim3((unsigned)sf::ceil_div<int64_t>(V, 64), (unsigned)sf::ceil_div<int64_t>(rows, 64)), 256, 0, s>>>(
+        Z, rows, V, lse, labels + c0, ignore_index, inv_n, G, Gt, chunk);
+    SF_TRY(sf::check_launch("k_lce_grad"));
+    if (dH) SF_TRY(sf::tc_gemm_abt(G, Wt, dH + c0 * D, rows, D, V, V, V, D, 1.0f, false, s));
+    if (dW) {
+      sf::k_transpose_bf16<<<dim3((unsigned)sf::ceil_div<int64_t>(D, 64), (unsigned)sf::ceil_div<int64_t>(rows, 64)), 256, 0,
+                             s>>>(Hb + c0 * D, rows, D, D, Ht, chunk);
+      SF_TRY(sf::check_launch("k_transpose_bf16"));
+      SF_TRY(sf::tc_gemm_abt(Gt, Ht, dW, V, D, rows, chunk, chunk, D, 1.0f, c0 > 0, s));
+    }
+  }
+  if (loss) {
+    sf::k_lce_loss<<<1, 1024, 0, s>>>(row_loss, N, inv_n, loss);
+    SF_TRY(sf::check_launch("k_lce_loss"));
+  }
+  return SF_OK;
+}
+
+}  // extern "C"

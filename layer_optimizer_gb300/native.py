@@ -27,7 +27,7 @@ EXPORTS = [
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
     "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
-    "sf_gemm_abt_bf16",
+    "sf_gemm_abt_bf16", "lce_workspace_bytes", "lce_forward_backward",
 ]
 
 
@@ -102,6 +102,8 @@ _SIGS = {
                                      ctypes.c_size_t, _P]),
     "lsp_projector_export_values": (_ST, [_P, _P, _P]),
     "sf_gemm_abt_bf16": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _INT, _P]),
+    "lce_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
+    "lce_forward_backward": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
 _lib = None
@@ -267,6 +269,15 @@ def lsp_projector_export_values(p, val, stream=None):
 def sf_gemm_abt_bf16(A, B, C, M, N, K, lda, ldb, ldc, alpha=1.0, accumulate=False, stream=None):
     _check(load().sf_gemm_abt_bf16(_addr(A), _addr(B), _addr(C), M, N, K, lda, ldb, ldc, float(alpha),
                                    int(bool(accumulate)), _stream(stream)))
+
+
+def lce_workspace_bytes(n_tokens, d, vocab, chunk):
+    return load().lce_workspace_bytes(n_tokens, d, vocab, chunk)
+
+
+def lce_forward_backward(H, W, labels, N, D, V, chunk, ignore_index, loss, dH, dW, ws, ws_bytes, stream=None):
+    _check(load().lce_forward_backward(_addr(H), _addr(W), _addr(labels), N, D, V, chunk, ignore_index, _addr(loss),
+                                       _addr(dH), _addr(dW), _addr(ws), ws_bytes, _stream(stream)))
 
 
 # ------------------------------------------------------------------ (c) ----
