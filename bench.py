@@ -45,6 +45,7 @@ sys.path.insert(0, ROOT)
 HP = dict(lr=1e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)
 ADAM_BYTES_PER_PARAM = 28        # 2 B grad + 3 x (4 B read + 4 B write) + 2 B bf16 weight
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0   # dense bf16, burst (no measured-peaks file on this machine)
 
 
 def parse():
@@ -56,12 +57,15 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-lsp", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-lce", action="store_true")
     ap.add_argument("--layers", type=int, default=24, help="OPT-1.3B layers (24 = the full stack)")
     ap.add_argument("--workload", default="opt-1.3b", choices=["opt-1.3b", "llama2-7b", "mistral-window"],
                     help="opt-1.3b: the headline stack; llama2-7b: the full LLaMA-2-7B step resident in HBM; "
                          "mistral-window: four Mistral-Large layers in pinned host memory through 2 device slots")
     ap.add_argument("--profile-small", action="store_true",
                     help="1 layer, 1 warm-up + 1 timed step, no extras: a small case for ncu captures")
+    ap.add_argument("--profile-lce", action="store_true",
+                    help="only the fused linear cross-entropy, 1 warm-up + 1 timed call (ncu case)")
     ap.add_argument("--profile-lsp", action="store_true",
                     help="only the projector chain on one 4096 x 4096 matrix, 1 warm-up + 1 timed rep (ncu case)")
     return ap.parse_args()
@@ -113,6 +117,20 @@ def measured_peak_hbm():
         except Exception:
             pass
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_peak_bf16():
+    """Dense bf16 tensor peak in TFLOP/s: the measured burst figure if the file has one, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            for k in ("bf16_tflops", "bf16_TFLOPs"):
+                if k in d and isinstance(d[k], (int, float)):
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def kernel_traffic(kernel):
@@ -582,6 +600,50 @@ def run_lsp(args, matrices=None):
     return out
 
 
+def run_lce(args, N=8192, D=4096, V=128256, chunk=2048):
+    """Fused linear cross-entropy (loss, dH, dW) on a Llama-3.1-8B output layer."""
+    import torch
+
+    from layer_optimizer_gb300 import native, synth
+    H = synth.fill_normal_(torch.empty(N, D, dtype=torch.bfloat16, device="cuda"), 1.0, synth.sub_seed(21, 0))
+    W = synth.fill_normal_(torch.empty(V, D, dtype=torch.bfloat16, device="cuda"), 0.02, synth.sub_seed(21, 1))
+    g = torch.Generator(device="cuda")
+    g.manual_seed(synth.sub_seed(21, 2))
+    y = torch.randint(0, V, (N,), generator=g, device="cuda", dtype=torch.int32)
+    wsb = native.lce_workspace_bytes(N, D, V, chunk)
+    ws = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    loss = torch.empty(1, dtype=torch.float64, device="cuda")
+    dH = torch.empty(N, D, device="cuda")
+    dW = torch.empty(V, D, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def call():
+        native.lce_forward_backward(H, W, y, N, D, V, chunk, -100, loss, dH, dW, ws, wsb, stream)
+    reps = 1 if args.profile_lce else max(3, args.steps // 4)
+    for _ in range(1 if args.profile_lce else args.warmup):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    flops = 6.0 * N * V * D
+    peak, kind = measured_peak_bf16()
+    out = {"workload": f"Llama-3.1-8B output layer: {N} tokens, D {D}, V {V}, chunks of {chunk}; bf16 H and W, "
+                       "fp32 dH and dW",
+           "ms": ms, "tokens_per_s": N / (ms / 1e3),
+           "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": peak, "unit": "TFLOP/s",
+                        "frac": flops / ms / 1e9 / peak, "peak_kind": f"{kind} (of {kind})",
+                        "flops_per_call": flops},
+           "logits_bytes_full": N * V * 4, "workspace_bytes": wsb, "loss": float(loss.item())}
+    del H, W, dH, dW, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def host_update_rate(steps=3):
     """The same AdamW step on all host cores (sf_adamw_host_step), one OPT-1.3B layer in host memory."""
     import torch
@@ -807,6 +869,11 @@ def main_ours(args, rank, world):
             line["lsp"] = run_lsp(args)
         except Exception as ex:  # the line still prints; the failure is recorded on it
             line["lsp"] = {"error": str(ex)[:300]}
+    if not args.no_lce and rank == 0 and args.workload == "opt-1.3b":
+        try:
+            line["lce"] = run_lce(args)
+        except Exception as ex:
+            line["lce"] = {"error": str(ex)[:300]}
     if not args.no_cpu and rank == 0 and args.workload == "opt-1.3b":
         line["host_update"] = host_update_rate()
     if not args.no_cpu and rank == 0:
@@ -848,6 +915,12 @@ def main():
     if args.profile_small:
         args.layers, args.steps, args.warmup = 1, 1, 1
         args.no_e2e = args.no_lsp = args.no_cpu = True
+    if args.profile_lce:
+        import torch
+        from layer_optimizer_gb300 import native
+        native.load()
+        print(json.dumps({"profile_lce": run_lce(args, N=2048)}))
+        return
     if args.profile_lsp:
         import torch
         from layer_optimizer_gb300 import native
