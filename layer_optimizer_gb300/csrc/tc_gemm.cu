@@ -94,6 +94,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Tensor store / reduce-add of a shared-memory box into global memory
+// (bulk async group of this thread), and the group waits.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   map),
+               "r"(src), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void sts_f4(uint32_t a, float x, float y, float z, float w) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w) : "memory");
+}
+
 struct TcGemmArgs {
   float* C;
   int64_t ldc;
@@ -101,11 +122,12 @@ struct TcGemmArgs {
   float alpha;
   int32_t accumulate;    // 1: C += alpha A B^T, 0: C = alpha A B^T
   int32_t vec;           // C rows 16-byte aligned (float4 epilogue)
+  int32_t tma;           // C written by tensor stores (reduce-add when accumulating) from shared memory
 };
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-              const TcGemmArgs g) {
+              const __grid_constant__ CUtensorMap map_c, const TcGemmArgs g) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
@@ -189,6 +211,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row = m0 + 32 * quarter + lane;
     const bool row_on = ok && row < g.M;
     float* crow = g.C + (int64_t)row * g.ldc;
+    if (g.tma) {
+      // 32 x 32 boxes through two 4 KB staging buffers per warp (in the idle
+      // stage-0 ring memory), 128-byte swizzled to match the store's tensor
+      // map (conflict-free 16-byte writes); one thread stores or reduce-adds
+      // each box, and a buffer is rewritten only once its store has read it
+      const uint32_t stg = smem_base + (uint32_t)(warp - 2) * 8192u;
+      const int row0 = m0 + 32 * quarter;
+#pragma unroll 1
+      for (int ci = 0; ci < kBN / 32; ++ci) {
+        uint32_t r[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(32 * ci), r);
+        tmem_ld_wait();
+        const uint32_t buf = stg + (uint32_t)(ci & 1) * 4096u;
+        if (ci >= 2) {
+          if (lane == 0) bulk_wait_read_1();
+          __syncwarp();
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          sts_f4(buf + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) * 16), g.alpha * __uint_as_float(r[4 * q]),
+                 g.alpha * __uint_as_float(r[4 * q + 1]), g.alpha * __uint_as_float(r[4 * q + 2]),
+                 g.alpha * __uint_as_float(r[4 * q + 3]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (ok && row0 < g.M && n0 + 32 * ci < g.N) {
+            if (g.accumulate) tma_reduce_add_2d(&map_c, buf, n0 + 32 * ci, row0);
+            else tma_store_2d(&map_c, buf, n0 + 32 * ci, row0);
+          }
+          bulk_commit();
+        }
+        __syncwarp();
+      }
+      if (lane == 0) bulk_wait_all();
+    } else
 #pragma unroll 1
     for (int c0 = 0; c0 < kBN; c0 += 32) {
       uint32_t r[32];
@@ -230,6 +287,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+sf_status make_map_c(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t ldc) {
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+  cuuint64_t strides[1] = {(cuuint64_t)(ldc * 4)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, C, dims, strides, box, estr,
+                                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled (C) failed (%d)", (int)r);
+  return SF_OK;
+}
+
 sf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
@@ -269,6 +338,9 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
   g.alpha = alpha;
   g.accumulate = accumulate ? 1 : 0;
   g.vec = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0) ? 1 : 0;
+  g.tma = g.vec;
+  CUtensorMap mc = ma;       // unused unless g.tma
+  if (g.tma) SF_TRY(make_map_c(&mc, C, M, N, ldc));
   static thread_local bool configured = false;
   if (!configured) {
     SF_CUDA_TRY(cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem),
@@ -276,7 +348,7 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
     configured = true;
   }
   const dim3 grid((unsigned)((N + kBN - 1) / kBN), (unsigned)((M + kBM - 1) / kBM));
-  k_tc_gemm<<<grid, kGemmThreads, kGemmSmem, s>>>(ma, mb, g);
+  k_tc_gemm<<<grid, kGemmThreads, kGemmSmem, s>>>(ma, mb, mc, g);
   return check_launch("k_tc_gemm");
 }
 
