@@ -3,22 +3,28 @@
 //
 // The dense products of the fused linear cross-entropy (logits, and the two
 // gradient products) are real dense contractions, so they run here rather
-// than on CUDA cores.  One CTA computes a 128 x 256 tile of C:
+// than on CUDA cores.  A persistent grid (one CTA per SM) walks the 128 x 256
+// tiles of C; in each CTA:
 //   warp 0       TMA producer: 64-wide K slabs of A (128 x 64) and B
 //                (256 x 64) into a 4-stage shared-memory ring, 128-byte
 //                swizzled, completion on an mbarrier per stage;
-//   warp 1       allocates 256 TMEM columns (the 128 x 256 fp32
-//                accumulator) and one elected thread issues tcgen05.mma
+//   warp 1       allocates 512 TMEM columns (two 128 x 256 fp32
+//                accumulators) and one elected thread issues tcgen05.mma
 //                (M 128, N 256, K 16, bf16 in, fp32 accumulate), four per
-//                slab; tcgen05.commit frees a stage when its MMAs are done
-//                and, after the last slab, signals the epilogue;
+//                slab, into the accumulator the epilogue has released;
+//                tcgen05.commit frees a stage when its MMAs are done and,
+//                after a tile's last slab, hands the accumulator over;
 //   warps 2..5   epilogue: each reads its 32 TMEM lanes (rows) with
-//                tcgen05.ld and writes (or adds into) C.
+//                tcgen05.ld and writes (or reduce-adds into) C by tensor
+//                stores from shared memory, while the next tile's MMAs run
+//                into the other accumulator.
 // Every wait is bounded: a wait that runs out records an error for
 // sf_sync_status, and the CTA still releases its TMEM before it exits.
 // Sums over K run in slab order on the tensor cores; results are
 // deterministic for a given shape.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "common.h"
 #include "ptx.cuh"
@@ -30,9 +36,10 @@ constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
 constexpr int kStageA = kBM * kBK * 2;         // 16 KB
 constexpr int kStageB = kBN * kBK * 2;         // 32 KB
 constexpr int kStageBytes = kStageA + kStageB;
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 256;                 // one accumulator; two are allocated
 constexpr int kGemmThreads = 192;
-constexpr size_t kGemmSmem = (size_t)kStages * kStageBytes + 1024 + 256;
+constexpr int kStagingBytes = 4 * 2 * 4096;    // epilogue: 4 warps x 2 boxes of 32 x 32 fp32
+constexpr size_t kGemmSmem = (size_t)kStages * kStageBytes + kStagingBytes + 1024 + 256;
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator
 // (bits 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), both K-major
@@ -130,16 +137,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const __grid_constant__ CUtensorMap map_c, const TcGemmArgs g) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
+  // [ring: kStages x (A 16 KB + B 32 KB)] [epilogue staging: 4 warps x 2 x 4 KB] [barriers]
+  unsigned char* staging = smem + (size_t)kStages * kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* accum = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* tfull = empty + kStages;     // [2] accumulator buffer b holds a finished tile
+  uint64_t* tempty = tfull + 2;          // [2] accumulator buffer b has been read out
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   const uint32_t smem_base = smem_u32(smem);
-  const uint32_t full_a = smem_u32(full), empty_a = smem_u32(empty), accum_a = smem_u32(accum);
+  const uint32_t empty_a = smem_u32(empty), tfull_a = smem_u32(tfull);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * kBN;
   const int nk = (g.K + kBK - 1) / kBK;
+  const int m_tiles = (g.M + kBM - 1) / kBM;
+  const int n_tiles = (g.N + kBN - 1) / kBN;
+  const int tiles = m_tiles * n_tiles;
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&map_a);
@@ -148,11 +160,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(accum, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);          // one arrival per epilogue warp
+    }
     fence_mbar_init_cluster();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), 2 * kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -160,130 +175,163 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // tiles t = blockIdx.x, + gridDim.x, ...; m fastest, so the CTAs working
+  // at the same time share B tiles in L2
   if (warp == 0) {
     if (lane == 0) {
       griddep_wait();
-      int s = 0;
+      int s = 0, issued = 0;
       uint32_t pass = 0;
-      int kb = 0;
-      for (; kb < nk; ++kb) {
-        if (kb >= kStages && !mbar_wait(&empty[s], pass ^ 1u)) break;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
-        unsigned char* st = smem + (size_t)s * kStageBytes;
-        tma_load_2d(st, &map_a, &full[s], kb * kBK, m0);
-        tma_load_2d(st + kStageA, &map_b, &full[s], kb * kBK, n0);
-        if (++s == kStages) {
-          s = 0;
-          pass ^= 1u;
+      bool failed = false;
+      for (int t = blockIdx.x; t < tiles && !failed; t += gridDim.x) {
+        const int m0 = (t % m_tiles) * kBM, n0 = (t / m_tiles) * kBN;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (issued >= kStages && !mbar_wait(&empty[s], pass ^ 1u)) {
+            failed = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+          unsigned char* st = smem + (size_t)s * kStageBytes;
+          tma_load_2d(st, &map_a, &full[s], kb * kBK, m0);
+          tma_load_2d(st + kStageA, &map_b, &full[s], kb * kBK, n0);
+          ++issued;
+          if (++s == kStages) {
+            s = 0;
+            pass ^= 1u;
+          }
         }
       }
       // the copies of the last stages have landed before the CTA can exit
       // (immediate when the MMA thread consumed them; bounded otherwise)
-      for (int j = kb > kStages ? kb - kStages : 0; j < kb; ++j)
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
         mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int s = 0;
+      int s = 0, j = 0;
       uint32_t pass = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait(&full[s], pass)) break;
+      bool failed = false;
+      for (int t = blockIdx.x; t < tiles && !failed; t += gridDim.x, ++j) {
+        const int b = j & 1;
+        const uint32_t use = (uint32_t)(j >> 1);
+        // the epilogue has read this accumulator buffer out (its previous use)
+        if (use > 0 && !mbar_wait(&tempty[b], (use - 1u) & 1u)) break;
         tc_fence_after();
-        const uint32_t a_addr = smem_base + (uint32_t)s * kStageBytes;
-        const uint64_t adesc = umma_desc_sw128(a_addr);
-        const uint64_t bdesc = umma_desc_sw128(a_addr + kStageA);
+        const uint32_t d_tmem = tmem + (uint32_t)(b * kTmemCols);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait(&full[s], pass)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_base + (uint32_t)s * kStageBytes;
+          const uint64_t adesc = umma_desc_sw128(a_addr);
+          const uint64_t bdesc = umma_desc_sw128(a_addr + kStageA);
 #pragma unroll
-        for (int k = 0; k < kBK / 16; ++k)   // 16 bf16 = 32 bytes = 2 descriptor units along K
-          tc_mma(tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
-        tc_commit(empty_a + 8u * (uint32_t)s);
-        if (++s == kStages) {
-          s = 0;
-          pass ^= 1u;
+          for (int k = 0; k < kBK / 16; ++k)   // 16 bf16 = 32 bytes = 2 descriptor units along K
+            tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          tc_commit(empty_a + 8u * (uint32_t)s);
+          if (++s == kStages) {
+            s = 0;
+            pass ^= 1u;
+          }
         }
+        tc_commit(tfull_a + 8u * (uint32_t)b);
       }
-      tc_commit(accum_a);
     }
   } else {
     // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = rows of the tile
     const int quarter = warp & 3;
-    const bool ok = mbar_wait(accum, 0);
-    tc_fence_after();
-    const int row = m0 + 32 * quarter + lane;
-    const bool row_on = ok && row < g.M;
-    float* crow = g.C + (int64_t)row * g.ldc;
-    if (g.tma) {
-      // 32 x 32 boxes through two 4 KB staging buffers per warp (in the idle
-      // stage-0 ring memory), 128-byte swizzled to match the store's tensor
-      // map (conflict-free 16-byte writes); one thread stores or reduce-adds
-      // each box, and a buffer is rewritten only once its store has read it
-      const uint32_t stg = smem_base + (uint32_t)(warp - 2) * 8192u;
-      const int row0 = m0 + 32 * quarter;
+    const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
+    const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * 8192u;
+    int j = 0, boxes = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
+      const int m0 = (t % m_tiles) * kBM, n0 = (t / m_tiles) * kBN;
+      const int b = j & 1;
+      if (!mbar_wait(&tfull[b], (uint32_t)(j >> 1) & 1u)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + (uint32_t)(b * kTmemCols) + lane_off;
+      const int row = m0 + 32 * quarter + lane;
+      if (g.tma) {
+        // 32 x 32 boxes through two 4 KB staging buffers per warp, 128-byte
+        // swizzled to match the store's tensor map (conflict-free 16-byte
+        // writes); one thread stores or reduce-adds each box, and a buffer
+        // is rewritten only once its previous store has read it
+        const int row0 = m0 + 32 * quarter;
 #pragma unroll 1
-      for (int ci = 0; ci < kBN / 32; ++ci) {
-        uint32_t r[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(32 * ci), r);
-        tmem_ld_wait();
-        const uint32_t buf = stg + (uint32_t)(ci & 1) * 4096u;
-        if (ci >= 2) {
-          if (lane == 0) bulk_wait_read_1();
+        for (int ci = 0; ci < kBN / 32; ++ci, ++boxes) {
+          uint32_t r[32];
+          tmem_ld32(acc + (uint32_t)(32 * ci), r);
+          tmem_ld_wait();
+          const uint32_t buf = stg + (uint32_t)(boxes & 1) * 4096u;
+          if (boxes >= 2) {
+            if (lane == 0) bulk_wait_read_1();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            sts_f4(buf + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) * 16), g.alpha * __uint_as_float(r[4 * q]),
+                   g.alpha * __uint_as_float(r[4 * q + 1]), g.alpha * __uint_as_float(r[4 * q + 2]),
+                   g.alpha * __uint_as_float(r[4 * q + 3]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (row0 < g.M && n0 + 32 * ci < g.N) {
+              if (g.accumulate) tma_reduce_add_2d(&map_c, buf, n0 + 32 * ci, row0);
+              else tma_store_2d(&map_c, buf, n0 + 32 * ci, row0);
+            }
+            bulk_commit();
+          }
           __syncwarp();
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          sts_f4(buf + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) * 16), g.alpha * __uint_as_float(r[4 * q]),
-                 g.alpha * __uint_as_float(r[4 * q + 1]), g.alpha * __uint_as_float(r[4 * q + 2]),
-                 g.alpha * __uint_as_float(r[4 * q + 3]));
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (ok && row0 < g.M && n0 + 32 * ci < g.N) {
-            if (g.accumulate) tma_reduce_add_2d(&map_c, buf, n0 + 32 * ci, row0);
-            else tma_store_2d(&map_c, buf, n0 + 32 * ci, row0);
-          }
-          bulk_commit();
-        }
-        __syncwarp();
-      }
-      if (lane == 0) bulk_wait_all();
-    } else
-#pragma unroll 1
-    for (int c0 = 0; c0 < kBN; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)c0, r);
-      tmem_ld_wait();
-      const int col0 = n0 + c0;
-      if (!row_on || col0 >= g.N) continue;
-      if (g.vec && col0 + 32 <= g.N) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 v = make_float4(g.alpha * __uint_as_float(r[j]), g.alpha * __uint_as_float(r[j + 1]),
-                                 g.alpha * __uint_as_float(r[j + 2]), g.alpha * __uint_as_float(r[j + 3]));
-          float4* p = reinterpret_cast<float4*>(crow + col0 + j);
-          if (g.accumulate) {
-            const float4 o = *p;
-            v.x += o.x;
-            v.y += o.y;
-            v.z += o.z;
-            v.w += o.w;
-          }
-          *p = v;
-        }
       } else {
+        const bool row_on = row < g.M;
+        float* crow = g.C + (int64_t)row * g.ldc;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(acc + (uint32_t)c0, r);
+          tmem_ld_wait();
+          const int col0 = n0 + c0;
+          if (!row_on || col0 >= g.N) continue;
+          if (g.vec && col0 + 32 <= g.N) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (col0 + j < g.N) {
-            const float v = g.alpha * __uint_as_float(r[j]);
-            crow[col0 + j] = g.accumulate ? crow[col0 + j] + v : v;
+            for (int jj = 0; jj < 32; jj += 4) {
+              float4 v = make_float4(g.alpha * __uint_as_float(r[jj]), g.alpha * __uint_as_float(r[jj + 1]),
+                                     g.alpha * __uint_as_float(r[jj + 2]), g.alpha * __uint_as_float(r[jj + 3]));
+              float4* p = reinterpret_cast<float4*>(crow + col0 + jj);
+              if (g.accumulate) {
+                const float4 o = *p;
+                v.x += o.x;
+                v.y += o.y;
+                v.z += o.z;
+                v.w += o.w;
+              }
+              *p = v;
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              if (col0 + jj < g.N) {
+                const float v = g.alpha * __uint_as_float(r[jj]);
+                crow[col0 + jj] = g.accumulate ? crow[col0 + jj] + v : v;
+              }
+            }
           }
         }
       }
+      // this warp is done with accumulator buffer b
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(&tempty[b]);
     }
+    if (lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, 2 * kTmemCols);
   }
 }
 
@@ -325,7 +373,6 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
       (reinterpret_cast<uintptr_t>(B) % 16))
     return fail(SF_ERR_UNSUPPORTED, "A and B need 16-byte aligned bases and rows (lda, ldb multiples of 8)");
   if (!tensor_map_encoder()) return fail(SF_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available");
-  if ((M + kBM - 1) / kBM > 65535) return fail(SF_ERR_UNSUPPORTED, "M too large for one launch");
   CUtensorMap ma, mb;
   SF_TRY(make_map(&ma, A, M, K, lda, kBM));
   SF_TRY(make_map(&mb, B, N, K, ldb, kBN));
@@ -347,7 +394,9 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
                 "cudaFuncSetAttribute(k_tc_gemm)");
     configured = true;
   }
-  const dim3 grid((unsigned)((N + kBN - 1) / kBN), (unsigned)((M + kBM - 1) / kBM));
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  if (tiles > INT32_MAX) return fail(SF_ERR_UNSUPPORTED, "too many tiles");
+  const unsigned grid = (unsigned)std::min<int64_t>(tiles, sm_count());
   k_tc_gemm<<<grid, kGemmThreads, kGemmSmem, s>>>(ma, mb, mc, g);
   return check_launch("k_tc_gemm");
 }
