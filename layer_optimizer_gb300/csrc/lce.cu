@@ -31,18 +31,36 @@ namespace {
 constexpr int kLseThreads = 256;
 
 // out[c][r] = in[r][c] for a rows x cols bf16 matrix (row pitches ld_in,
-// ld_out), through a padded 64 x 64 tile.
+// ld_out; cols, ld_in and ld_out even), through a padded 64 x 64 tile held as
+// 32-bit words: coalesced 4-byte loads of column pairs, and each output word
+// (rows 2p and 2p + 1 of one column) assembled from two tile words.
 __global__ void __launch_bounds__(256) k_transpose_bf16(const uint16_t* __restrict__ in, int64_t rows,
                                                         int64_t cols, int64_t ld_in, uint16_t* __restrict__ out,
                                                         int64_t ld_out) {
-  __shared__ uint16_t tile[64][66];
+  __shared__ uint32_t tile[64][33];
   const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
-  for (int r = ty; r < 64; r += 4)
-    if (r0 + r < rows && c0 + tx < cols) tile[r][tx] = in[(r0 + r) * ld_in + c0 + tx];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int q = threadIdx.x + 256 * k;       // 64 rows x 32 words
+    const int r = q >> 5, w = q & 31;
+    const int64_t i = r0 + r, j = c0 + 2 * w;
+    uint32_t v = 0;
+    if (i < rows && j < cols) v = *reinterpret_cast<const uint32_t*>(in + i * ld_in + j);
+    tile[r][w] = v;
+  }
   __syncthreads();
-  for (int c = ty; c < 64; c += 4)
-    if (c0 + c < cols && r0 + tx < rows) out[(c0 + c) * ld_out + r0 + tx] = tile[tx][c];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int q = threadIdx.x + 256 * k;       // 64 output rows (columns c) x 32 words (row pairs p)
+    const int c = q >> 5, p = q & 31;
+    const int64_t j = c0 + c, i = r0 + 2 * p;
+    if (j < cols && i < rows) {
+      const uint32_t lo = tile[2 * p][c >> 1], hi = tile[2 * p + 1][c >> 1];
+      // the half of each word that holds column c (low half = even column)
+      const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+      *reinterpret_cast<uint32_t*>(out + j * ld_out + i) = __byte_perm(lo, hi, sel);
+    }
+  }
 }
 
 // Number n of labelled tokens (label != ignore and in [0, V)); a label that
@@ -119,32 +137,50 @@ __global__ void __launch_bounds__(kLseThreads) k_lce_lse(const float* __restrict
 }
 
 // The gradient tile: g = (exp(z - lse) - [j == y]) * inv_n (0 for an
-// unlabelled row), rounded to bf16, written to G [rows][V] and, through
-// shared memory, to Gt [V][ld_gt] (columns = rows of the chunk).
+// unlabelled row), rounded to bf16, written to G [rows][V] and Gt
+// [V][ld_gt] (columns = rows of the chunk).  Each thread takes column pairs
+// (8-byte loads of Z, 4-byte stores of G); the transposed copy goes through
+// a padded tile of 32-bit words like k_transpose_bf16.  V, ld_gt even.
 __global__ void __launch_bounds__(256) k_lce_grad(const float* __restrict__ Z, int64_t rows, int64_t V,
                                                   const float* __restrict__ lse, const int32_t* __restrict__ labels,
                                                   int32_t ignore, const float* __restrict__ inv_n,
                                                   __nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__ Gt,
                                                   int64_t ld_gt) {
-  __shared__ __nv_bfloat16 tile[64][66];
+  __shared__ uint32_t tile[64][33];
   const int64_t r0 = (int64_t)blockIdx.y * 64, j0 = (int64_t)blockIdx.x * 64;
-  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
   const float sc = *inv_n;
-  for (int r = ty; r < 64; r += 4) {
-    const int64_t i = r0 + r, j = j0 + tx;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int q = threadIdx.x + 256 * k;       // 64 rows x 32 column pairs
+    const int r = q >> 5, w = q & 31;
+    const int64_t i = r0 + r, j = j0 + 2 * w;
+    uint32_t word = 0;
     if (i < rows && j < V) {
       const int32_t y = labels[i];
-      float g = 0.0f;
-      if (labelled(y, ignore, V)) g = (expf(Z[i * V + j] - lse[i]) - (j == y ? 1.0f : 0.0f)) * sc;
-      const __nv_bfloat16 b = __float2bfloat16_rn(g);
-      G[i * V + j] = b;
-      tile[r][tx] = b;
+      float g0 = 0.0f, g1 = 0.0f;
+      if (labelled(y, ignore, V)) {
+        const float2 z = *reinterpret_cast<const float2*>(Z + i * V + j);
+        const float l = lse[i];
+        g0 = (expf(z.x - l) - (j == y ? 1.0f : 0.0f)) * sc;
+        g1 = (expf(z.y - l) - (j + 1 == y ? 1.0f : 0.0f)) * sc;
+      }
+      const __nv_bfloat162 h = __floats2bfloat162_rn(g0, g1);
+      word = *reinterpret_cast<const uint32_t*>(&h);
+      *reinterpret_cast<uint32_t*>(G + i * V + j) = word;
     }
+    tile[r][w] = word;
   }
   __syncthreads();
-  for (int c = ty; c < 64; c += 4) {
-    const int64_t j = j0 + c, i = r0 + tx;
-    if (j < V && i < rows) Gt[j * ld_gt + i] = tile[tx][c];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int q = threadIdx.x + 256 * k;       // 64 columns c x 32 row pairs p
+    const int c = q >> 5, p = q & 31;
+    const int64_t j = j0 + c, i = r0 + 2 * p;
+    if (j < V && i < rows) {
+      const uint32_t lo = tile[2 * p][c >> 1], hi = tile[2 * p + 1][c >> 1];
+      const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+      *reinterpret_cast<uint32_t*>(Gt + j * ld_gt + i) = __byte_perm(lo, hi, sel);
+    }
   }
 }
 

@@ -130,6 +130,7 @@ struct TcGemmArgs {
   int32_t accumulate;    // 1: C += alpha A B^T, 0: C = alpha A B^T
   int32_t vec;           // C rows 16-byte aligned (float4 epilogue)
   int32_t tma;           // C written by tensor stores (reduce-add when accumulating) from shared memory
+  int32_t n_fast;        // tile order: n fastest (A is the larger operand) or m fastest
 };
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -175,8 +176,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // tiles t = blockIdx.x, + gridDim.x, ...; m fastest, so the CTAs working
-  // at the same time share B tiles in L2
+  // tiles t = blockIdx.x, + gridDim.x, ...; the index runs fastest along the
+  // dimension whose operand is the smaller one, so the CTAs working at the
+  // same time share the tile of the larger operand and it streams from
+  // memory about once, while the smaller one is re-read from L2
   if (warp == 0) {
     if (lane == 0) {
       griddep_wait();
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t pass = 0;
       bool failed = false;
       for (int t = blockIdx.x; t < tiles && !failed; t += gridDim.x) {
-        const int m0 = (t % m_tiles) * kBM, n0 = (t / m_tiles) * kBN;
+        const int m0 = (g.n_fast ? t / n_tiles : t % m_tiles) * kBM, n0 = (g.n_fast ? t % n_tiles : t / m_tiles) * kBN;
         for (int kb = 0; kb < nk; ++kb) {
           if (issued >= kStages && !mbar_wait(&empty[s], pass ^ 1u)) {
             failed = true;
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * 8192u;
     int j = 0, boxes = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
-      const int m0 = (t % m_tiles) * kBM, n0 = (t / m_tiles) * kBN;
+      const int m0 = (g.n_fast ? t / n_tiles : t % m_tiles) * kBM, n0 = (g.n_fast ? t % n_tiles : t / m_tiles) * kBN;
       const int b = j & 1;
       if (!mbar_wait(&tfull[b], (uint32_t)(j >> 1) & 1u)) break;
       tc_fence_after();
@@ -386,6 +389,7 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
   g.accumulate = accumulate ? 1 : 0;
   g.vec = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0) ? 1 : 0;
   g.tma = g.vec;
+  g.n_fast = M > N ? 1 : 0;
   CUtensorMap mc = ma;       // unused unless g.tma
   if (g.tma) SF_TRY(make_map_c(&mc, C, M, N, ldc));
   static thread_local bool configured = false;
