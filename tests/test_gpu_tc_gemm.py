@@ -34,7 +34,9 @@ def _check(C, A64, B64, C0=None, alpha=1.0):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 1024), (200, 300, 136), (1000, 777, 520),
-                                   (64, 40, 8), (384, 1024, 4096)])
+                                   (64, 40, 8), (384, 1024, 4096), (1, 1, 8), (129, 257, 72),
+                                   (2000, 300, 64),      # more rows than columns: tiles taken n fastest
+                                   (300, 5000, 256)])    # more tiles than SMs: several tiles per CTA
 def test_gemm_matches_fp64(M, N, K):
     A, B = _inputs(M, N, K, M + N + K)
     C = torch.full((M, N), float("nan"), device=DEV)
