@@ -9,7 +9,9 @@
 // activation for big vocabularies) never exist in full.  For each chunk of
 // tokens c:
 //   Z_c  = H_c W^T                      tensor cores, fp32 [chunk][V]
-//   lse  = logsumexp over each row of Z_c, and the rows' losses
+//   lse  = logsumexp over each row of Z_c, from (max, sum exp) pairs the
+//          logits GEMM's epilogue writes per row and 256-column tile, and
+//          the rows' losses
 //   G_c  = (softmax(Z_c) - onehot(y_c)) / n  rounded to bf16, written both
 //          as [chunk][V] and transposed [V][chunk]
 //   dH_c = G_c W                        tensor cores (W^T made once per call)
@@ -27,8 +29,6 @@
 
 namespace sf {
 namespace {
-
-constexpr int kLseThreads = 256;
 
 // out[c][r] = in[r][c] for a rows x cols bf16 matrix (row pitches ld_in,
 // ld_out; cols, ld_in and ld_out even), through a padded 64 x 64 tile held as
@@ -94,45 +94,53 @@ __device__ __forceinline__ bool labelled(int32_t y, int32_t ignore, int64_t V) {
   return y != ignore && y >= 0 && y < V;
 }
 
-// One block per row of the chunk: lse = log sum_j exp(z_j), by a running
-// (max, sum) per thread over a fixed strided set of columns, then a fixed
-// tree; the row's loss lse - z[y] (0 for an unlabelled token).
-__global__ void __launch_bounds__(kLseThreads) k_lce_lse(const float* __restrict__ Z, int64_t V,
-                                                         const int32_t* __restrict__ labels, int32_t ignore,
-                                                         float* __restrict__ lse, float* __restrict__ row_loss) {
-  __shared__ float sm[kLseThreads], ss[kLseThreads];
-  const int64_t r = blockIdx.x;
-  const float* z = Z + r * V;
+// (m, s) pairs meaning "s = sum of exp(x - m)" combined into one.
+__device__ __forceinline__ void combine_stats(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  const float mn = fmaxf(m, m2);
+  s = s * expf(m - mn) + s2 * expf(m2 - mn);
+  m = mn;
+}
+
+// One warp per row of the chunk: lse = log sum_j exp(z_j) from the logits
+// GEMM's per-tile (max, sum of exp) pairs, combined in a fixed order (lanes
+// over tiles, then a butterfly); the row's loss lse - z[y] (0 for an
+// unlabelled token).
+__global__ void __launch_bounds__(256) k_lce_lse(const float2* __restrict__ stats, int n_tiles, int64_t rows,
+                                                 const float* __restrict__ Z, int64_t V,
+                                                 const int32_t* __restrict__ labels, int32_t ignore,
+                                                 float* __restrict__ lse, float* __restrict__ row_loss) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
   float m = -INFINITY, s = 0.0f;
-  for (int64_t j = threadIdx.x; j < V; j += kLseThreads) {
-    const float x = z[j];
-    if (x > m) {
-      s = s * expf(m - x) + 1.0f;
-      m = x;
+  for (int t = lane; t < n_tiles; t += 32) {
+    const float2 p = stats[r * n_tiles + t];
+    combine_stats(m, s, p.x, p.y);
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    // the same pair order on both lanes of the exchange: lower lane first
+    if (lane & o) {
+      float mm = m2, ss = s2;
+      combine_stats(mm, ss, m, s);
+      m = mm;
+      s = ss;
     } else {
-      s += expf(x - m);
+      combine_stats(m, s, m2, s2);
     }
   }
-  sm[threadIdx.x] = m;
-  ss[threadIdx.x] = s;
-  __syncthreads();
-  for (int st = kLseThreads / 2; st > 0; st >>= 1) {
-    if ((int)threadIdx.x < st) {
-      const float m1 = sm[threadIdx.x], m2 = sm[threadIdx.x + st];
-      const float s1 = ss[threadIdx.x], s2 = ss[threadIdx.x + st];
-      const float mm = fmaxf(m1, m2);
-      const float a = m1 == -INFINITY ? 0.0f : s1 * expf(m1 - mm);
-      const float b = m2 == -INFINITY ? 0.0f : s2 * expf(m2 - mm);
-      sm[threadIdx.x] = mm;
-      ss[threadIdx.x] = a + b;
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    const float l = sm[0] + logf(ss[0]);
+  if (lane == 0) {
+    const float l = m + logf(s);
     lse[r] = l;
     const int32_t y = labels[r];
-    row_loss[r] = labelled(y, ignore, V) ? l - z[y] : 0.0f;
+    row_loss[r] = labelled(y, ignore, V) ? l - Z[r * V + y] : 0.0f;
   }
 }
 
@@ -200,7 +208,7 @@ __global__ void __launch_bounds__(1024) k_lce_loss(const float* __restrict__ row
 }
 
 struct LcePlan {
-  size_t off_z, off_g, off_gt, off_wt, off_ht, off_lse, off_rowloss, off_n, bytes;
+  size_t off_z, off_g, off_gt, off_wt, off_ht, off_lse, off_rowloss, off_n, off_stats, bytes;
 };
 
 LcePlan plan_lce(int64_t N, int64_t D, int64_t V, int64_t chunk) {
@@ -219,6 +227,7 @@ LcePlan plan_lce(int64_t N, int64_t D, int64_t V, int64_t chunk) {
   p.off_lse = take((size_t)chunk * 4);
   p.off_rowloss = take((size_t)N * 4);
   p.off_n = take(16);
+  p.off_stats = take((size_t)chunk * ((V + kTcTileN - 1) / kTcTileN) * 8);
   p.bytes = off;
   return p;
 }
@@ -271,6 +280,8 @@ sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labe
   float* row_loss = reinterpret_cast<float*>(w + p.off_rowloss);
   int64_t* n_valid = reinterpret_cast<int64_t*>(w + p.off_n);
   float* inv_n = reinterpret_cast<float*>(w + p.off_n + 8);
+  float2* stats = reinterpret_cast<float2*>(w + p.off_stats);
+  const int n_vt = (int)((V + sf::kTcTileN - 1) / sf::kTcTileN);
   const uint16_t* Hb = static_cast<const uint16_t*>(H);
   const bool grads = dH || dW;
 
@@ -283,8 +294,9 @@ sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labe
   }
   for (int64_t c0 = 0; c0 < N; c0 += chunk) {
     const int64_t rows = std::min(chunk, N - c0);
-    SF_TRY(sf::tc_gemm_abt(Hb + c0 * D, W, Z, rows, V, D, D, D, V, 1.0f, false, s));
-    sf::k_lce_lse<<<(unsigned)rows, sf::kLseThreads, 0, s>>>(Z, V, labels + c0, ignore_index, lse, row_loss + c0);
+    SF_TRY(sf::tc_gemm_abt(Hb + c0 * D, W, Z, rows, V, D, D, D, V, 1.0f, false, s, stats));
+    sf::k_lce_lse<<<(unsigned)sf::ceil_div<int64_t>(rows, 8), 256, 0, s>>>(stats, n_vt, rows, Z, V, labels + c0,
+                                                                             ignore_index, lse, row_loss + c0);
     SF_TRY(sf::check_launch("k_lce_lse"));
     if (!grads) continue;
     sf::k_lce_grad<<<dim3((unsigned)sf::ceil_div<int64_t>(V, 64), (unsigned)sf::ceil_div<int64_t>(rows, 64)), 256, 0, s>>>(

@@ -131,7 +131,25 @@ struct TcGemmArgs {
   int32_t vec;           // C rows 16-byte aligned (float4 epilogue)
   int32_t tma;           // C written by tensor stores (reduce-add when accumulating) from shared memory
   int32_t n_fast;        // tile order: n fastest (A is the larger operand) or m fastest
+  float2* row_stats;     // optional [M][n_tiles]: per row and column tile, (max, sum exp(c - max)) of C
 };
+
+// Folds 32 values of a row into a running (max, sum of exp(x - max)):
+// the chunk's maximum first, then one rescale of the running sum.
+__device__ __forceinline__ void fold_row_stats(const float (&x)[32], int valid, float& m, float& s) {
+  float cm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < valid) cm = fmaxf(cm, x[j]);
+  if (cm == -INFINITY) return;
+  const float mn = fmaxf(m, cm);
+  float acc = m == -INFINITY ? 0.0f : s * expf(m - mn);
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (j < valid) acc += expf(x[j] - mn);
+  m = mn;
+  s = acc;
+}
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_tc_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -261,11 +279,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // writes); one thread stores or reduce-adds each box, and a buffer
         // is rewritten only once its previous store has read it
         const int row0 = m0 + 32 * quarter;
+        float rm = -INFINITY, rs = 0.0f;
 #pragma unroll 1
         for (int ci = 0; ci < kBN / 32; ++ci, ++boxes) {
           uint32_t r[32];
           tmem_ld32(acc + (uint32_t)(32 * ci), r);
           tmem_ld_wait();
+          if (g.row_stats) {
+            float x[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) x[jj] = g.alpha * __uint_as_float(r[jj]);
+            fold_row_stats(x, min(32, g.N - (n0 + 32 * ci)), rm, rs);
+          }
           const uint32_t buf = stg + (uint32_t)(boxes & 1) * 4096u;
           if (boxes >= 2) {
             if (lane == 0) bulk_wait_read_1();
@@ -287,15 +312,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           __syncwarp();
         }
+        if (g.row_stats && row < g.M) g.row_stats[(int64_t)row * n_tiles + n0 / kBN] = make_float2(rm, rs);
       } else {
         const bool row_on = row < g.M;
         float* crow = g.C + (int64_t)row * g.ldc;
+        float rm = -INFINITY, rs = 0.0f;
 #pragma unroll 1
         for (int c0 = 0; c0 < kBN; c0 += 32) {
           uint32_t r[32];
           tmem_ld32(acc + (uint32_t)c0, r);
           tmem_ld_wait();
           const int col0 = n0 + c0;
+          if (g.row_stats) {
+            float x[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) x[jj] = g.alpha * __uint_as_float(r[jj]);
+            fold_row_stats(x, min(32, g.N - col0), rm, rs);
+          }
           if (!row_on || col0 >= g.N) continue;
           if (g.vec && col0 + 32 <= g.N) {
 #pragma unroll
@@ -322,6 +355,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
+        if (g.row_stats && row_on) g.row_stats[(int64_t)row * n_tiles + n0 / kBN] = make_float2(rm, rs);
       }
       // this warp is done with accumulator buffer b
       tc_fence_before();
@@ -366,7 +400,7 @@ sf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, 
 
 // C = alpha A B^T (+ C); shared with the cross-entropy unit.
 sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                      int64_t ldb, int64_t ldc, float alpha, bool accumulate, cudaStream_t s) {
+                      int64_t ldb, int64_t ldc, float alpha, bool accumulate, cudaStream_t s, float2* row_stats) {
   if (!A || !B || !C) return fail(SF_ERR_INVALID, "A, B or C is NULL");
   if (M < 1 || N < 1 || K < 1) return fail(SF_ERR_INVALID, "M, N, K must be >= 1");
   if (M > INT32_MAX - kBM || N > INT32_MAX - kBN || K > INT32_MAX - kBK)
@@ -390,6 +424,7 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
   g.vec = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0) ? 1 : 0;
   g.tma = g.vec;
   g.n_fast = M > N ? 1 : 0;
+  g.row_stats = row_stats;
   CUtensorMap mc = ma;       // unused unless g.tma
   if (g.tma) SF_TRY(make_map_c(&mc, C, M, N, ldc));
   static thread_local bool configured = false;
