@@ -601,8 +601,12 @@ def run_lsp(args, matrices=None):
     return out
 
 
-def run_lce(args, N=8192, D=4096, V=128256, chunk=2048):
-    """Fused linear cross-entropy (loss, dH, dW) on a Llama-3.1-8B output layer."""
+def run_lce(args, N=8192, D=4096, V=128256, chunk=2432):
+    """Fused linear cross-entropy (loss, dH, dW) on a Llama-3.1-8B output layer.
+
+    Chunks of 2432 tokens = 19 tiles of 128 rows: the dH product (19 x 16 tiles)
+    then fills the 152 SMs in exactly two waves.
+    """
     import torch
 
     from layer_optimizer_gb300 import native, synth
