@@ -453,6 +453,14 @@ const char* sf_version(void);
  * thread-safe; meant for tests only. */
 void sf_test_fail_copy_after(int64_t n);
 
+/* Test hook for the kernels' bounded waits: launches one warp that waits on
+ * an mbarrier nothing arrives on, with a limit of limit_cycles SM clock
+ * cycles (1 .. 4e9; the library's own waits use ~4e9, about 2 s).  The wait
+ * runs out, records the timeout in the device error word and the kernel
+ * returns, so the next sf_sync_status() returns SF_ERR_TIMEOUT and clears
+ * it; the context stays usable.  SF_ERR_INVALID for a limit out of range. */
+sf_status sf_test_device_wait_runs_out(int64_t limit_cycles, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -487,6 +487,17 @@ sf_status adamw_compressed_impl(const float* S, float* m, float* v, float* dS, i
   return SF_OK;
 }
 
+// A wait on an mbarrier that nothing arrives on, bounded by `limit` cycles:
+// runs out, records kDevErrTimeout and returns (the path every bounded wait
+// in the library takes when its copies never land).
+__global__ void k_test_wait_runs_out(long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init_cluster();
+  mbar_wait_limit(&bar, 0, limit);
+}
+
 int read_and_clear_device_error_adamw() {
   int v = 0, z = 0;
   if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return 0;
@@ -510,6 +521,14 @@ sf_status lsp_adamw_compressed(const float* S, float* m, float* v, float* dS, in
   sf::clear_error();
   sf::NvtxRange nvtx_range("lsp_adamw_compressed");
   return sf::adamw_compressed_impl(S, m, v, dS, d2, hp, step, sf::as_stream(stream));
+}
+
+sf_status sf_test_device_wait_runs_out(int64_t limit_cycles, void* stream) {
+  sf::clear_error();
+  if (limit_cycles < 1 || limit_cycles > 4000000000LL)
+    return sf::fail(SF_ERR_INVALID, "limit_cycles must be in [1, 4e9]");
+  sf::k_test_wait_runs_out<<<1, 32, 0, sf::as_stream(stream)>>>((long long)limit_cycles);
+  return sf::check_launch("k_test_wait_runs_out");
 }
 
 }  // extern "C"

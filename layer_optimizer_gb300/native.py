@@ -27,7 +27,7 @@ EXPORTS = [
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
     "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
-    "sf_gemm_abt_bf16", "lce_workspace_bytes", "lce_forward_backward",
+    "sf_gemm_abt_bf16", "lce_workspace_bytes", "lce_forward_backward", "sf_test_device_wait_runs_out",
 ]
 
 
@@ -103,6 +103,7 @@ _SIGS = {
     "lsp_projector_export_values": (_ST, [_P, _P, _P]),
     "sf_gemm_abt_bf16": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _INT, _P]),
     "lce_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
+    "sf_test_device_wait_runs_out": (_ST, [_I64, _P]),
     "lce_forward_backward": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I64, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P]),
 }
 
@@ -402,6 +403,10 @@ def sf_last_error():
 
 def sf_version():
     return load().sf_version().decode()
+
+
+def sf_test_device_wait_runs_out(limit_cycles, stream=None):
+    _check(load().sf_test_device_wait_runs_out(limit_cycles, _stream(stream)))
 
 
 def sf_test_fail_copy_after(n):

@@ -163,6 +163,27 @@ def test_bounded_wait_times_out_then_recovers():
     win.close()
 
 
+def test_device_wait_runs_out_sets_timeout_and_context_stays_usable():
+    # a kernel whose mbarrier wait nothing completes: the bounded wait runs
+    # out (~0.1 ms here), records the timeout, and the kernel returns
+    native.sf_test_device_wait_runs_out(200_000)
+    torch.cuda.synchronize()
+    with pytest.raises(native.SfError) as e:
+        native.sf_sync_status()
+    assert e.value.status == native.SF_ERR_TIMEOUT and "ran out" in str(e.value)
+    native.sf_sync_status()                       # the word was cleared
+    # the context still works: an AdamW step runs and checks out
+    n = 4096
+    g = torch.full((n,), 1e-3, dtype=torch.bfloat16, device="cuda")
+    p, m, v = torch.ones(n, device="cuda"), torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda")
+    native.sf_adamw_layer_step([native.make_tensor(g, p, m, v, None, n)], native.hparams(**HP), 1)
+    torch.cuda.synchronize()
+    native.sf_sync_status()
+    assert torch.all(p < 1.0)
+    with pytest.raises(native.SfError, match="limit_cycles"):
+        native.sf_test_device_wait_runs_out(0)
+
+
 def test_invalid_visits_rejected_before_enqueue():
     layers = [_host_layer([100], 99)]
     streams = [torch.cuda.Stream() for _ in range(3)]
