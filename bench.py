@@ -231,6 +231,45 @@ def oracle_params_per_s(budget_s=12.0, chunk=1 << 21, max_steps=None):
     return done / el, done, el
 
 
+def oracle_lsp_chain_rate(m=4096, n=4096, d=512, k=8):
+    """fp64 oracle compress + compressed AdamW + decompress-apply on one LLaMA-7B q matrix (params/s)."""
+    import numpy as np
+
+    from layer_optimizer_gb300 import synth
+    from oracle import adamw as oa
+    from oracle import lsp as ol
+    P = ol.Projector(*synth.projector(m, d, k, 1), d)
+    Q = ol.Projector(*synth.projector(n, d, k, 2), d)
+    rng = np.random.default_rng(3)
+    G = rng.normal(0.0, 1e-3, size=(m, n))
+    W = rng.normal(0.0, 0.02, size=(m, n))
+    t0 = time.perf_counter()
+    S, _ = ol.compress(P, Q, G)
+    dS, *_ = oa.compressed_adamw_step(S, np.zeros((d, d)), np.zeros((d, d)), 1, HP["lr"], HP["beta1"],
+                                      HP["beta2"], HP["eps"])
+    D, _ = ol.decompress(P, Q, dS)
+    ol.apply_fp32(W, D)
+    el = time.perf_counter() - t0
+    return {"params_per_s": m * n / el, "s": el,
+            "sample": f"one {m} x {n} matrix, d {d}, k {k}: fp64 numpy (dense projector products)"}
+
+
+def oracle_lce_rate(N=64, D=4096, V=128256):
+    """fp64 oracle linear cross-entropy (loss, dH, dW) on a sample of tokens (tokens/s)."""
+    import numpy as np
+
+    from oracle.lce import lce
+    rng = np.random.default_rng(4)
+    H = rng.standard_normal((N, D), dtype=np.float32)
+    W = rng.standard_normal((V, D), dtype=np.float32) * np.float32(0.02)
+    y = rng.integers(0, V, size=N)
+    t0 = time.perf_counter()
+    lce(H, W, y)
+    el = time.perf_counter() - t0
+    return {"tokens_per_s": N / el, "s": el,
+            "sample": f"{N} tokens of the same output layer (D {D}, V {V}): fp64 numpy, BLAS threads as installed"}
+
+
 # ------------------------------------------------------------------ ours ---
 
 def make_groups(groups, seed=0):
@@ -881,6 +920,11 @@ def main_ours(args, rank, world):
             line["lce"] = {"error": str(ex)[:300]}
     if not args.no_cpu and rank == 0 and args.workload == "opt-1.3b":
         line["host_update"] = host_update_rate()
+        # the oracle beside the other two workloads (bounded samples)
+        if isinstance(line.get("lsp"), dict) and "error" not in line["lsp"]:
+            line["lsp"]["cpu_oracle"] = oracle_lsp_chain_rate()
+        if isinstance(line.get("lce"), dict) and "error" not in line["lce"]:
+            line["lce"]["cpu_oracle"] = oracle_lce_rate()
     if not args.no_cpu and rank == 0:
         v, done, el = oracle_params_per_s()
         line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
