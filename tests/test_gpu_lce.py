@@ -115,3 +115,41 @@ def test_lce_rejects_and_flags():
                                 ws.numel())
     with pytest.raises(native.SfError, match="out-of-range"):
         native.sf_sync_status()
+
+
+@pytest.mark.slow
+def test_lce_llama31_head_full_size_sampled():
+    # the benchmark's configuration: 8192 tokens of a Llama-3.1-8B output
+    # layer in chunks of 2432; rows of dH checked against the oracle one by
+    # one, and dW through a property that holds at any size: every row of
+    # dZ sums to zero, so the sum of dW over the vocabulary is zero
+    N, D, V, chunk = 8192, 4096, 128256, 2432
+    H = synth.fill_normal_(torch.empty(N, D, dtype=torch.bfloat16, device=DEV), 1.0, synth.sub_seed(31, 0))
+    W = synth.fill_normal_(torch.empty(V, D, dtype=torch.bfloat16, device=DEV), 0.02, synth.sub_seed(31, 1))
+    g = torch.Generator(device=DEV)
+    g.manual_seed(synth.sub_seed(31, 2))
+    y = torch.randint(0, V, (N,), generator=g, device=DEV, dtype=torch.int32)
+    y[::97] = -100
+    loss, dH, dW = _run(H, W, y, chunk)
+    n = int((y != -100).sum())
+    rows = [0, 1, 97, 2431, 2432, 5000, N - 1]
+    W64 = f64(W)
+    Hs = f64(H[rows])
+    Z = Hs @ W64.T
+    Z -= Z.max(axis=1, keepdims=True)
+    Pr = np.exp(Z)
+    Pr /= Pr.sum(axis=1, keepdims=True)
+    ys = y[rows].cpu().numpy()
+    dZ = np.where((ys != -100)[:, None], Pr, 0.0)
+    for r, yy in enumerate(ys):
+        if yy != -100:
+            dZ[r, yy] -= 1.0
+    dZ /= n
+    ref, mag = dZ @ W64, np.abs(dZ) @ np.abs(W64)
+    err = np.abs(f64(dH[rows]) - ref)
+    assert not (err > TOL_GRAD * mag + 1e-30).any(), float((err / (mag + 1e-30)).max())
+    assert not dH[97].any()                               # an unlabelled token has no gradient
+    colsum = dW.double().sum(dim=0)
+    bound = TOL_GRAD * (2.0 / n) * H.double().abs().sum(dim=0) + 1e-12
+    assert bool((colsum.abs() <= bound).all()), float((colsum.abs() / bound).max())
+    assert 0.0 < loss < 2 * np.log(V)
