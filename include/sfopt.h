@@ -109,6 +109,10 @@ typedef struct {
  * SF_MAX_TENSORS_PER_LAUNCH tensors.  Empty tensors (numel 0) are allowed.
  * Returns SF_ERR_INVALID for n_tensors < 0, a NULL array, a negative numel,
  * step < 1, or non-finite hyper-parameters.
+ * The arrays may also be in pinned host memory (cudaHostAlloc / registered):
+ * they are then updated in place over the host link by zero-copy loads and
+ * stores (same arithmetic and bits; on GB300 about half the rate of the
+ * copy-engine window, sf_slide_window_step).
  * ---------------------------------------------------------------------- */
 #define SF_MAX_TENSORS_PER_LAUNCH 48
 

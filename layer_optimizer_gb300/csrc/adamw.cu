@@ -393,6 +393,18 @@ sf_status adamw_layer_step_impl(const sf_tensor* tensors, int n_tensors, const s
     if (tensors[i].numel < 0) return fail(SF_ERR_INVALID, "tensor %d: numel < 0", i);
 
   static_assert(sizeof(LaunchArgs) <= 4096, "kernel parameter block too large");
+  // Arrays in pinned host memory are updated in place over the host link
+  // (zero-copy loads and stores from the register-staged kernel; the bulk
+  // kernel's shared-memory copies are kept for device memory).
+  bool host_resident = false;
+  for (int i = 0; i < n_tensors && !host_resident; ++i) {
+    if (tensors[i].numel == 0) continue;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, tensors[i].master) == cudaSuccess && a.type == cudaMemoryTypeHost)
+      host_resident = true;
+    else
+      cudaGetLastError();
+  }
   LaunchArgs L;
   const int grid_cap = sm_count() * blocks_per_sm();
   int i = 0;
@@ -416,7 +428,7 @@ sf_status adamw_layer_step_impl(const sf_tensor* tensors, int n_tensors, const s
     int64_t vec_elems = 0;
     for (int t = 0; t < L.nt; ++t)
       if (L.t[t].vector_mode) vec_elems += L.t[t].nvec * kUnitElems;
-    L.skip_vector = vec_elems >= kBulkMinElems ? 1 : 0;
+    L.skip_vector = !host_resident && vec_elems >= kBulkMinElems ? 1 : 0;
     if (L.skip_vector) {
       BulkArgs B;
       B.c = c;

@@ -244,3 +244,28 @@ def test_host_step_bitwise_equals_device_step():
         for k in (1, 2, 3):
             assert torch.equal(d_[k].cpu().view(torch.int32), h_[k].view(torch.int32))
         assert torch.equal(d_[4].cpu().view(torch.int16), h_[4].view(torch.int16))
+
+
+def test_pinned_host_arrays_updated_in_place_bitwise_equal_to_device():
+    # arrays in pinned host memory are updated over the host link by the
+    # same arithmetic (zero-copy loads and stores); large enough that device
+    # arrays of the same sizes take the bulk-copy kernel
+    sizes = [(1 << 20) + 8, 3000, 1 << 19]
+    hp = native.hparams(**HP)
+    dev, host = [], []
+    for i, n in enumerate(sizes):
+        g = synth.normal((n,), 1e-3, synth.sub_seed(40, i), dtype=torch.bfloat16)
+        p = synth.normal((n,), 0.02, synth.sub_seed(41, i))
+        dev.append([g.cuda(), p.cuda(), torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda"),
+                    torch.empty(n, dtype=torch.bfloat16, device="cuda")])
+        host.append([g.pin_memory(), p.pin_memory(), torch.zeros(n).pin_memory(), torch.zeros(n).pin_memory(),
+                     torch.empty(n, dtype=torch.bfloat16).pin_memory()])
+    for step in (1, 2):
+        native.sf_adamw_layer_step([native.make_tensor(*t) for t in dev], hp, step)
+        native.sf_adamw_layer_step([native.make_tensor(*t) for t in host], hp, step)
+    torch.cuda.synchronize()
+    native.sf_sync_status()
+    for d, h in zip(dev, host):
+        for a, b in zip(d[1:4], h[1:4]):
+            assert torch.equal(a.cpu().view(torch.int32), b.view(torch.int32))
+        assert torch.equal(d[4].cpu().view(torch.int16), h[4].view(torch.int16))
