@@ -461,12 +461,7 @@ sf_status adamw_layer_step_impl(const sf_tensor* tensors, int n_tensors, const s
       B.total_chunks = (int32_t)chunks;
       static_assert(sizeof(BulkArgs) <= 4096, "kernel parameter block too large");
       const size_t smem = (size_t)kBulkStages * kBulkStageBytes + 2 * kBulkStages * 8 + 8;
-      static thread_local bool configured = false;
-      if (!configured) {
-        SF_CUDA_TRY(cudaFuncSetAttribute(adamw_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem),
-                    "cudaFuncSetAttribute(adamw_bulk_kernel)");
-        configured = true;
-      }
+      SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&adamw_bulk_kernel), smem));
       if (B.nt > 0) {
         const int grid = (int)std::min<int64_t>(chunks, sm_count());
         SF_CUDA_TRY(launch_pdl(adamw_bulk_kernel, dim3(grid), dim3(32 * (kBulkConsumerWarps + 1)), smem, stream, B),

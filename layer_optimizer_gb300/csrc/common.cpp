@@ -1,6 +1,10 @@
 // Status plumbing, bounded host waits and AdamW constant derivation.
 #include "common.h"
 
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include <chrono>
 #include <cmath>
 #include <cstdlib>
@@ -99,6 +103,21 @@ sf_status make_adam_consts(const sf_adamw_hparams* hp, int64_t step, bool with_d
   out->sqrt_bc2 = static_cast<float>(std::sqrt(bc2));
   out->inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
   out->eps = static_cast<float>(hp->eps);
+  return SF_OK;
+}
+
+sf_status allow_dynamic_smem(const void* func, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = done[{dev, func}];
+  if (have >= bytes) return SF_OK;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+  have = bytes;
   return SF_OK;
 }
 

@@ -42,6 +42,11 @@ constexpr T ceil_div(T a, T b) { return (a + b - 1) / b; }
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// Lets kernel `func` use up to `bytes` of dynamic shared memory on the
+// current device (cudaFuncSetAttribute once per device, kernel and size;
+// thread-safe).
+sf_status allow_dynamic_smem(const void* func, size_t bytes);
+
 // cuTensorMapEncodeTiled from the driver (looked up once), or null.
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {

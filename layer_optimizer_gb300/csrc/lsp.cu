@@ -1191,13 +1191,7 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
 
   const size_t smem = (size_t)A.stages * A.stage_stride + 2 * kMaxStages * sizeof(uint64_t) + kMaxStages * 4 + 8 + 1024;
-  static thread_local size_t configured[2] = {0, 0};
-  const int slot = es == 4 ? 0 : 1;
-  if (configured[slot] < smem) {
-    SF_CUDA_TRY(cudaFuncSetAttribute(k_gather_t<TB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxGatherSmem),
-                "cudaFuncSetAttribute(k_gather_t)");
-    configured[slot] = smem;
-  }
+  SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&k_gather_t<TB>), kMaxGatherSmem));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_cb, (unsigned)p.n_ar, (unsigned)p.splits);
   cfg.blockDim = dim3(32 * (p.warps + 1));
@@ -1518,13 +1512,7 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
     const int64_t gy_used = ceil_div<int64_t>(n, cols_per_cta);
     if (Q->k <= sf::kVMaxK) {
       const size_t smem_v = sf::v_smem_bytes(d);
-      static thread_local bool v_cfg = false;
-      if (!v_cfg) {
-        SF_CUDA_TRY(cudaFuncSetAttribute(sf::k_v, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sf::v_smem_bytes(sf::kMaxFastD)),
-                    "cudaFuncSetAttribute(k_v)");
-        v_cfg = true;
-      }
+      SF_TRY(sf::allow_dynamic_smem(reinterpret_cast<const void*>(&sf::k_v), sf::v_smem_bytes(sf::kMaxFastD)));
       SF_CUDA_TRY(sf::launch_pdl(sf::k_v, dim3((unsigned)n_ab, (unsigned)gy_used), dim3(32 * sf::kVWarps), smem_v, s,
                                  dS, d, Q->ell_idx, Q->ell_val, Q->k, n, V, cols_per_cta),
                   "launch k_v");
@@ -1539,13 +1527,8 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
     const int64_t total = n_jb * m;
     const bool bf16w = w_dtype == SF_BF16;
     auto kern = bf16w ? sf::k_apply<true> : sf::k_apply<false>;
-    static thread_local bool a_cfg[2] = {false, false};
-    if (!a_cfg[bf16w]) {
-      SF_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)((size_t)sf::kMaxFastD * sf::kApplyCols * 4 + 16 * 32 * 8)),
-                  "cudaFuncSetAttribute(k_apply)");
-      a_cfg[bf16w] = true;
-    }
+    SF_TRY(sf::allow_dynamic_smem(reinterpret_cast<const void*>(kern),
+                                  (size_t)sf::kMaxFastD * sf::kApplyCols * 4 + 16 * 32 * 8));
     int occ = 1;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 512, smem_a);
     occ = std::max(1, occ);
@@ -1591,12 +1574,7 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
                                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
         if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled(W) failed (%d)", (int)r);
         auto kt = bf16w ? sf::k_apply_tma<true> : sf::k_apply_tma<false>;
-        static thread_local bool t_cfg[2] = {false, false};
-        if (!t_cfg[bf16w]) {
-          SF_CUDA_TRY(cudaFuncSetAttribute(kt, cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024),
-                      "cudaFuncSetAttribute(k_apply_tma)");
-          t_cfg[bf16w] = true;
-        }
+        SF_TRY(sf::allow_dynamic_smem(reinterpret_cast<const void*>(kt), 220 * 1024));
         SF_CUDA_TRY(sf::launch_pdl(kt, dim3((unsigned)ceil_div<int64_t>(A.total, A.per_cta)),
                                    dim3(32 * (sf::kApplyConsumerWarps + 1)), smem2, s, wmap, A),
                     "launch k_apply_tma");

@@ -427,12 +427,7 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
   g.row_stats = row_stats;
   CUtensorMap mc = ma;       // unused unless g.tma
   if (g.tma) SF_TRY(make_map_c(&mc, C, M, N, ldc));
-  static thread_local bool configured = false;
-  if (!configured) {
-    SF_CUDA_TRY(cudaFuncSetAttribute(k_tc_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem),
-                "cudaFuncSetAttribute(k_tc_gemm)");
-    configured = true;
-  }
+  SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&k_tc_gemm), kGemmSmem));
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   if (tiles > INT32_MAX) return fail(SF_ERR_UNSUPPORTED, "too many tiles");
   const unsigned grid = (unsigned)std::min<int64_t>(tiles, sm_count());
