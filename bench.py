@@ -640,11 +640,12 @@ def run_lsp(args, matrices=None):
     return out
 
 
-def run_lce(args, N=8192, D=4096, V=128256, chunk=2432):
+def run_lce(args, N=8192, D=4096, V=128256, chunk=4608):
     """Fused linear cross-entropy (loss, dH, dW) on a Llama-3.1-8B output layer.
 
-    Chunks of 2432 tokens = 19 tiles of 128 rows: the dH product (19 x 16 tiles)
-    then fills the 152 SMs in exactly two waves.
+    Chunks of 4608 tokens = 18 tiles of 256 rows (one per CTA pair): the dH
+    product's 18 x 16 tiles take 3.8 of the 4 waves of 76 CTA pairs, the
+    3584-token remainder's 14 x 16 tiles 2.95 of 3.
     """
     import torch
 

@@ -3,28 +3,38 @@
 //
 // The dense products of the fused linear cross-entropy (logits, and the two
 // gradient products) are real dense contractions, so they run here rather
-// than on CUDA cores.  A persistent grid (one CTA per SM) walks the 128 x 256
-// tiles of C; in each CTA:
-//   warp 0       TMA producer: 64-wide K slabs of A (128 x 64) and B
-//                (256 x 64) into a 4-stage shared-memory ring, 128-byte
-//                swizzled, completion on an mbarrier per stage;
-//   warp 1       allocates 512 TMEM columns (two 128 x 256 fp32
-//                accumulators) and one elected thread issues tcgen05.mma
-//                (M 128, N 256, K 16, bf16 in, fp32 accumulate), four per
-//                slab, into the accumulator the epilogue has released;
-//                tcgen05.commit frees a stage when its MMAs are done and,
-//                after a tile's last slab, hands the accumulator over;
+// than on CUDA cores.  Pairs of CTAs (a cluster of two, one per SM of a
+// TPC) walk the 256 x 256 tiles of C in a persistent grid, and each pair
+// computes its tile with the pair form of the MMA (cta_group::2, M 256):
+// every CTA holds 128 rows of A and 128 rows of B per K slab, the MMA reads
+// both halves across the pair, and each CTA's TMEM receives its 128 rows of
+// the 256 x 256 accumulator.  Per SM that is half the B tile in shared
+// memory and half its shared-memory read traffic, compared with one CTA
+// computing 128 x 256 alone, which leaves room for a 6-deep ring.  In each
+// CTA:
+//   warp 0       TMA producer: 64-wide K slabs of its A rows (128 x 64) and
+//                B rows (128 x 64) into a 6-stage ring, 128-byte swizzled;
+//                both CTAs' copies complete on the first CTA's stage barrier;
+//   warp 1       allocates 512 TMEM columns with its peer (two accumulators
+//                of 256 fp32 columns); in the first CTA one elected thread
+//                issues tcgen05.mma (M 256, N 256, K 16, bf16 in, fp32
+//                accumulate), four per slab, into the accumulator both
+//                epilogues have released; tcgen05.commit frees a stage in
+//                both CTAs when its MMAs are done and, after a tile's last
+//                slab, hands the accumulator to both epilogues;
 //   warps 2..5   epilogue: each reads its 32 TMEM lanes (rows) with
 //                tcgen05.ld and writes (or reduce-adds into) C by tensor
 //                stores from shared memory, while the next tile's MMAs run
 //                into the other accumulator.
 // Every wait is bounded: a wait that runs out records an error for
-// sf_sync_status, and the CTA still releases its TMEM before it exits.
+// sf_sync_status, and the CTAs still release their TMEM before they exit.
 // Sums over K run in slab order on the tensor cores; results are
 // deterministic for a given shape.
 #include <cuda_bf16.h>
 
 #include <algorithm>
+#include <map>
+#include <mutex>
 
 #include "common.h"
 #include "ptx.cuh"
@@ -32,9 +42,11 @@
 namespace sf {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 4;
+constexpr int kPair = 2;                       // CTAs per tile (cta_group::2)
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 6;
+constexpr int kBRows = kBN / kPair;            // rows of B held by one CTA
 constexpr int kStageA = kBM * kBK * 2;         // 16 KB
-constexpr int kStageB = kBN * kBK * 2;         // 32 KB
+constexpr int kStageB = kBRows * kBK * 2;      // 16 KB
 constexpr int kStageBytes = kStageA + kStageB;
 constexpr int kTmemCols = 256;                 // one accumulator; two are allocated
 constexpr int kGemmThreads = 192;
@@ -43,9 +55,10 @@ constexpr size_t kGemmSmem = (size_t)kStages * kStageBytes + kStagingBytes + 102
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator
 // (bits 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), both K-major
-// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M = 256:
+// the pair's rows).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
-                            ((uint32_t)(kBM >> 4) << 24);
+                            ((uint32_t)((kPair * kBM) >> 4) << 24);
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes (64 bf16 of K), 8-row atoms of
@@ -59,33 +72,90 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// TMEM allocation of the CTA pair: one warp of each CTA issues these
+// together (the pair form requires both).
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
                : "memory");
 }
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A B^T for one K-16 step; accumulate = 0 overwrites D.
+// D[tmem] (+)= A B^T for one K-16 step over the pair (M 256: A rows from
+// both CTAs' shared memory at the descriptor's offset, B likewise, D rows
+// 0-127 into this CTA's TMEM and 128-255 into the peer's); accumulate = 0
+// overwrites D.
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                        uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-// Arrive on `mbar` once every tcgen05.mma issued so far by this thread is done.
-__device__ __forceinline__ void tc_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar)
-               : "memory");
+// Arrive on the barrier at shared offset `mbar` in both CTAs of the pair
+// once every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void tc_commit_pair(uint32_t mbar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          mbar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+
+// 2D tiled TMA load into this CTA's shared memory whose completion is
+// counted on the barrier at shared::cluster address `bar` (the pair form
+// lets it be the first CTA's barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+// Arrival on a barrier of another CTA of the cluster, ordering this
+// thread's earlier accesses (TMEM reads included, after
+// tcgen05.fence::before_thread_sync) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+}
+
+// Bounded wait with cluster-scope acquire (arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+  auto test = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (test()) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (test()) return true;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      atomicOr(&g_device_error, kDevErrTimeout);
+      return false;
+    }
+  }
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -156,19 +226,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               const __grid_constant__ CUtensorMap map_c, const TcGemmArgs g) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  // [ring: kStages x (A 16 KB + B 32 KB)] [epilogue staging: 4 warps x 2 x 4 KB] [barriers]
+  // [ring: kStages x (A 16 KB + B 16 KB)] [epilogue staging: 4 warps x 2 x 4 KB] [barriers]
   unsigned char* staging = smem + (size_t)kStages * kStageBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + kStagingBytes);   // used in the first CTA
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;     // [2] accumulator buffer b holds a finished tile
-  uint64_t* tempty = tfull + 2;          // [2] accumulator buffer b has been read out
+  uint64_t* tempty = tfull + 2;          // [2] both CTAs have read buffer b out (first CTA)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   const uint32_t smem_base = smem_u32(smem);
   const uint32_t empty_a = smem_u32(empty), tfull_a = smem_u32(tfull);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();              // 0: issues the MMAs, 1: its peer
+  const int pair = blockIdx.x / kPair, n_pairs = gridDim.x / kPair;
   const int nk = (g.K + kBK - 1) / kBK;
-  const int m_tiles = (g.M + kBM - 1) / kBM;
+  const int m_tiles = (g.M + kPair * kBM - 1) / (kPair * kBM);   // 256-row tiles
   const int n_tiles = (g.N + kBN - 1) / kBN;
   const int tiles = m_tiles * n_tiles;
 
@@ -176,12 +248,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     prefetch_tensormap(&map_a);
     prefetch_tensormap(&map_b);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full[s], 1);            // the first CTA's producer arrives, both CTAs' copies complete it
+      mbar_init(&empty[s], 1);           // the MMA commit arrives in both CTAs
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);          // one arrival per epilogue warp
+      mbar_init(&tempty[b], 4 * kPair);  // one arrival per epilogue warp of the pair
     }
     fence_mbar_init_cluster();
   }
@@ -190,31 +262,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();                        // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // tiles t = blockIdx.x, + gridDim.x, ...; the index runs fastest along the
-  // dimension whose operand is the smaller one, so the CTAs working at the
+  // tiles t = pair, + n_pairs, ...; the index runs fastest along the
+  // dimension whose operand is the smaller one, so the pairs working at the
   // same time share the tile of the larger operand and it streams from
   // memory about once, while the smaller one is re-read from L2
   if (warp == 0) {
     if (lane == 0) {
       griddep_wait();
+      const uint32_t full_lead = cluster_addr(smem_u32(full), 0);
       int s = 0, issued = 0;
       uint32_t pass = 0;
       bool failed = false;
-      for (int t = blockIdx.x; t < tiles && !failed; t += gridDim.x) {
-        const int m0 = (g.n_fast ? t / n_tiles : t % m_tiles) * kBM, n0 = (g.n_fast ? t % n_tiles : t / m_tiles) * kBN;
+      for (int t = pair; t < tiles && !failed; t += n_pairs) {
+        const int mt = g.n_fast ? t / n_tiles : t % m_tiles, nt = g.n_fast ? t % n_tiles : t / m_tiles;
+        const int m0 = mt * (kPair * kBM) + (int)rank * kBM;
+        const int nb = nt * kBN + (int)rank * kBRows;
         for (int kb = 0; kb < nk; ++kb) {
-          if (issued >= kStages && !mbar_wait(&empty[s], pass ^ 1u)) {
+          if (issued >= kStages && !mbar_wait_cluster(&empty[s], pass ^ 1u)) {
             failed = true;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
-          unsigned char* st = smem + (size_t)s * kStageBytes;
-          tma_load_2d(st, &map_a, &full[s], kb * kBK, m0);
-          tma_load_2d(st + kStageA, &map_b, &full[s], kb * kBK, n0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(kPair * kStageBytes));
+          const uint32_t st = smem_base + (uint32_t)s * kStageBytes;
+          tma_load_2d_pair(st, &map_a, full_lead + 8u * (uint32_t)s, kb * kBK, m0);
+          tma_load_2d_pair(st + kStageA, &map_b, full_lead + 8u * (uint32_t)s, kb * kBK, nb);
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -222,25 +297,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      // the copies of the last stages have landed before the CTA can exit
-      // (immediate when the MMA thread consumed them; bounded otherwise)
-      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-        mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u);
+      // the copies of the last stages (both CTAs') have landed before the
+      // pair can exit: immediate when the MMA thread consumed them, bounded
+      // otherwise
+      if (rank == 0)
+        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+          mbar_wait_cluster(&full[j % kStages], (uint32_t)(j / kStages) & 1u);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       int s = 0, j = 0;
       uint32_t pass = 0;
       bool failed = false;
-      for (int t = blockIdx.x; t < tiles && !failed; t += gridDim.x, ++j) {
+      for (int t = pair; t < tiles && !failed; t += n_pairs, ++j) {
         const int b = j & 1;
         const uint32_t use = (uint32_t)(j >> 1);
-        // the epilogue has read this accumulator buffer out (its previous use)
-        if (use > 0 && !mbar_wait(&tempty[b], (use - 1u) & 1u)) break;
+        // both epilogues have read this accumulator buffer out (its previous use)
+        if (use > 0 && !mbar_wait_cluster(&tempty[b], (use - 1u) & 1u)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(b * kTmemCols);
         for (int kb = 0; kb < nk; ++kb) {
-          if (!mbar_wait(&full[s], pass)) {
+          if (!mbar_wait_cluster(&full[s], pass)) {
             failed = true;
             break;
           }
@@ -251,25 +328,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)   // 16 bf16 = 32 bytes = 2 descriptor units along K
             tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
-          tc_commit(empty_a + 8u * (uint32_t)s);
+          tc_commit_pair(empty_a + 8u * (uint32_t)s);
           if (++s == kStages) {
             s = 0;
             pass ^= 1u;
           }
         }
-        tc_commit(tfull_a + 8u * (uint32_t)b);
+        tc_commit_pair(tfull_a + 8u * (uint32_t)b);
       }
     }
   } else {
-    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = rows of the tile
+    // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 = rows of this
+    // CTA's half of the tile
     const int quarter = warp & 3;
     const uint32_t lane_off = (uint32_t)(32 * quarter) << 16;
     const uint32_t stg = smem_u32(staging) + (uint32_t)(warp - 2) * 8192u;
+    const uint32_t tempty_lead = cluster_addr(smem_u32(tempty), 0);
     int j = 0, boxes = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++j) {
-      const int m0 = (g.n_fast ? t / n_tiles : t % m_tiles) * kBM, n0 = (g.n_fast ? t % n_tiles : t / m_tiles) * kBN;
+    for (int t = pair; t < tiles; t += n_pairs, ++j) {
+      const int mt = g.n_fast ? t / n_tiles : t % m_tiles, nt = g.n_fast ? t % n_tiles : t / m_tiles;
+      const int m0 = mt * (kPair * kBM) + (int)rank * kBM, n0 = nt * kBN;
       const int b = j & 1;
-      if (!mbar_wait(&tfull[b], (uint32_t)(j >> 1) & 1u)) break;
+      if (!mbar_wait_cluster(&tfull[b], (uint32_t)(j >> 1) & 1u)) break;
       tc_fence_after();
       const uint32_t acc = tmem + (uint32_t)(b * kTmemCols) + lane_off;
       const int row = m0 + 32 * quarter + lane;
@@ -312,7 +392,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           __syncwarp();
         }
-        if (g.row_stats && row < g.M) g.row_stats[(int64_t)row * n_tiles + n0 / kBN] = make_float2(rm, rs);
+        if (g.row_stats && row < g.M) g.row_stats[(int64_t)row * n_tiles + nt] = make_float2(rm, rs);
       } else {
         const bool row_on = row < g.M;
         float* crow = g.C + (int64_t)row * g.ldc;
@@ -355,17 +435,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
         }
-        if (g.row_stats && row_on) g.row_stats[(int64_t)row * n_tiles + n0 / kBN] = make_float2(rm, rs);
+        if (g.row_stats && row_on) g.row_stats[(int64_t)row * n_tiles + nt] = make_float2(rm, rs);
       }
-      // this warp is done with accumulator buffer b
+      // this warp is done with accumulator buffer b: tell the MMA thread
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_local(&tempty[b]);
+      if (lane == 0) {
+        if (rank == 0) mbar_arrive_local(&tempty[b]);
+        else mbar_arrive_remote_release(tempty_lead + 8u * (uint32_t)b);
+      }
     }
     if (lane == 0) bulk_wait_all();
   }
+  // both CTAs are done with the pair's TMEM (the peer's epilogue waited for
+  // every MMA into it) before the pair releases it
   tc_fence_before();
-  __syncthreads();
+  cluster_sync();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 2 * kTmemCols);
@@ -396,6 +481,26 @@ sf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, 
   return SF_OK;
 }
 
+// Clusters of two GEMM CTAs that fit on the device at once (cached per
+// device): the persistent grid's size.
+sf_status resident_pairs(cudaLaunchConfig_t* cfg, int* out) {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  SF_CUDA_TRY(cudaGetDevice(&dev), "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it == cache.end()) {
+    int n = 0;
+    cfg->gridDim = dim3((unsigned)(kPair * std::max(1, sm_count() / kPair)));
+    SF_CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, k_tc_gemm, cfg), "cudaOccupancyMaxActiveClusters (k_tc_gemm)");
+    if (n < 1) return fail(SF_ERR_UNSUPPORTED, "no cluster of two GEMM CTAs fits on this device");
+    it = cache.emplace(dev, n).first;
+  }
+  *out = it->second;
+  return SF_OK;
+}
+
 }  // namespace
 
 // C = alpha A B^T (+ C); shared with the cross-entropy unit.
@@ -412,7 +517,7 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
   if (!tensor_map_encoder()) return fail(SF_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available");
   CUtensorMap ma, mb;
   SF_TRY(make_map(&ma, A, M, K, lda, kBM));
-  SF_TRY(make_map(&mb, B, N, K, ldb, kBN));
+  SF_TRY(make_map(&mb, B, N, K, ldb, kBRows));
   TcGemmArgs g;
   g.C = C;
   g.ldc = ldc;
@@ -428,11 +533,24 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
   CUtensorMap mc = ma;       // unused unless g.tma
   if (g.tma) SF_TRY(make_map_c(&mc, C, M, N, ldc));
   SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&k_tc_gemm), kGemmSmem));
-  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int64_t tiles = ((M + kPair * kBM - 1) / (kPair * kBM)) * ((N + kBN - 1) / kBN);
   if (tiles > INT32_MAX) return fail(SF_ERR_UNSUPPORTED, "too many tiles");
-  const unsigned grid = (unsigned)std::min<int64_t>(tiles, sm_count());
-  k_tc_gemm<<<grid, kGemmThreads, kGemmSmem, s>>>(ma, mb, mc, g);
-  return check_launch("k_tc_gemm");
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kPair;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int pairs = 0;
+  SF_TRY(resident_pairs(&cfg, &pairs));
+  cfg.gridDim = dim3((unsigned)(kPair * std::min<int64_t>(tiles, pairs)));
+  SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_tc_gemm, ma, mb, mc, g), "launch k_tc_gemm");
+  return SF_OK;
 }
 
 int read_and_clear_device_error_gemm() {

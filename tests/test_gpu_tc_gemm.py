@@ -1,7 +1,10 @@
 """Tensor-core GEMM C = alpha A B^T (+ C) against an fp64 product (GPU).
 
 bf16 inputs, so every product is exact in fp32; the kernel sums K of them
-in fp32, which the check bounds by 1e-5 of sum |a||b| per element.
+in fp32, which the check bounds by 1e-5 of sum |a||b| per element.  The
+shapes take the pair kernel through its edges: rows or columns that end
+inside the second CTA's half of a 256 x 256 tile (or before it), ragged K,
+and more tiles than CTA pairs.
 """
 
 import numpy as np
@@ -34,9 +37,12 @@ def _check(C, A64, B64, C0=None, alpha=1.0):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 512, 1024), (200, 300, 136), (1000, 777, 520),
-                                   (64, 40, 8), (384, 1024, 4096), (1, 1, 8), (129, 257, 72),
+                                   (64, 40, 8),          # the second CTA of the pair holds no row of A or B
+                                   (384, 1024, 4096),    # odd number of 128-row halves
+                                   (1, 1, 8), (129, 257, 72),
                                    (2000, 300, 64),      # more rows than columns: tiles taken n fastest
-                                   (300, 5000, 256)])    # more tiles than SMs: several tiles per CTA
+                                   (300, 5000, 256),
+                                   (1500, 7000, 96)])    # 168 tiles: up to three per CTA pair, both accumulators reused
 def test_gemm_matches_fp64(M, N, K):
     A, B = _inputs(M, N, K, M + N + K)
     C = torch.full((M, N), float("nan"), device=DEV)
