@@ -287,6 +287,21 @@ sf_status sf_gemm_abt_bf16(const void* A, const void* B, float* C, int64_t M,
                            int64_t N, int64_t K, int64_t lda, int64_t ldb,
                            int64_t ldc, float alpha, int accumulate, void* stream);
 
+/* The same product with either operand stored transposed:
+ *   a_layout 0: A is [M][lda] row-major (K-major), lda >= K;
+ *   a_layout 1: A is stored as A^T, [K][lda] row-major (M-major), lda >= M;
+ *   b_layout 0: B is [N][ldb] row-major (K-major), ldb >= K;
+ *   b_layout 1: B is stored as B^T, [K][ldb] row-major (N-major), ldb >= N.
+ * For example, b_layout 1 with a row-major X [K][N] as B gives
+ * C = alpha * A * X, and a_layout 1 with a row-major Y [K][M] as A gives
+ * C = alpha * Y^T * B^T.  A layout other than 0 or 1 returns SF_ERR_INVALID;
+ * alignment, shape limits and determinism as sf_gemm_abt_bf16 (which is
+ * layouts 0, 0). */
+sf_status sf_gemm_bf16(const void* A, int a_layout, const void* B, int b_layout,
+                       float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                       int64_t ldb, int64_t ldc, float alpha, int accumulate,
+                       void* stream);
+
 /* ------------------------------------------------------------------------
  * Fused linear cross-entropy (SlideFormer, "Fused LinearCrossEntropy" in the
  * summaries' kernel lists: the output projection and the loss fused, the
@@ -303,7 +318,8 @@ sf_status sf_gemm_abt_bf16(const void* A, const void* B, float* C, int64_t M,
  *            ignore_index counts as unlabelled and is reported by
  *            sf_sync_status (SF_ERR_INVALID).
  *   chunk  : tokens per block (a positive multiple of 8; the call holds one
- *            chunk of fp32 logits and two of the bf16 gradient).
+ *            chunk of fp32 logits and one of the bf16 gradient, no
+ *            transposed copies).
  *   loss   : device double [1], written; may be NULL.
  *   dH     : device fp32 [N][D], written; may be NULL.
  *   dW     : device fp32 [V][D], written; may be NULL (both NULL: loss only).

@@ -113,14 +113,16 @@ int read_and_clear_device_error_adamw();
 int read_and_clear_device_error_gemm();
 int read_and_clear_device_error_lce();
 
-// C = alpha A B^T (+ C) on the tensor cores (tc_gemm.cu): A [M][K] and
-// B [N][K] bf16 row-major, C fp32 [M][ldc].  With row_stats (float2
-// [M][ceil(N / 256)]) the epilogue also writes, per row and 256-column tile,
-// the maximum of the row's values and the sum of exp(value - maximum).
+// C = alpha A B^T (+ C) on the tensor cores (tc_gemm.cu): A bf16 [M][lda]
+// row-major (K-major) or, with a_mn, [K][lda] (MN-major: A^T stored);
+// B likewise [N][ldb] or, with b_mn, [K][ldb]; C fp32 [M][ldc].  With
+// row_stats (float2 [M][ceil(N / 256)]) the epilogue also writes, per row and
+// 256-column tile, the maximum of the row's values and the sum of
+// exp(value - maximum).
 constexpr int kTcTileN = 256;
-sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                      int64_t ldb, int64_t ldc, float alpha, bool accumulate, cudaStream_t s,
-                      float2* row_stats = nullptr);
+sf_status tc_gemm(const void* A, bool a_mn, const void* B, bool b_mn, float* C, int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc, float alpha, bool accumulate, cudaStream_t s,
+                  float2* row_stats = nullptr);
 
 sf_status make_adam_consts(const sf_adamw_hparams* hp, int64_t step, bool with_decay,
                            AdamConsts* out);

@@ -12,14 +12,14 @@
 //   lse  = logsumexp over each row of Z_c, from (max, sum exp) pairs the
 //          logits GEMM's epilogue writes per row and 256-column tile, and
 //          the rows' losses
-//   G_c  = (softmax(Z_c) - onehot(y_c)) / n  rounded to bf16, written both
-//          as [chunk][V] and transposed [V][chunk]
-//   dH_c = G_c W                        tensor cores (W^T made once per call)
-//   dW  += G_c^T H_c                    tensor cores (H_c^T made per chunk)
+//   G_c  = (softmax(Z_c) - onehot(y_c)) / n  rounded to bf16 [chunk][V]
+//   dH_c = G_c W                        tensor cores, W read MN-major
+//   dW  += G_c^T H_c                    tensor cores, G_c and H_c read MN-major
 // n is the number of tokens whose label is not ignore_index.  The three
-// products run on the tensor-core GEMM (tc_gemm.cu); the row statistics and
-// the gradient tile are fp32 CUDA-core kernels.  Memory: one chunk of
-// logits (fp32) and two of the bf16 gradient instead of N x V.
+// products run on the tensor-core GEMM (tc_gemm.cu), which reads either
+// layout of an operand, so no transposed copy of W, G or H is made; the row
+// statistics and the gradient are fp32 CUDA-core kernels.  Memory: one
+// chunk of logits (fp32) and one of the bf16 gradient instead of N x V.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -29,39 +29,6 @@
 
 namespace sf {
 namespace {
-
-// out[c][r] = in[r][c] for a rows x cols bf16 matrix (row pitches ld_in,
-// ld_out; cols, ld_in and ld_out even), through a padded 64 x 64 tile held as
-// 32-bit words: coalesced 4-byte loads of column pairs, and each output word
-// (rows 2p and 2p + 1 of one column) assembled from two tile words.
-__global__ void __launch_bounds__(256) k_transpose_bf16(const uint16_t* __restrict__ in, int64_t rows,
-                                                        int64_t cols, int64_t ld_in, uint16_t* __restrict__ out,
-                                                        int64_t ld_out) {
-  __shared__ uint32_t tile[64][33];
-  const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int q = threadIdx.x + 256 * k;       // 64 rows x 32 words
-    const int r = q >> 5, w = q & 31;
-    const int64_t i = r0 + r, j = c0 + 2 * w;
-    uint32_t v = 0;
-    if (i < rows && j < cols) v = *reinterpret_cast<const uint32_t*>(in + i * ld_in + j);
-    tile[r][w] = v;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int q = threadIdx.x + 256 * k;       // 64 output rows (columns c) x 32 words (row pairs p)
-    const int c = q >> 5, p = q & 31;
-    const int64_t j = c0 + c, i = r0 + 2 * p;
-    if (j < cols && i < rows) {
-      const uint32_t lo = tile[2 * p][c >> 1], hi = tile[2 * p + 1][c >> 1];
-      // the half of each word that holds column c (low half = even column)
-      const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
-      *reinterpret_cast<uint32_t*>(out + j * ld_out + i) = __byte_perm(lo, hi, sel);
-    }
-  }
-}
 
 // Number n of labelled tokens (label != ignore and in [0, V)); a label that
 // is neither is counted as unlabelled and flagged.  inv_n = 1/n (0 if n = 0).
@@ -144,50 +111,46 @@ __global__ void __launch_bounds__(256) k_lce_lse(const float2* __restrict__ stat
   }
 }
 
-// The gradient tile: g = (exp(z - lse) - [j == y]) * inv_n (0 for an
-// unlabelled row), rounded to bf16, written to G [rows][V] and Gt
-// [V][ld_gt] (columns = rows of the chunk).  Each thread takes column pairs
-// (8-byte loads of Z, 4-byte stores of G); the transposed copy goes through
-// a padded tile of 32-bit words like k_transpose_bf16.  V, ld_gt even.
+// The gradient: g = (exp(z - lse) - [j == y]) * inv_n (0 for an unlabelled
+// row), rounded to bf16, G [rows][V].  A CTA takes 8192 columns of one row:
+// each thread 8 float4 loads of Z in flight (read once, streaming) and
+// 8-byte stores of 4 bf16.  V is a multiple of 8.
+constexpr int kGradCols = 256 * 4 * 8;
 __global__ void __launch_bounds__(256) k_lce_grad(const float* __restrict__ Z, int64_t rows, int64_t V,
                                                   const float* __restrict__ lse, const int32_t* __restrict__ labels,
                                                   int32_t ignore, const float* __restrict__ inv_n,
-                                                  __nv_bfloat16* __restrict__ G, __nv_bfloat16* __restrict__ Gt,
-                                                  int64_t ld_gt) {
-  __shared__ uint32_t tile[64][33];
-  const int64_t r0 = (int64_t)blockIdx.y * 64, j0 = (int64_t)blockIdx.x * 64;
+                                                  __nv_bfloat16* __restrict__ G) {
   const float sc = *inv_n;
+  const int64_t j0 = (int64_t)blockIdx.x * kGradCols + 4 * threadIdx.x;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    const int32_t y = labels[r];
+    const bool on = labelled(y, ignore, V);
+    const float l = lse[r];
+    const float* zr = Z + r * V;
+    __nv_bfloat16* gr = G + r * V;
+    float4 z[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int q = threadIdx.x + 256 * k;       // 64 rows x 32 column pairs
-    const int r = q >> 5, w = q & 31;
-    const int64_t i = r0 + r, j = j0 + 2 * w;
-    uint32_t word = 0;
-    if (i < rows && j < V) {
-      const int32_t y = labels[i];
-      float g0 = 0.0f, g1 = 0.0f;
-      if (labelled(y, ignore, V)) {
-        const float2 z = *reinterpret_cast<const float2*>(Z + i * V + j);
-        const float l = lse[i];
-        g0 = (expf(z.x - l) - (j == y ? 1.0f : 0.0f)) * sc;
-        g1 = (expf(z.y - l) - (j + 1 == y ? 1.0f : 0.0f)) * sc;
-      }
-      const __nv_bfloat162 h = __floats2bfloat162_rn(g0, g1);
-      word = *reinterpret_cast<const uint32_t*>(&h);
-      *reinterpret_cast<uint32_t*>(G + i * V + j) = word;
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = j0 + 1024 * u;
+      z[u] = (on && j < V) ? __ldcs(reinterpret_cast<const float4*>(zr + j)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    tile[r][w] = word;
-  }
-  __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const int q = threadIdx.x + 256 * k;       // 64 columns c x 32 row pairs p
-    const int c = q >> 5, p = q & 31;
-    const int64_t j = j0 + c, i = r0 + 2 * p;
-    if (j < V && i < rows) {
-      const uint32_t lo = tile[2 * p][c >> 1], hi = tile[2 * p + 1][c >> 1];
-      const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
-      *reinterpret_cast<uint32_t*>(Gt + j * ld_gt + i) = __byte_perm(lo, hi, sel);
+    for (int u = 0; u < 8; ++u) {
+      const int64_t j = j0 + 1024 * u;
+      if (j < V) {
+        float g0 = 0.0f, g1 = 0.0f, g2 = 0.0f, g3 = 0.0f;
+        if (on) {
+          g0 = (expf(z[u].x - l) - (j == y ? 1.0f : 0.0f)) * sc;
+          g1 = (expf(z[u].y - l) - (j + 1 == y ? 1.0f : 0.0f)) * sc;
+          g2 = (expf(z[u].z - l) - (j + 2 == y ? 1.0f : 0.0f)) * sc;
+          g3 = (expf(z[u].w - l) - (j + 3 == y ? 1.0f : 0.0f)) * sc;
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(g0, g1), hi = __floats2bfloat162_rn(g2, g3);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t*>(&lo);
+        w.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(gr + j) = w;
+      }
     }
   }
 }
@@ -208,7 +171,7 @@ __global__ void __launch_bounds__(1024) k_lce_loss(const float* __restrict__ row
 }
 
 struct LcePlan {
-  size_t off_z, off_g, off_gt, off_wt, off_ht, off_lse, off_rowloss, off_n, off_stats, bytes;
+  size_t off_z, off_g, off_lse, off_rowloss, off_n, off_stats, bytes;
 };
 
 LcePlan plan_lce(int64_t N, int64_t D, int64_t V, int64_t chunk) {
@@ -221,9 +184,6 @@ LcePlan plan_lce(int64_t N, int64_t D, int64_t V, int64_t chunk) {
   };
   p.off_z = take((size_t)chunk * V * 4);
   p.off_g = take((size_t)chunk * V * 2);
-  p.off_gt = take((size_t)V * chunk * 2);
-  p.off_wt = take((size_t)D * V * 2);
-  p.off_ht = take((size_t)D * chunk * 2);
   p.off_lse = take((size_t)chunk * 4);
   p.off_rowloss = take((size_t)N * 4);
   p.off_n = take(16);
@@ -264,7 +224,7 @@ sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labe
   if ((dH && reinterpret_cast<uintptr_t>(dH) % 16) || (dW && reinterpret_cast<uintptr_t>(dW) % 16))
     return sf::fail(SF_ERR_UNSUPPORTED, "dH and dW need 16-byte aligned bases");
   chunk = std::min(chunk, (N + 7) / 8 * 8);
-  if ((chunk + 63) / 64 > 65535 || (V + 63) / 64 > (int64_t)INT32_MAX || N > (int64_t)INT32_MAX)
+  if (V > (int64_t)INT32_MAX / 2 || N > (int64_t)INT32_MAX || D > (int64_t)INT32_MAX / 2)
     return sf::fail(SF_ERR_UNSUPPORTED, "sizes too large");
   const sf::LcePlan p = sf::plan_lce(N, D, V, chunk);
   if (!ws || ws_bytes < p.bytes || (reinterpret_cast<uintptr_t>(ws) % 256))
@@ -273,9 +233,6 @@ sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labe
   char* w = static_cast<char*>(ws);
   float* Z = reinterpret_cast<float*>(w + p.off_z);
   __nv_bfloat16* G = reinterpret_cast<__nv_bfloat16*>(w + p.off_g);
-  __nv_bfloat16* Gt = reinterpret_cast<__nv_bfloat16*>(w + p.off_gt);
-  uint16_t* Wt = reinterpret_cast<uint16_t*>(w + p.off_wt);
-  uint16_t* Ht = reinterpret_cast<uint16_t*>(w + p.off_ht);
   float* lse = reinterpret_cast<float*>(w + p.off_lse);
   float* row_loss = reinterpret_cast<float*>(w + p.off_rowloss);
   int64_t* n_valid = reinterpret_cast<int64_t*>(w + p.off_n);
@@ -287,28 +244,20 @@ sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labe
 
   sf::k_lce_count<<<1, 1024, 0, s>>>(labels, N, V, ignore_index, n_valid, inv_n);
   SF_TRY(sf::check_launch("k_lce_count"));
-  if (dH) {
-    sf::k_transpose_bf16<<<dim3((unsigned)sf::ceil_div<int64_t>(D, 64), (unsigned)sf::ceil_div<int64_t>(V, 64)), 256, 0, s>>>(
-        static_cast<const uint16_t*>(W), V, D, D, Wt, V);
-    SF_TRY(sf::check_launch("k_transpose_bf16"));
-  }
   for (int64_t c0 = 0; c0 < N; c0 += chunk) {
     const int64_t rows = std::min(chunk, N - c0);
-    SF_TRY(sf::tc_gemm_abt(Hb + c0 * D, W, Z, rows, V, D, D, D, V, 1.0f, false, s, stats));
+    SF_TRY(sf::tc_gemm(Hb + c0 * D, false, W, false, Z, rows, V, D, D, D, V, 1.0f, false, s, stats));
     sf::k_lce_lse<<<(unsigned)sf::ceil_div<int64_t>(rows, 8), 256, 0, s>>>(stats, n_vt, rows, Z, V, labels + c0,
                                                                              ignore_index, lse, row_loss + c0);
     SF_TRY(sf::check_launch("k_lce_lse"));
     if (!grads) continue;
-    sf::k_lce_grad<<<dim3((unsigned)sf::ceil_div<int64_t>(V, 64), (unsigned)sf::ceil_div<int64_t>(rows, 64)), 256, 0, s>>>(
-        Z, rows, V, lse, labels + c0, ignore_index, inv_n, G, Gt, chunk);
+    const dim3 grid((unsigned)sf::ceil_div<int64_t>(V, sf::kGradCols), (unsigned)std::min<int64_t>(rows, 65535));
+    sf::k_lce_grad<<<grid, 256, 0, s>>>(Z, rows, V, lse, labels + c0, ignore_index, inv_n, G);
     SF_TRY(sf::check_launch("k_lce_grad"));
-    if (dH) SF_TRY(sf::tc_gemm_abt(G, Wt, dH + c0 * D, rows, D, V, V, V, D, 1.0f, false, s));
-    if (dW) {
-      sf::k_transpose_bf16<<<dim3((unsigned)sf::ceil_div<int64_t>(D, 64), (unsigned)sf::ceil_div<int64_t>(rows, 64)), 256, 0,
-                             s>>>(Hb + c0 * D, rows, D, D, Ht, chunk);
-      SF_TRY(sf::check_launch("k_transpose_bf16"));
-      SF_TRY(sf::tc_gemm_abt(Gt, Ht, dW, V, D, rows, chunk, chunk, D, 1.0f, c0 > 0, s));
-    }
+    // dH_c = G_c W: G_c K-major [rows][V]; W is [V][D] = B stored [K][N]
+    if (dH) SF_TRY(sf::tc_gemm(G, false, W, true, dH + c0 * D, rows, D, V, V, D, D, 1.0f, false, s));
+    // dW += G_c^T H_c: A = G_c^T stored [K = rows][M = V], B = H_c^T stored [K][N = D]
+    if (dW) SF_TRY(sf::tc_gemm(G, true, Hb + c0 * D, true, dW, V, D, rows, V, D, D, 1.0f, c0 > 0, s));
   }
   if (loss) {
     sf::k_lce_loss<<<1, 1024, 0, s>>>(row_loss, N, inv_n, loss);

@@ -1,5 +1,7 @@
 // Tensor-core GEMM on the 5th-generation tensor cores: C (fp32) = alpha A B^T
-// (+ C), A [M][K] and B [N][K] bf16 row-major (both K-contiguous).
+// (+ C) with A [M x K] and B [N x K] in bf16, each stored either K-major
+// (row-major [M][K], [N][K]) or MN-major (row-major [K][M], [K][N]: the
+// transposed matrix), so products like G W or G^T H need no transposed copy.
 //
 // The dense products of the fused linear cross-entropy (logits, and the two
 // gradient products) are real dense contractions, so they run here rather
@@ -13,8 +15,10 @@
 // computing 128 x 256 alone, which leaves room for a 6-deep ring.  In each
 // CTA:
 //   warp 0       TMA producer: 64-wide K slabs of its A rows (128 x 64) and
-//                B rows (128 x 64) into a 6-stage ring, 128-byte swizzled;
-//                both CTAs' copies complete on the first CTA's stage barrier;
+//                B rows (128 x 64) into a 6-stage ring, 128-byte swizzled
+//                (a K-major operand as one 128-row box, an MN-major one as
+//                two boxes of 64 x 64); both CTAs' copies complete on the
+//                first CTA's stage barrier;
 //   warp 1       allocates 512 TMEM columns with its peer (two accumulators
 //                of 256 fp32 columns); in the first CTA one elected thread
 //                issues tcgen05.mma (M 256, N 256, K 16, bf16 in, fp32
@@ -48,15 +52,16 @@ constexpr int kBRows = kBN / kPair;            // rows of B held by one CTA
 constexpr int kStageA = kBM * kBK * 2;         // 16 KB
 constexpr int kStageB = kBRows * kBK * 2;      // 16 KB
 constexpr int kStageBytes = kStageA + kStageB;
+constexpr int kMnBox = 64 * kBK * 2;           // an MN-major box: 64 MN x 64 K bf16 = 8 KB
 constexpr int kTmemCols = 256;                 // one accumulator; two are allocated
 constexpr int kGemmThreads = 192;
 constexpr int kStagingBytes = 4 * 2 * 4096;    // epilogue: 4 warps x 2 boxes of 32 x 32 fp32
 constexpr size_t kGemmSmem = (size_t)kStages * kStageBytes + kStagingBytes + 1024 + 256;
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator
-// (bits 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), both K-major
-// (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28 (M = 256:
-// the pair's rows).
+// (bits 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), A and B K-major
+// (bits 15, 16 = 0; set per launch for an MN-major operand), N >> 3 in
+// bits 17-22, M >> 4 in bits 24-28 (M = 256: the pair's rows).
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) |
                             ((uint32_t)((kPair * kBM) >> 4) << 24);
 
@@ -69,6 +74,21 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   d |= (uint64_t)(1024 >> 4) << 32;       // stride-dimension offset: 1024 bytes
   d |= (uint64_t)1 << 46;                 // descriptor version
   d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+
+// The same for an MN-major operand tile: TMA boxes of 64 MN-contiguous
+// elements (128 bytes) by 64 K rows, 128-byte swizzled, two of them side by
+// side for 128 rows of MN.  The canonical MN-major layout takes the offset
+// between 64-element MN blocks as the leading-dimension offset (one box,
+// 8192 bytes) and between 8-row K groups as the stride-dimension offset
+// (1024 bytes); a K-16 step advances the start by 16 rows = 2048 bytes.
+__device__ __forceinline__ uint64_t umma_desc_mn_sw128(uint32_t smem_addr) {
+  uint64_t d = (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(kMnBox >> 4) << 16;     // leading-dimension offset: next 64 MN elements
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride-dimension offset: next 8 K rows
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
   return d;
 }
 
@@ -201,6 +221,7 @@ struct TcGemmArgs {
   int32_t vec;           // C rows 16-byte aligned (float4 epilogue)
   int32_t tma;           // C written by tensor stores (reduce-add when accumulating) from shared memory
   int32_t n_fast;        // tile order: n fastest (A is the larger operand) or m fastest
+  int32_t a_mn, b_mn;    // operand stored MN-major ([K][M], [K][N]) instead of K-major
   float2* row_stats;     // optional [M][n_tiles]: per row and column tile, (max, sum exp(c - max)) of C
 };
 
@@ -288,8 +309,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           if (rank == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(kPair * kStageBytes));
           const uint32_t st = smem_base + (uint32_t)s * kStageBytes;
-          tma_load_2d_pair(st, &map_a, full_lead + 8u * (uint32_t)s, kb * kBK, m0);
-          tma_load_2d_pair(st + kStageA, &map_b, full_lead + 8u * (uint32_t)s, kb * kBK, nb);
+          const uint32_t bar = full_lead + 8u * (uint32_t)s;
+          if (g.a_mn) {
+            tma_load_2d_pair(st, &map_a, bar, m0, kb * kBK);
+            tma_load_2d_pair(st + kMnBox, &map_a, bar, m0 + 64, kb * kBK);
+          } else {
+            tma_load_2d_pair(st, &map_a, bar, kb * kBK, m0);
+          }
+          if (g.b_mn) {
+            tma_load_2d_pair(st + kStageA, &map_b, bar, nb, kb * kBK);
+            tma_load_2d_pair(st + kStageA + kMnBox, &map_b, bar, nb + 64, kb * kBK);
+          } else {
+            tma_load_2d_pair(st + kStageA, &map_b, bar, kb * kBK, nb);
+          }
           ++issued;
           if (++s == kStages) {
             s = 0;
@@ -306,6 +338,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
+      // K-16 step in descriptor units (16 bytes): 32 bytes along a K-major
+      // row, 16 rows of 128 bytes down an MN-major box
+      const uint32_t a_step = g.a_mn ? 128u : 2u, b_step = g.b_mn ? 128u : 2u;
+      const uint32_t idesc = kIdesc | ((uint32_t)g.a_mn << 15) | ((uint32_t)g.b_mn << 16);
       int s = 0, j = 0;
       uint32_t pass = 0;
       bool failed = false;
@@ -323,11 +359,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t a_addr = smem_base + (uint32_t)s * kStageBytes;
-          const uint64_t adesc = umma_desc_sw128(a_addr);
-          const uint64_t bdesc = umma_desc_sw128(a_addr + kStageA);
+          const uint64_t adesc = g.a_mn ? umma_desc_mn_sw128(a_addr) : umma_desc_sw128(a_addr);
+          const uint64_t bdesc = g.b_mn ? umma_desc_mn_sw128(a_addr + kStageA) : umma_desc_sw128(a_addr + kStageA);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)   // 16 bf16 = 32 bytes = 2 descriptor units along K
-            tc_mma(d_tmem, adesc + 2u * k, bdesc + 2u * k, kIdesc, (kb | k) != 0 ? 1u : 0u);
+          for (int k = 0; k < kBK / 16; ++k)
+            tc_mma(d_tmem, adesc + a_step * (uint32_t)k, bdesc + b_step * (uint32_t)k, idesc, (kb | k) != 0 ? 1u : 0u);
           tc_commit_pair(empty_a + 8u * (uint32_t)s);
           if (++s == kStages) {
             s = 0;
@@ -469,10 +505,14 @@ sf_status make_map_c(CUtensorMap* map, float* C, int64_t M, int64_t N, int64_t l
   return SF_OK;
 }
 
-sf_status make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int64_t ld, int box_rows) {
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+// bf16 operand map: a row-major [outer][ld] matrix read as boxes of 64
+// inner elements (128 bytes, swizzled) by box_outer rows.  K-major operands
+// have K inner (box_outer = their rows in a CTA), MN-major ones MN inner
+// (box_outer = 64 K rows).
+sf_status make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
                                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -504,20 +544,25 @@ sf_status resident_pairs(cudaLaunchConfig_t* cfg, int* out) {
 }  // namespace
 
 // C = alpha A B^T (+ C); shared with the cross-entropy unit.
-sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                      int64_t ldb, int64_t ldc, float alpha, bool accumulate, cudaStream_t s, float2* row_stats) {
+sf_status tc_gemm(const void* A, bool a_mn, const void* B, bool b_mn, float* C, int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc, float alpha, bool accumulate, cudaStream_t s,
+                  float2* row_stats) {
   if (!A || !B || !C) return fail(SF_ERR_INVALID, "A, B or C is NULL");
   if (M < 1 || N < 1 || K < 1) return fail(SF_ERR_INVALID, "M, N, K must be >= 1");
-  if (M > INT32_MAX - kBM || N > INT32_MAX - kBN || K > INT32_MAX - kBK)
+  if (M > INT32_MAX - 2 * kPair * kBM || N > INT32_MAX - kBN || K > INT32_MAX - kBK)
     return fail(SF_ERR_UNSUPPORTED, "M, N, K must be below 2^31");
-  if (lda < K || ldb < K || ldc < N) return fail(SF_ERR_INVALID, "leading dimensions must be >= K (A, B), N (C)");
+  if (lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldc < N)
+    return fail(SF_ERR_INVALID, "leading dimensions must be >= the stored rows' length (lda: K or M, ldb: K or N; "
+                                "ldc: N)");
   if ((lda * 2) % 16 || (ldb * 2) % 16 || (reinterpret_cast<uintptr_t>(A) % 16) ||
       (reinterpret_cast<uintptr_t>(B) % 16))
     return fail(SF_ERR_UNSUPPORTED, "A and B need 16-byte aligned bases and rows (lda, ldb multiples of 8)");
   if (!tensor_map_encoder()) return fail(SF_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available");
   CUtensorMap ma, mb;
-  SF_TRY(make_map(&ma, A, M, K, lda, kBM));
-  SF_TRY(make_map(&mb, B, N, K, ldb, kBRows));
+  if (a_mn) SF_TRY(make_map(&ma, A, M, K, lda, kBK));
+  else SF_TRY(make_map(&ma, A, K, M, lda, kBM));
+  if (b_mn) SF_TRY(make_map(&mb, B, N, K, ldb, kBK));
+  else SF_TRY(make_map(&mb, B, K, N, ldb, kBRows));
   TcGemmArgs g;
   g.C = C;
   g.ldc = ldc;
@@ -529,6 +574,8 @@ sf_status tc_gemm_abt(const void* A, const void* B, float* C, int64_t M, int64_t
   g.vec = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0) ? 1 : 0;
   g.tma = g.vec;
   g.n_fast = M > N ? 1 : 0;
+  g.a_mn = a_mn ? 1 : 0;
+  g.b_mn = b_mn ? 1 : 0;
   g.row_stats = row_stats;
   CUtensorMap mc = ma;       // unused unless g.tma
   if (g.tma) SF_TRY(make_map_c(&mc, C, M, N, ldc));
@@ -568,7 +615,18 @@ sf_status sf_gemm_abt_bf16(const void* A, const void* B, float* C, int64_t M, in
                            int64_t ldb, int64_t ldc, float alpha, int accumulate, void* stream) {
   sf::clear_error();
   sf::NvtxRange nvtx_range("sf_gemm_abt_bf16");
-  return sf::tc_gemm_abt(A, B, C, M, N, K, lda, ldb, ldc, alpha, accumulate != 0, sf::as_stream(stream));
+  return sf::tc_gemm(A, false, B, false, C, M, N, K, lda, ldb, ldc, alpha, accumulate != 0, sf::as_stream(stream),
+                     nullptr);
+}
+
+sf_status sf_gemm_bf16(const void* A, int a_layout, const void* B, int b_layout, float* C, int64_t M, int64_t N,
+                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc, float alpha, int accumulate, void* stream) {
+  sf::clear_error();
+  sf::NvtxRange nvtx_range("sf_gemm_bf16");
+  if ((a_layout != 0 && a_layout != 1) || (b_layout != 0 && b_layout != 1))
+    return sf::fail(SF_ERR_INVALID, "a_layout and b_layout must be 0 (K-major) or 1 (MN-major)");
+  return sf::tc_gemm(A, a_layout == 1, B, b_layout == 1, C, M, N, K, lda, ldb, ldc, alpha, accumulate != 0,
+                     sf::as_stream(stream), nullptr);
 }
 
 }  // extern "C"

@@ -79,3 +79,38 @@ def test_gemm_is_deterministic_and_rejects_bad_strides():
     assert torch.equal(C1, C2)
     with pytest.raises(native.SfError, match="aligned"):
         native.sf_gemm_abt_bf16(Ad, Bd, C1, M, N, K - 4, K - 4, K, N)
+
+
+@pytest.mark.parametrize("a_layout,b_layout", [(0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (64, 40, 8), (129, 257, 72), (2000, 300, 136),
+                                   (1500, 7000, 96)])
+def test_gemm_transposed_layouts(a_layout, b_layout, M, N, K):
+    # an operand stored transposed (MN-major: [K][M] or [K][N]) with padded
+    # rows; the product is the same as with both operands K-major
+    A, B = _inputs(M, N, K, 31 + M + N + K)
+    lda = -(-(M if a_layout else K) // 8) * 8 + 8       # rows padded, 16-byte multiples
+    ldb = -(-(N if b_layout else K) // 8) * 8 + 16
+    As = A.t() if a_layout else A
+    Bs = B.t() if b_layout else B
+    Ad = torch.zeros(As.shape[0], lda, dtype=torch.bfloat16, device=DEV)
+    Bd = torch.zeros(Bs.shape[0], ldb, dtype=torch.bfloat16, device=DEV)
+    Ad[:, :As.shape[1]] = As.to(DEV)
+    Bd[:, :Bs.shape[1]] = Bs.to(DEV)
+    C = torch.full((M, N), float("nan"), device=DEV)
+    native.sf_gemm_bf16(Ad, a_layout, Bd, b_layout, C, M, N, K, lda, ldb, N)
+    torch.cuda.synchronize()
+    native.sf_sync_status()
+    _check(C, f64(A), f64(B))
+    C0 = C.clone()
+    native.sf_gemm_bf16(Ad, a_layout, Bd, b_layout, C, M, N, K, lda, ldb, N, alpha=2.0, accumulate=True)
+    torch.cuda.synchronize()
+    _check(C, f64(A), f64(B), C0=f64(C0), alpha=2.0)
+
+
+def test_gemm_layout_rejections():
+    A = torch.zeros(64, 64, dtype=torch.bfloat16, device=DEV)
+    C = torch.empty(64, 64, device=DEV)
+    with pytest.raises(native.SfError, match="layout"):
+        native.sf_gemm_bf16(A, 2, A, 0, C, 64, 64, 64, 64, 64, 64)
+    with pytest.raises(native.SfError, match="leading"):
+        native.sf_gemm_bf16(A, 1, A, 0, C, 72, 64, 64, 64, 64, 64)     # lda 64 < M 72 for a transposed A
