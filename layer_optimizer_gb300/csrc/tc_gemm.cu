@@ -142,6 +142,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// The same with a 3D box (an MN-major operand: 64 MN x 64 K x two
+// 64-element MN blocks, stored block after block).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                                 int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+      "l"(map), "r"(bar), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
@@ -221,7 +232,8 @@ struct TcGemmArgs {
   int32_t vec;           // C rows 16-byte aligned (float4 epilogue)
   int32_t tma;           // C written by tensor stores (reduce-add when accumulating) from shared memory
   int32_t n_fast;        // tile order: n fastest (A is the larger operand) or m fastest
-  int32_t a_mn, b_mn;    // operand stored MN-major ([K][M], [K][N]) instead of K-major
+  int32_t a_mn, b_mn;    // operand stored MN-major ([K][M], [K][N]) instead of K-major:
+                         // 1 loaded as two 2D boxes, 2 as one 3D box (MN a multiple of 64)
   float2* row_stats;     // optional [M][n_tiles]: per row and column tile, (max, sum exp(c - max)) of C
 };
 
@@ -310,13 +322,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (rank == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(kPair * kStageBytes));
           const uint32_t st = smem_base + (uint32_t)s * kStageBytes;
           const uint32_t bar = full_lead + 8u * (uint32_t)s;
-          if (g.a_mn) {
+          if (g.a_mn == 2) {
+            tma_load_3d_pair(st, &map_a, bar, 0, kb * kBK, m0 >> 6);
+          } else if (g.a_mn) {
             tma_load_2d_pair(st, &map_a, bar, m0, kb * kBK);
             tma_load_2d_pair(st + kMnBox, &map_a, bar, m0 + 64, kb * kBK);
           } else {
             tma_load_2d_pair(st, &map_a, bar, kb * kBK, m0);
           }
-          if (g.b_mn) {
+          if (g.b_mn == 2) {
+            tma_load_3d_pair(st + kStageA, &map_b, bar, 0, kb * kBK, nb >> 6);
+          } else if (g.b_mn) {
             tma_load_2d_pair(st + kStageA, &map_b, bar, nb, kb * kBK);
             tma_load_2d_pair(st + kStageA + kMnBox, &map_b, bar, nb + 64, kb * kBK);
           } else {
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // K-16 step in descriptor units (16 bytes): 32 bytes along a K-major
       // row, 16 rows of 128 bytes down an MN-major box
       const uint32_t a_step = g.a_mn ? 128u : 2u, b_step = g.b_mn ? 128u : 2u;
-      const uint32_t idesc = kIdesc | ((uint32_t)g.a_mn << 15) | ((uint32_t)g.b_mn << 16);
+      const uint32_t idesc = kIdesc | ((g.a_mn ? 1u : 0u) << 15) | ((g.b_mn ? 1u : 0u) << 16);
       int s = 0, j = 0;
       uint32_t pass = 0;
       bool failed = false;
@@ -521,6 +537,22 @@ sf_status make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t ou
   return SF_OK;
 }
 
+// An MN-major operand [K][ld] (MN inner, a multiple of 64) viewed in 3D as
+// {64 MN, K, MN / 64 blocks} with the blocks 128 bytes apart, so one box
+// {64, 64, 2} brings the 128 MN rows a CTA needs for a K slab (two 64 x 64
+// swizzled blocks, one after the other) in one copy.  Every address of the
+// view lies inside the matrix; false if the driver does not take the map.
+bool make_map_mn3d(CUtensorMap* map, const void* base, int64_t mn, int64_t K, int64_t ld) {
+  if (mn % 64) return false;
+  cuuint64_t dims[3] = {64u, (cuuint64_t)K, (cuuint64_t)(mn / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)(ld * 2), 128u};
+  cuuint32_t box[3] = {64u, (cuuint32_t)kBK, 2u};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return tensor_map_encoder()(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Clusters of two GEMM CTAs that fit on the device at once (cached per
 // device): the persistent grid's size.
 sf_status resident_pairs(cudaLaunchConfig_t* cfg, int* out) {
@@ -559,10 +591,19 @@ sf_status tc_gemm(const void* A, bool a_mn, const void* B, bool b_mn, float* C, 
     return fail(SF_ERR_UNSUPPORTED, "A and B need 16-byte aligned bases and rows (lda, ldb multiples of 8)");
   if (!tensor_map_encoder()) return fail(SF_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available");
   CUtensorMap ma, mb;
-  if (a_mn) SF_TRY(make_map(&ma, A, M, K, lda, kBK));
-  else SF_TRY(make_map(&ma, A, K, M, lda, kBM));
-  if (b_mn) SF_TRY(make_map(&mb, B, N, K, ldb, kBK));
-  else SF_TRY(make_map(&mb, B, K, N, ldb, kBRows));
+  int a_form = 0, b_form = 0;      // 0 K-major, 1 MN-major in 2D boxes, 2 MN-major in 3D boxes
+  if (a_mn) {
+    a_form = make_map_mn3d(&ma, A, M, K, lda) ? 2 : 1;
+    if (a_form == 1) SF_TRY(make_map(&ma, A, M, K, lda, kBK));
+  } else {
+    SF_TRY(make_map(&ma, A, K, M, lda, kBM));
+  }
+  if (b_mn) {
+    b_form = make_map_mn3d(&mb, B, N, K, ldb) ? 2 : 1;
+    if (b_form == 1) SF_TRY(make_map(&mb, B, N, K, ldb, kBK));
+  } else {
+    SF_TRY(make_map(&mb, B, K, N, ldb, kBRows));
+  }
   TcGemmArgs g;
   g.C = C;
   g.ldc = ldc;
@@ -574,8 +615,8 @@ sf_status tc_gemm(const void* A, bool a_mn, const void* B, bool b_mn, float* C, 
   g.vec = (ldc % 4 == 0) && (reinterpret_cast<uintptr_t>(C) % 16 == 0) ? 1 : 0;
   g.tma = g.vec;
   g.n_fast = M > N ? 1 : 0;
-  g.a_mn = a_mn ? 1 : 0;
-  g.b_mn = b_mn ? 1 : 0;
+  g.a_mn = a_form;
+  g.b_mn = b_form;
   g.row_stats = row_stats;
   CUtensorMap mc = ma;       // unused unless g.tma
   if (g.tma) SF_TRY(make_map_c(&mc, C, M, N, ldc));

@@ -83,7 +83,9 @@ def test_gemm_is_deterministic_and_rejects_bad_strides():
 
 @pytest.mark.parametrize("a_layout,b_layout", [(0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("M,N,K", [(300, 520, 200), (64, 40, 8), (129, 257, 72), (2000, 300, 136),
-                                   (1500, 7000, 96)])
+                                   (1500, 7000, 96),
+                                   # M, N multiples of 64: transposed operands load as one 3D box
+                                   (384, 1024, 200), (1024, 640, 72), (2048, 4096, 320)])
 def test_gemm_transposed_layouts(a_layout, b_layout, M, N, K):
     # an operand stored transposed (MN-major: [K][M] or [K][N]) with padded
     # rows; the product is the same as with both operands K-major
