@@ -31,6 +31,7 @@ params all ranks updated divided by the slowest rank's time.
 
 import argparse
 import ctypes
+import contextlib
 import hashlib
 import json
 import os
@@ -664,16 +665,18 @@ def run_lce(args, N=8192, D=4096, V=128256, chunk=4608):
 
     def call():
         native.lce_forward_backward(H, W, y, N, D, V, chunk, -100, loss, dH, dW, ws, wsb, stream)
-    reps = 1 if args.profile_lce else max(3, args.steps // 4)
+    reps = 1 if args.profile_lce else max(5, args.steps // 2)
     for _ in range(1 if args.profile_lce else args.warmup):
         call()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(reps):
-        call()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    clk = Clocks(bus_id_of_current_device())
+    with (contextlib.nullcontext() if args.profile_lce else clk):
+        e0.record(stream)
+        for _ in range(reps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     flops = 6.0 * N * V * D
     peak, kind = measured_peak_bf16()
@@ -683,7 +686,8 @@ def run_lce(args, N=8192, D=4096, V=128256, chunk=4608):
            "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": peak, "unit": "TFLOP/s",
                         "frac": flops / ms / 1e9 / peak, "peak_kind": f"{kind} (of {kind})",
                         "flops_per_call": flops},
-           "logits_bytes_full": N * V * 4, "workspace_bytes": wsb, "loss": float(loss.item())}
+           "logits_bytes_full": N * V * 4, "workspace_bytes": wsb, "loss": float(loss.item()), "calls": reps,
+           "clocks": clk.summary()}
     del H, W, dH, dW, ws
     torch.cuda.empty_cache()
     return out
