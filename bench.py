@@ -606,6 +606,23 @@ def run_lsp(args, matrices=None):
         del wsf_t
     except Exception as ex:
         fit_ms = f"fit step failed: {str(ex)[:120]}"
+    # the second roof of these kernels: gathered multiply-adds per second
+    # with every operand in shared memory (the gather kernels' inner loop alone)
+    gather_rate = None
+    try:
+        nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        sink = torch.empty(nsm * 512, device="cuda")
+        native.sf_bench_gather_rate(nsm, 1024, sink, stream)
+        torch.cuda.synchronize()
+        ra, rb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        iters = 1 << 15
+        ra.record(stream)
+        native.sf_bench_gather_rate(nsm, iters, sink, stream)
+        rb.record(stream)
+        torch.cuda.synchronize()
+        gather_rate = nsm * 512 * iters * 8 / (ra.elapsed_time(rb) / 1e3)
+    except Exception as ex:
+        gather_rate = f"gather-rate probe failed: {str(ex)[:120]}"
     n_params = sum(m * n for (_, m, n, *_r) in mats)
     comp_t = sum(p[2] for p in per) / reps
     ad_t = sum(p[3] for p in per) / reps
@@ -633,6 +650,19 @@ def run_lsp(args, matrices=None):
         g_bytes = sum(m * n * 4 for (_, m, n, *_r) in mats)
         out["fit_step"].update({"G_GBps": g_bytes / fit_ms / 1e6, "frac": g_bytes / fit_ms / 1e6 / peak,
                                 "bytes": "G read once (m n 4 B per matrix) is the algorithmic minimum"})
+    if isinstance(gather_rate, float):
+        # compress: m n k (stage 1 over G) + n d k (stage 2); decompress:
+        # d n k (V = dS Q^T) + m n k (apply); fp32 G at k = 8 is 2 MAC per byte
+        comp_macs = sum(m * n * k + n * d * k for (_, m, n, *_r) in mats)
+        dec_macs = sum(d * n * k + m * n * k for (_, m, n, *_r) in mats)
+        out["gather_roof"] = {
+            "macs_per_s": gather_rate,
+            "as_hbm_fraction": gather_rate / (k / 4) / (peak * 1e9),
+            "compress_frac": comp_macs / (comp_t / 1e3) / gather_rate,
+            "decompress_frac": dec_macs / (dec_t / 1e3) / gather_rate,
+            "probe": "sf_bench_gather_rate: 16 warps per SM, 2 entries + 2 float4 tile loads + 8 FMA per step"}
+    else:
+        out["gather_roof"] = gather_rate
     out["ms_per_chain_all7_graph_streams"] = graph_ms_streams
     out["ms_per_chain_all7_host_moments_window"] = host_ms
     if isinstance(host_ms, float):

@@ -481,6 +481,18 @@ void sf_test_fail_copy_after(int64_t n);
  * it; the context stays usable.  SF_ERR_INVALID for a limit out of range. */
 sf_status sf_test_device_wait_runs_out(int64_t limit_cycles, void* stream);
 
+/* Measurement hook: the shared-memory gather rate that bounds the projector
+ * kernels (compress and decompress are sparse products whose every
+ * multiply-add reads a shared-memory tile row chosen by a projector index).
+ * Launches `ctas` CTAs of 512 threads; each thread runs `iters` steps of the
+ * gather kernels' inner loop (two entries, two 16-byte tile loads at dynamic
+ * rows, 8 fp32 multiply-adds) on shared-memory data only, and writes one
+ * float to sink[cta * 512 + thread] (device, ctas * 512 floats) so the work
+ * is not optimised away.  Multiply-adds done: ctas * 512 * iters * 8; the
+ * caller times the call (CUDA events on `stream`).  SF_ERR_INVALID for
+ * ctas < 1, iters < 1 or a NULL sink. */
+sf_status sf_bench_gather_rate(int32_t ctas, int64_t iters, float* sink, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -27,7 +27,7 @@ EXPORTS = [
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
     "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
-    "sf_gemm_abt_bf16", "sf_gemm_bf16", "lce_workspace_bytes", "lce_forward_backward", "sf_test_device_wait_runs_out",
+    "sf_gemm_abt_bf16", "sf_gemm_bf16", "sf_bench_gather_rate", "lce_workspace_bytes", "lce_forward_backward", "sf_test_device_wait_runs_out",
 ]
 
 
@@ -102,6 +102,7 @@ _SIGS = {
                                      ctypes.c_size_t, _P]),
     "lsp_projector_export_values": (_ST, [_P, _P, _P]),
     "sf_gemm_abt_bf16": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _INT, _P]),
+    "sf_bench_gather_rate": (_ST, [_INT, _I64, _P, _P]),
     "sf_gemm_bf16": (_ST, [_P, _INT, _P, _INT, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _INT, _P]),
     "lce_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
     "sf_test_device_wait_runs_out": (_ST, [_I64, _P]),
@@ -276,6 +277,10 @@ def sf_gemm_abt_bf16(A, B, C, M, N, K, lda, ldb, ldc, alpha=1.0, accumulate=Fals
 def sf_gemm_bf16(A, a_layout, B, b_layout, C, M, N, K, lda, ldb, ldc, alpha=1.0, accumulate=False, stream=None):
     _check(load().sf_gemm_bf16(_addr(A), int(a_layout), _addr(B), int(b_layout), _addr(C), M, N, K, lda, ldb, ldc,
                                float(alpha), int(bool(accumulate)), _stream(stream)))
+
+
+def sf_bench_gather_rate(ctas, iters, sink, stream=None):
+    _check(load().sf_bench_gather_rate(int(ctas), int(iters), _addr(sink), _stream(stream)))
 
 
 def lce_workspace_bytes(n_tokens, d, vocab, chunk):
