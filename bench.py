@@ -399,23 +399,32 @@ def run_e2e(args, world):
 
     from layer_optimizer_gb300 import native, synth
     n_layers = args.layers
-    host = []
+    # each layer's arrays flat in pinned host memory (grad, master, m, v,
+    # weight: one buffer each, the tensors views into it), as flattened
+    # optimizer states are kept; the window then moves each array of a
+    # layer as one copy
+    sizes = [n for _, n in synth.OPT13_LAYER]
+    per_layer = sum(sizes)
+    dtypes = (torch.bfloat16, torch.float32, torch.float32, torch.float32, torch.bfloat16)
+
+    def views(flat):
+        out, o = [], 0
+        for n in sizes:
+            out.append([f[o:o + n] for f in flat])
+            o += n
+        return out
+    host_flat, host = [], []
     for li in range(n_layers):
-        ts = []
-        for ti, (_, n) in enumerate(synth.OPT13_LAYER):
-            g = torch.empty(n, dtype=torch.bfloat16, pin_memory=True)
-            p = torch.empty(n, pin_memory=True)
-            tmpg = synth.fill_normal_(torch.empty(n, dtype=torch.bfloat16, device="cuda"), 1e-3, synth.sub_seed(3, li, ti))
-            tmpp = synth.fill_normal_(torch.empty(n, device="cuda"), 0.02, synth.sub_seed(4, li, ti))
-            g.copy_(tmpg)
-            p.copy_(tmpp)
-            ts.append([g, p, torch.zeros(n, pin_memory=True), torch.zeros(n, pin_memory=True),
-                       torch.empty(n, dtype=torch.bfloat16, pin_memory=True)])
+        flat = [torch.zeros(per_layer, dtype=dt, pin_memory=True) for dt in dtypes]
+        ts = views(flat)
+        for ti, n in enumerate(sizes):
+            ts[ti][0].copy_(synth.fill_normal_(torch.empty(n, dtype=torch.bfloat16, device="cuda"), 1e-3,
+                                               synth.sub_seed(3, li, ti)))
+            ts[ti][1].copy_(synth.fill_normal_(torch.empty(n, device="cuda"), 0.02, synth.sub_seed(4, li, ti)))
+        host_flat.append(flat)
         host.append(ts)
-    caps = [n for _, n in synth.OPT13_LAYER]
-    slots = [[[torch.empty(c, dtype=torch.bfloat16, device="cuda"), torch.empty(c, device="cuda"),
-               torch.empty(c, device="cuda"), torch.empty(c, device="cuda"),
-               torch.empty(c, dtype=torch.bfloat16, device="cuda")] for c in caps] for _ in range(2)]
+    slot_flat = [[torch.empty(per_layer, dtype=dt, device="cuda") for dt in dtypes] for _ in range(2)]
+    slots = [views(f) for f in slot_flat]
     streams = [torch.cuda.Stream() for _ in range(3)]
     win = native.sf_window_create([[native.make_tensor(*t) for t in s] for s in slots], *streams)
     hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in host])
@@ -429,16 +438,13 @@ def run_e2e(args, world):
     # engine, no kernel, no events): the link rate these buffers allow
     torch.cuda.synchronize()
     tr = time.perf_counter()
-    for li, L in enumerate(host):
-        sl = slots[li % 2]
+    for li, F in enumerate(host_flat):
         with torch.cuda.stream(streams[0]):
-            for h, dv in zip(L, sl):
-                for k in range(4):
-                    dv[k][:h[k].numel()].copy_(h[k], non_blocking=True)
+            for k in range(4):
+                slot_flat[li % 2][k].copy_(F[k], non_blocking=True)
         with torch.cuda.stream(streams[2]):
-            for h, dv in zip(L, slots[(li + 1) % 2]):
-                for k in (1, 2, 3, 4):
-                    h[k].copy_(dv[k][:h[k].numel()], non_blocking=True)
+            for k in (1, 2, 3, 4):
+                F[k].copy_(slot_flat[(li + 1) % 2][k], non_blocking=True)
     torch.cuda.synchronize()
     raw_s = time.perf_counter() - tr
     barrier(world)
@@ -450,7 +456,7 @@ def run_e2e(args, world):
     barrier(world)
     params = n_layers * synth.layer_numel(synth.OPT13_LAYER)
     win.close()
-    del host, slots
+    del host, slots, host_flat, slot_flat
     torch.cuda.empty_cache()
     return dict(wall_s=wall, params_per_step=params, h2d=14 * params, d2h=14 * params,
                 raw_copy_GBps_each_way=14 * params / raw_s / 1e9)

@@ -362,6 +362,10 @@ sf_status lsp_projector_export_values(lsp_projector p, float* val, void* stream)
  *   d2h:     wait for the update; copy master, exp_avg, exp_avg_sq and
  *            weight (if the host layer has one) back to layer l; the slot is
  *            free again when these copies end.
+ * Copies are issued per array (grad, master, exp_avg, exp_avg_sq, weight):
+ * consecutive tensors whose host arrays and slot arrays both follow one
+ * another in memory move as one copy (a layer kept as flat per-array
+ * buffers moves as one copy per array); the bytes moved are the same.
  * Host-layer pointers must be pinned (page-locked) host memory.  The call
  * returns when everything is enqueued; `steps` (int64 [n_layers], host) is
  * updated on return.  Host buffers of a layer must not be touched until its

@@ -67,6 +67,49 @@ sf_status copy_async(void* dst, const void* src, size_t bytes, cudaMemcpyKind ki
   return e == cudaSuccess ? SF_OK : sf::cuda_fail(e, what);
 }
 
+// The arrays of a tensor that move over the link.
+enum Part { kGrad, kMaster, kExpAvg, kExpAvgSq, kWeight };
+
+inline void* part_ptr(const sf_tensor& t, Part k) {
+  switch (k) {
+    case kGrad: return const_cast<void*>(t.grad);
+    case kMaster: return t.master;
+    case kExpAvg: return t.exp_avg;
+    case kExpAvgSq: return t.exp_avg_sq;
+    default: return t.weight;
+  }
+}
+inline size_t part_bytes(Part k) { return (k == kGrad || k == kWeight) ? 2 : 4; }
+
+// Copies array `k` of tensors [t0, t1) between the host layer and the slot.
+// Tensors whose host arrays and slot arrays both follow one another in
+// memory (a layer kept as flat per-array buffers, as flattened optimizer
+// states are) move as one copy: one descriptor instead of one per tensor.
+// A tensor without that array (a NULL weight) ends a run and is skipped.
+sf_status copy_runs(const sf_host_layer& L, const std::vector<sf_tensor>& slot, int t0, int t1, Part k,
+                    cudaMemcpyKind kind, cudaStream_t s, const char* what) {
+  const size_t es = part_bytes(k);
+  int t = t0;
+  while (t < t1) {
+    char* h = static_cast<char*>(part_ptr(L.tensors[t], k));
+    char* d = static_cast<char*>(part_ptr(slot[t], k));
+    if (!h) {
+      ++t;
+      continue;
+    }
+    size_t bytes = es * (size_t)L.tensors[t].numel;
+    int u = t + 1;
+    while (u < t1 && part_ptr(L.tensors[u], k) == h + bytes && part_ptr(slot[u], k) == d + bytes) {
+      bytes += es * (size_t)L.tensors[u].numel;
+      ++u;
+    }
+    if (kind == cudaMemcpyHostToDevice) SF_TRY(copy_async(d, h, bytes, kind, s, what));
+    else SF_TRY(copy_async(h, d, bytes, kind, s, what));
+    t = u;
+  }
+  return SF_OK;
+}
+
 void destroy_events(sf_window_s* w) {
   for (auto* v : {&w->ev_in, &w->ev_done, &w->ev_free, &w->ev_layer})
     for (cudaEvent_t e : *v)
@@ -198,15 +241,10 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
         if (e >= 0 && e != last) SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_free[e], 0), "wait slot tensor free");
         last = e;
       }
-      for (int t = t0; t < t1; ++t) {
-        const sf_tensor& h = L.tensors[t];
-        const size_t n = (size_t)h.numel;
-        SF_TRY(copy_async(const_cast<void*>(slot[t].grad), h.grad, 2 * n, cudaMemcpyHostToDevice, w->h2d, "h2d grad"));
-        SF_TRY(copy_async(slot[t].master, h.master, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d master"));
-        SF_TRY(copy_async(slot[t].exp_avg, h.exp_avg, 4 * n, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg"));
-        SF_TRY(copy_async(slot[t].exp_avg_sq, h.exp_avg_sq, 4 * n, cudaMemcpyHostToDevice, w->h2d,
-                          "h2d exp_avg_sq"));
-      }
+      SF_TRY(copy_runs(L, slot, t0, t1, kGrad, cudaMemcpyHostToDevice, w->h2d, "h2d grad"));
+      SF_TRY(copy_runs(L, slot, t0, t1, kMaster, cudaMemcpyHostToDevice, w->h2d, "h2d master"));
+      SF_TRY(copy_runs(L, slot, t0, t1, kExpAvg, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg"));
+      SF_TRY(copy_runs(L, slot, t0, t1, kExpAvgSq, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg_sq"));
       SF_CUDA_TRY(cudaEventRecord(w->ev_in[eb + t0], w->h2d), "record ev_in");
 
       // compute: the fused update of the group
@@ -221,16 +259,10 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
 
       // d2h: write the group back; each tensor of the slot is free when its copies end
       SF_CUDA_TRY(cudaStreamWaitEvent(w->d2h, w->ev_done[eb + t0], 0), "wait ev_done");
-      for (int t = t0; t < t1; ++t) {
-        const sf_tensor& h = L.tensors[t];
-        const size_t n = (size_t)h.numel;
-        SF_TRY(copy_async(h.master, slot[t].master, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h master"));
-        SF_TRY(copy_async(h.exp_avg, slot[t].exp_avg, 4 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg"));
-        SF_TRY(copy_async(h.exp_avg_sq, slot[t].exp_avg_sq, 4 * n, cudaMemcpyDeviceToHost, w->d2h,
-                          "d2h exp_avg_sq"));
-        if (h.weight)
-          SF_TRY(copy_async(h.weight, slot[t].weight, 2 * n, cudaMemcpyDeviceToHost, w->d2h, "d2h weight"));
-      }
+      SF_TRY(copy_runs(L, slot, t0, t1, kMaster, cudaMemcpyDeviceToHost, w->d2h, "d2h master"));
+      SF_TRY(copy_runs(L, slot, t0, t1, kExpAvg, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg"));
+      SF_TRY(copy_runs(L, slot, t0, t1, kExpAvgSq, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg_sq"));
+      SF_TRY(copy_runs(L, slot, t0, t1, kWeight, cudaMemcpyDeviceToHost, w->d2h, "d2h weight"));
       SF_CUDA_TRY(cudaEventRecord(w->ev_free[eb + t0], w->d2h), "record ev_free");
       for (int t = t0; t < t1; ++t) w->free_ev[eb + t] = eb + t0;
       t0 = t1;

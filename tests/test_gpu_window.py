@@ -196,3 +196,55 @@ def test_invalid_visits_rejected_before_enqueue():
         native.sf_slide_window_step(win, hl, [1], native.hparams(**HP), steps)
     assert steps[0] == 0
     win.close()
+
+
+def _flat_layer(sizes, seed, no_weight=()):
+    """A layer kept as one pinned buffer per array, the tensors views into it."""
+    tot = sum(sizes)
+    flat = [torch.zeros(tot, dtype=dt).pin_memory()
+            for dt in (torch.bfloat16, torch.float32, torch.float32, torch.float32, torch.bfloat16)]
+    out, o = [], 0
+    for i, n in enumerate(sizes):
+        t = [f[o:o + n] for f in flat]
+        t[0].copy_(synth.normal((n,), 1e-3, synth.sub_seed(seed, 0, i), dtype=torch.bfloat16))
+        t[1].copy_(synth.normal((n,), 0.02, synth.sub_seed(seed, 1, i)))
+        if i in no_weight:
+            t[4] = None
+        out.append(t)
+        o += n
+    return out
+
+
+def test_window_flat_layers_copy_as_runs_bitwise():
+    # contiguous host arrays and contiguous slot arrays move as one copy per
+    # run; a missing weight and a slot tensor with spare capacity end runs
+    sizes = [4099, 17, 65536, 3, 1024]
+    layers = [_flat_layer(sizes, 200 + l, no_weight=(2,) if l == 1 else ()) for l in range(3)]
+    ref_in = [[[x.clone() if x is not None else None for x in t] for t in L] for L in layers]
+    caps = list(sizes)
+    caps[3] = 8                                     # spare capacity: tensors 3 and 4 are not adjacent in the slot
+    slots = []
+    for _ in range(2):
+        flat = [torch.empty(sum(caps), dtype=dt, device=DEV)
+                for dt in (torch.bfloat16, torch.float32, torch.float32, torch.float32, torch.bfloat16)]
+        sl, o = [], 0
+        for c in caps:
+            sl.append([f[o:o + c] for f in flat])
+            o += c
+        slots.append(sl)
+    order = [0, 1, 2, 1, 0, 2, 2]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = _window(slots, streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in layers])
+    steps = (ctypes.c_int64 * 3)()
+    native.sf_slide_window_step(win, hl, order, native.hparams(**HP), steps)
+    win.sync()
+    ref, ref_steps = _resident_reference(ref_in, order)
+    assert list(steps) == ref_steps
+    for L, R in zip(layers, ref):
+        for t, r in zip(L, R):
+            for k in (1, 2, 3):
+                assert torch.equal(t[k].view(torch.int32), r[k].cpu().view(torch.int32))
+            if t[4] is not None:
+                assert torch.equal(t[4].view(torch.int16), r[4].cpu().view(torch.int16))
+    win.close()
