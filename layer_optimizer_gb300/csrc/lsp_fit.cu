@@ -22,8 +22,9 @@ using sf::fail;
 //   dL/dQ[j,b] = -2 ( <U[j,:], (S + C)^T[b,:]> - sum_t Q[j,b_t] (S^T A_P S)[b_t, b] )
 //   L = ||G||^2 - 2 ||S||^2 + <A_P S, S A_Q>
 // so the m x n error E is never formed: the step needs the compress pair
-// (U, then S), one more gather for T over G^T, the two d x d Gram matrices,
-// five d x d products, and per-row dot products at the k stored positions.
+// (U, then S), one more gather for T over G^T, the two d x d Gram matrices
+// (from the sparse forms), five d x d products, and per-row dot products at
+// the k stored positions.
 namespace sf {
 namespace {
 
@@ -67,14 +68,96 @@ __global__ void __launch_bounds__(256) k_transpose_sumsq(const TB* __restrict__ 
   }
 }
 
-// Dense copy of a projector, out[i][c] = sum of row i's values with id c
-// (entries in ELL order; `out` zero-filled beforehand).  The Gram matrix
-// P^T P is then the gather of this m x d matrix with P itself.
-__global__ void k_densify(const int32_t* __restrict__ ell_idx, const float* __restrict__ ell_val, int64_t rows,
-                          int k, int d, float* __restrict__ out) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= rows) return;
-  for (int t = 0; t < k; ++t) out[i * d + ell_idx[i * k + t]] += ell_val[i * k + t];
+// Gram matrix A = X^T X of a projector X (rows x d, k entries per row),
+// straight from its sparse form: row a of A is the sum, over the entries
+// (i, v) of column a (rows ascending), of v times row i of X, i.e. of
+// v * x_t at column id_t for the k entries (id_t, x_t) of row i.  Four
+// warps per output row, each over a quarter of column a's entries into its
+// own shared-memory row; the quarters are then added in order.  In a warp
+// the lanes split into R = 32 / k row groups of k slots (one group of 32
+// slots per pass when k > 32); each lane loads its (entry, slot) pair for
+// kGramB batches of R rows at once (independent loads), then the rows are
+// applied one after another: a row's slots hit distinct output columns, so
+// its lanes add at once.  A batch in which some row repeats an id
+// (possible without validation) is applied slot by slot by the lanes that
+// own the output columns.  Every sum runs in a fixed order; m k^2
+// multiply-adds in all instead of the m d k of a gather over a dense copy.
+constexpr int kGramWarps = 8, kGramSplit = 4, kGramB = 8;
+__global__ void __launch_bounds__(32 * kGramWarps) k_gram_sparse(const int32_t* __restrict__ col_ptr,
+                                                                 const int32_t* __restrict__ row_idx,
+                                                                 const float* __restrict__ csc_val,
+                                                                 const int32_t* __restrict__ ell_idx,
+                                                                 const float* __restrict__ ell_val, int k, int d,
+                                                                 float* __restrict__ A) {
+  extern __shared__ float gram_rows[];   // [kGramWarps][d]: one partial row per warp
+  const unsigned kAll = 0xffffffffu;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp % kGramSplit;
+  const int a = blockIdx.x * (kGramWarps / kGramSplit) + warp / kGramSplit;
+  float* rb = gram_rows + (size_t)warp * d;
+  for (int c = lane; c < d; c += 32) rb[c] = 0.0f;
+  __syncwarp();
+  if (a < d) {
+    const int S = k < 32 ? k : 32;       // slots per row group and pass
+    const int R = 32 / S;                // rows per batch
+    const int r_l = lane / S, t_l = lane % S;
+    const int c0 = col_ptr[a], len = col_ptr[a + 1] - c0;
+    const int e0 = c0 + (int)((int64_t)len * quarter / kGramSplit);
+    const int e1 = c0 + (int)((int64_t)len * (quarter + 1) / kGramSplit);
+    for (int eb0 = e0; eb0 < e1; eb0 += R * kGramB) {
+      for (int t0 = 0; t0 < k; t0 += S) {
+        int bq[kGramB];
+        float vq[kGramB], xq[kGramB];
+#pragma unroll
+        for (int q = 0; q < kGramB; ++q) {
+          const int e = eb0 + q * R + r_l, t = t0 + t_l;
+          bq[q] = 0;
+          vq[q] = 0.0f;
+          xq[q] = 0.0f;
+          if (r_l < R && e < e1 && t < k) {
+            const int64_t i = row_idx[e];
+            vq[q] = csc_val[e];
+            bq[q] = ell_idx[i * k + t];
+            xq[q] = ell_val[i * k + t];
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kGramB; ++q) {
+          const int eq = eb0 + q * R;
+          if (eq >= e1) break;           // uniform
+          const bool on = r_l < R && eq + r_l < e1 && t0 + t_l < k;
+          // a repeated id inside a row of this batch: same (row, id) key
+          const unsigned on_mask = __ballot_sync(kAll, on);
+          unsigned peers = 0;
+          if (on) peers = __match_any_sync(on_mask, (r_l << 26) | bq[q]);
+          if (!__any_sync(kAll, on && __popc(peers) > 1)) {
+            for (int r = 0; r < R && eq + r < e1; ++r) {
+              if (on && r_l == r) rb[bq[q]] = fmaf(vq[q], xq[q], rb[bq[q]]);
+              __syncwarp();
+            }
+          } else {
+            for (int j = 0; j < 32; ++j) {
+              if (!((on_mask >> j) & 1u)) continue;   // uniform
+              const int bj = __shfl_sync(kAll, bq[q], j);
+              const float vj = __shfl_sync(kAll, vq[q], j), xj = __shfl_sync(kAll, xq[q], j);
+              if (lane == (bj & 31)) rb[bj] = fmaf(vj, xj, rb[bj]);
+              __syncwarp();
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (a < d && quarter == 0) {
+    const float* p0 = rb;
+    for (int c = lane; c < d; c += 32) {
+      float s = p0[c];
+#pragma unroll
+      for (int h = 1; h < kGramSplit; ++h) s += p0[(size_t)h * d + c];
+      A[(int64_t)a * d + c] = s;
+    }
+  }
 }
 
 // C = op(A) op(B) for d x d fp32 row-major matrices, op = identity or
@@ -359,8 +442,8 @@ constexpr int kCombineBlocks = 128;
 
 struct FitPlan {
   CompressPlan cp;
-  GatherPlan gt, gram_p, gram_q;
-  size_t off_gt, off_t, off_tp, off_dd, off_gp, off_gq, off_g2, off_part, off_dense, off_gramp, bytes;
+  GatherPlan gt;
+  size_t off_gt, off_t, off_tp, off_dd, off_gp, off_gq, off_g2, off_part, bytes;
   int64_t n_g2;
 };
 
@@ -386,12 +469,6 @@ FitPlan plan_fit(int64_t m, int64_t n, int d, size_t es, int kP, int kQ) {
   off = align_up(off + (size_t)f.n_g2 * 8, 256);
   f.off_part = off;
   off = align_up(off + (size_t)kCombineBlocks * 2 * 8, 256);
-  f.gram_p = plan_gather(m, d, d);
-  f.gram_q = plan_gather(n, d, d);
-  f.off_dense = off;
-  off = align_up(off + (size_t)std::max(m, n) * d * 4, 256);
-  f.off_gramp = off;
-  off = align_up(off + (size_t)std::max(f.gram_p.splits, f.gram_q.splits) * d * d * 4, 256);
   f.bytes = off;
   return f;
 }
@@ -464,18 +541,17 @@ sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G
   }
   SF_TRY(sf::launch_gather<float>(Q, U, d, d, f.cp.g2, S, Sp, s));
 
-  // Gram matrices (P^T P as the gather of a dense copy of P with P; same for
-  // Q, reusing the buffer) and the five d x d products
-  float* dense = reinterpret_cast<float*>(w + f.off_dense);
-  float* gram_part = reinterpret_cast<float*>(w + f.off_gramp);
-  SF_CUDA_TRY(cudaMemsetAsync(dense, 0, (size_t)m * d * 4, s), "clear dense P");
-  sf::k_densify<<<(unsigned)ceil_div<int64_t>(m, 256), 256, 0, s>>>(P->ell_idx, P->ell_val, m, P->k, d, dense);
-  SF_TRY(sf::check_launch("k_densify"));
-  SF_TRY(sf::launch_gather<float>(P, dense, d, d, f.gram_p, AP, gram_part, s));
-  SF_CUDA_TRY(cudaMemsetAsync(dense, 0, (size_t)n * d * 4, s), "clear dense Q");
-  sf::k_densify<<<(unsigned)ceil_div<int64_t>(n, 256), 256, 0, s>>>(Q->ell_idx, Q->ell_val, n, Q->k, d, dense);
-  SF_TRY(sf::check_launch("k_densify"));
-  SF_TRY(sf::launch_gather<float>(Q, dense, d, d, f.gram_q, AQ, gram_part, s));
+  // Gram matrices A_P = P^T P, A_Q = Q^T Q from the sparse forms, then the
+  // five d x d products
+  const size_t gram_smem = (size_t)sf::kGramWarps * d * 4;
+  SF_TRY(sf::allow_dynamic_smem(reinterpret_cast<const void*>(&sf::k_gram_sparse), gram_smem));
+  const unsigned gram_grid = (unsigned)ceil_div(d, sf::kGramWarps / sf::kGramSplit);
+  sf::k_gram_sparse<<<gram_grid, 32 * sf::kGramWarps, gram_smem, s>>>(P->col_ptr, P->row_idx, P->csc_val,
+                                                                       P->ell_idx, P->ell_val, P->k, d, AP);
+  SF_TRY(sf::check_launch("k_gram_sparse"));
+  sf::k_gram_sparse<<<gram_grid, 32 * sf::kGramWarps, gram_smem, s>>>(Q->col_ptr, Q->row_idx, Q->csc_val,
+                                                                       Q->ell_idx, Q->ell_val, Q->k, d, AQ);
+  SF_TRY(sf::check_launch("k_gram_sparse"));
   const unsigned tiles = (unsigned)ceil_div(d, 64);
   sf::DdBatch b1{};
   b1.d = d;

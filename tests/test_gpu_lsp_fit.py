@@ -94,6 +94,28 @@ def test_fit_step_matches_oracle(m, n, d, k, g_dtype):
     check_close("apply after the step", W, -D, D_abs, TOL_LSP)
 
 
+@pytest.mark.parametrize("k", [4, 40])
+def test_fit_step_with_repeated_ids(k):
+    # projectors built without validation may repeat an id inside a row (the
+    # values then add up); k = 40 also takes the Gram matrices' multi-pass path
+    m, n, d = 300, 200, 64
+    hPQ = []
+    for rows, seed in ((m, 131), (n, 137)):
+        idx, val = synth.projector(rows, d, k, seed)
+        idx[::7, 1] = idx[::7, 0]                 # every 7th row repeats its first id
+        idx[::11, k - 1] = idx[::11, 1]
+        h = native.lsp_projector_create(rows, d, k, torch.from_numpy(idx).to(DEV), torch.from_numpy(val).to(DEV),
+                                        validate=False)
+        hPQ.append((h, ol.Projector(idx, val, d)))
+    (hP, P), (hQ, Q) = hPQ
+    G, G64 = _gradient(m, n, native.SF_FP32, 141)
+    loss, gP, gQ = _fit(hP, hQ, G, native.SF_FP32, m, n, d, 1e-3)
+    ref = of.fit_step(G64, P, Q, 1e-3)
+    assert abs(loss - ref["loss"]) <= TOL_LSP * ref["loss_abs"], (loss, ref["loss"], ref["loss_abs"])
+    check_close("dL/dP", gP, ref["gP"], ref["gP_abs"], TOL_LSP)
+    check_close("dL/dQ", gQ, ref["gQ"], ref["gQ_abs"], TOL_LSP)
+
+
 def test_fit_steps_descend_and_are_deterministic():
     m, n, d, k = 512, 384, 64, 4
     hP, P = _make(m, d, k, 3)
