@@ -490,6 +490,83 @@ __global__ void k_gather_generic(const TB* __restrict__ B, int64_t ldb, int64_t 
   yt[col * d + a] = acc;
 }
 
+// Second compress stage when the dense operand is small and L2-resident
+// (B = R^T, n x d fp32, just written by stage 1):
+//   yt[c][a] = sum over the entries (j, q) of column a of A (rows ascending)
+//              of q * B[j][c]
+// One warp per output column a and 128-column slice of B: the warp fetches
+// 32 entries at a time (one per lane), broadcasts them in order, and each
+// lane reads 4 consecutive columns of row j (16-byte loads, eight rows in
+// flight), so B is read straight from L2 with no staging and no split
+// partials.  The CTA's 8 outputs are transposed through shared memory so
+// yt is written as 32-byte row segments.  Needs B 16-byte aligned with
+// ldb and ncols multiples of 4 (every 16-byte load inside a row).
+constexpr int kRgWarps = 8, kRgCols = 128, kRgUnroll = 8;
+__global__ void __launch_bounds__(32 * kRgWarps) k_rowgather(const float* __restrict__ B, int64_t ldb, int ncols,
+                                                             const int32_t* __restrict__ col_ptr,
+                                                             const int32_t* __restrict__ row_idx,
+                                                             const float* __restrict__ csc_val, int d,
+                                                             float* __restrict__ yt) {
+  __shared__ float tile[kRgWarps][kRgCols + 4];
+  griddep_launch_dependents();
+  griddep_wait();                // B is the previous kernel's output
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int a0 = blockIdx.x * kRgWarps, a = a0 + warp;
+  const int c0 = blockIdx.y * kRgCols, c = c0 + 4 * lane;
+  const bool col_on = c < ncols;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (a < d) {
+    const int e0 = col_ptr[a], e1 = col_ptr[a + 1];
+    for (int eb = e0; eb < e1; eb += 32) {
+      int jl = 0;
+      float ql = 0.0f;
+      if (eb + lane < e1) {
+        jl = row_idx[eb + lane];
+        ql = csc_val[eb + lane];
+      }
+      const int cnt = min(32, e1 - eb);
+      int t = 0;
+      for (; t + kRgUnroll <= cnt; t += kRgUnroll) {
+        float4 x[kRgUnroll];
+        float q[kRgUnroll];
+#pragma unroll
+        for (int u = 0; u < kRgUnroll; ++u) {
+          const int j = __shfl_sync(0xffffffffu, jl, t + u);
+          q[u] = __shfl_sync(0xffffffffu, ql, t + u);
+          x[u] = col_on ? *reinterpret_cast<const float4*>(B + (int64_t)j * ldb + c)
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int u = 0; u < kRgUnroll; ++u) {
+          acc.x = fmaf(q[u], x[u].x, acc.x);
+          acc.y = fmaf(q[u], x[u].y, acc.y);
+          acc.z = fmaf(q[u], x[u].z, acc.z);
+          acc.w = fmaf(q[u], x[u].w, acc.w);
+        }
+      }
+      for (; t < cnt; ++t) {
+        const int j = __shfl_sync(0xffffffffu, jl, t);
+        const float q = __shfl_sync(0xffffffffu, ql, t);
+        const float4 x = col_on ? *reinterpret_cast<const float4*>(B + (int64_t)j * ldb + c)
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        acc.x = fmaf(q, x.x, acc.x);
+        acc.y = fmaf(q, x.y, acc.y);
+        acc.z = fmaf(q, x.z, acc.z);
+        acc.w = fmaf(q, x.w, acc.w);
+      }
+    }
+  }
+  tile[warp][4 * lane] = acc.x;
+  tile[warp][4 * lane + 1] = acc.y;
+  tile[warp][4 * lane + 2] = acc.z;
+  tile[warp][4 * lane + 3] = acc.w;
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < kRgCols * kRgWarps; idx += blockDim.x) {
+    const int cc = idx / kRgWarps, w = idx % kRgWarps;
+    if (c0 + cc < ncols && a0 + w < d) yt[(int64_t)(c0 + cc) * d + a0 + w] = tile[w][cc];
+  }
+}
+
 // out[e] = sum over splits s = 0, 1, ... of part[s][e], in that order.
 __global__ void k_reduce_splits(const float* __restrict__ part, int splits, int64_t stride, int64_t n,
                                 float* __restrict__ out) {
@@ -1218,6 +1295,19 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   return SF_OK;
 }
 
+// Y^T = (A^T B)^T for a small L2-resident B (the second compress stage):
+// k_rowgather when B's rows are 16-byte aligned, else the staged gather.
+sf_status launch_stage2(const lsp_projector_s* Aproj, const float* B, int64_t ldb, int64_t ncols, const GatherPlan& p,
+                        float* yt_final, float* yt_partial, cudaStream_t stream) {
+  if ((reinterpret_cast<uintptr_t>(B) % 16) != 0 || ldb % 4 != 0 || ncols % 4 != 0 || ncols > INT32_MAX)
+    return launch_gather<float>(Aproj, B, ldb, ncols, p, yt_final, yt_partial, stream);
+  const dim3 grid((unsigned)ceil_div(Aproj->d, kRgWarps), (unsigned)ceil_div<int64_t>(ncols, kRgCols));
+  SF_CUDA_TRY(launch_pdl(k_rowgather, grid, dim3(32 * kRgWarps), 0, stream, B, ldb, (int)ncols, Aproj->col_ptr,
+                         Aproj->row_idx, Aproj->csc_val, Aproj->d, yt_final),
+              "launch k_rowgather");
+  return SF_OK;
+}
+
 sf_status check_proj(const lsp_projector_s* p, const char* name) {
   if (!p) return fail(SF_ERR_INVALID, "projector %s is NULL", name);
   int dev = 0;
@@ -1407,7 +1497,7 @@ sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G, sf_dtype
     SF_TRY(sf::launch_gather<float>(P, static_cast<const float*>(G), n, n, cp.g1, rt, rtp, s));
   else
     SF_TRY(sf::launch_gather<__nv_bfloat16>(P, static_cast<const __nv_bfloat16*>(G), n, n, cp.g1, rt, rtp, s));
-  return sf::launch_gather<float>(Q, rt, d, d, cp.g2, S, sp, s);
+  return sf::launch_stage2(Q, rt, d, d, cp.g2, S, sp, s);
 }
 
 }  // extern "C"

@@ -539,7 +539,7 @@ sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G
     SF_TRY(sf::check_launch("k_transpose_sumsq"));
     SF_TRY(sf::launch_gather<__nv_bfloat16>(Q, static_cast<const __nv_bfloat16*>(Gt), m, m, f.gt, T, Tp, s));
   }
-  SF_TRY(sf::launch_gather<float>(Q, U, d, d, f.cp.g2, S, Sp, s));
+  SF_TRY(sf::launch_stage2(Q, U, d, d, f.cp.g2, S, Sp, s));
 
   // Gram matrices A_P = P^T P, A_Q = Q^T Q from the sparse forms, then the
   // five d x d products

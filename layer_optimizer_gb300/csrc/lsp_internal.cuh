@@ -61,6 +61,12 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
                         float* yt_final, float* yt_partial, cudaStream_t stream);
 
 // SF_ERR_INVALID unless p is a projector built on the current device.
+// Second compress stage, Y^T = (A^T B)^T for a small L2-resident fp32 B:
+// a row gather straight from L2 when B's rows are 16-byte aligned, else
+// launch_gather (plan p, partials yt_partial).
+sf_status launch_stage2(const lsp_projector_s* Aproj, const float* B, int64_t ldb, int64_t ncols, const GatherPlan& p,
+                        float* yt_final, float* yt_partial, cudaStream_t stream);
+
 sf_status check_proj(const lsp_projector_s* p, const char* name);
 
 }  // namespace sf

@@ -80,6 +80,7 @@ COMPRESS_CASES = [
     (260, 136, 200, 3, torch.bfloat16),   # d = 200: 2-CTA clusters, ragged a-range
     (150, 96, 300, 5, torch.float32),     # d = 300: 3 a-ranges, no multicast
     (129, 64, 12, 3, torch.float32),      # d not a multiple of 8
+    (50, 40, 30, 3, torch.float32),       # d not a multiple of 4: stage 2 as the staged gather
 ]
 
 
