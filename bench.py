@@ -9,7 +9,7 @@ layers, with t advancing per step.  Metric: params updated per second.
 
 Also on the same line:
   e2e        the same step through the layer-sliding window: the 24 layers
-             live in pinned host memory and stream through 2 device slots
+             live in pinned host memory and stream through 3 device slots
              (h2d grad/master/m/v, update, d2h master/m/v/weight), copies
              inside the timed region.
   roofline   of the dominant kernel (the fused AdamW), from CUDA events
@@ -423,7 +423,10 @@ def run_e2e(args, world):
             ts[ti][1].copy_(synth.fill_normal_(torch.empty(n, device="cuda"), 0.02, synth.sub_seed(4, li, ti)))
         host_flat.append(flat)
         host.append(ts)
-    slot_flat = [[torch.empty(per_layer, dtype=dt, device="cuda") for dt in dtypes] for _ in range(2)]
+    # three device slots: a layer's update and write-back, the next layer's
+    # copy in and a third layer's copy in can all be in flight (0.8 GB each)
+    n_slots = 3
+    slot_flat = [[torch.empty(per_layer, dtype=dt, device="cuda") for dt in dtypes] for _ in range(n_slots)]
     slots = [views(f) for f in slot_flat]
     streams = [torch.cuda.Stream() for _ in range(3)]
     win = native.sf_window_create([[native.make_tensor(*t) for t in s] for s in slots], *streams)
@@ -441,10 +444,10 @@ def run_e2e(args, world):
     for li, F in enumerate(host_flat):
         with torch.cuda.stream(streams[0]):
             for k in range(4):
-                slot_flat[li % 2][k].copy_(F[k], non_blocking=True)
+                slot_flat[li % n_slots][k].copy_(F[k], non_blocking=True)
         with torch.cuda.stream(streams[2]):
             for k in (1, 2, 3, 4):
-                F[k].copy_(slot_flat[(li + 1) % 2][k], non_blocking=True)
+                F[k].copy_(slot_flat[(li + 1) % n_slots][k], non_blocking=True)
     torch.cuda.synchronize()
     raw_s = time.perf_counter() - tr
     barrier(world)
@@ -950,7 +953,7 @@ def main_ours(args, rank, world):
         wall = max_over_ranks(e["wall_s"], world)
         line["e2e"] = {"value": world * e["params_per_step"] * args.steps / wall, "unit": "params/s",
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "path": "sf_slide_window_step: 24 pinned host layers, 2 device slots, 3 streams",
+                       "path": "sf_slide_window_step: 24 pinned host layers (flat per-array buffers), 3 device slots, 3 streams",
                        "link_GBps_each_way": e["h2d"] * args.steps / wall / 1e9,
                        "same_buffers_plain_copies_GBps_each_way": e["raw_copy_GBps_each_way"]}
         try:
