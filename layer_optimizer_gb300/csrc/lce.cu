@@ -174,7 +174,10 @@ struct LcePlan {
   size_t off_z, off_g, off_lse, off_rowloss, off_n, off_stats, bytes;
 };
 
-LcePlan plan_lce(int64_t N, int64_t D, int64_t V, int64_t chunk) {
+// Workspace of one call: the chunk's logits and gradient, its row statistics,
+// the row losses of all tokens, the labelled-token count (no dependence on D:
+// nothing is transposed).
+LcePlan plan_lce(int64_t N, int64_t V, int64_t chunk) {
   LcePlan p;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -207,7 +210,7 @@ extern "C" {
 
 size_t lce_workspace_bytes(int64_t n_tokens, int64_t d, int64_t vocab, int64_t chunk) {
   if (n_tokens < 1 || d < 1 || vocab < 1 || chunk < 1) return 0;
-  return sf::plan_lce(n_tokens, d, vocab, std::min(chunk, (n_tokens + 7) / 8 * 8)).bytes;
+  return sf::plan_lce(n_tokens, vocab, std::min(chunk, (n_tokens + 7) / 8 * 8)).bytes;
 }
 
 sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labels, int64_t N, int64_t D, int64_t V,
@@ -226,7 +229,7 @@ sf_status lce_forward_backward(const void* H, const void* W, const int32_t* labe
   chunk = std::min(chunk, (N + 7) / 8 * 8);
   if (V > (int64_t)INT32_MAX / 2 || N > (int64_t)INT32_MAX || D > (int64_t)INT32_MAX / 2)
     return sf::fail(SF_ERR_UNSUPPORTED, "sizes too large");
-  const sf::LcePlan p = sf::plan_lce(N, D, V, chunk);
+  const sf::LcePlan p = sf::plan_lce(N, V, chunk);
   if (!ws || ws_bytes < p.bytes || (reinterpret_cast<uintptr_t>(ws) % 256))
     return sf::fail(SF_ERR_INVALID, "workspace needs %zu bytes, 256-byte aligned (got %zu)", p.bytes, ws_bytes);
   cudaStream_t s = sf::as_stream(stream_);
