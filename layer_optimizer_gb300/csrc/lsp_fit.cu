@@ -225,37 +225,46 @@ __global__ void __launch_bounds__(256) k_gemm_dd(const __grid_constant__ DdBatch
     }
 }
 
-// The same products when d is a multiple of 64: the k-slab of 32 of op(A)
-// and op(B) is staged k-major in shared memory from 16-byte global loads
-// (the next slab's loads in flight while the current one is used), and each
-// thread reads its 4 rows and 4 columns with one 16-byte load each per k.
-// Same order of the sums as k_gemm_dd.
-__global__ void __launch_bounds__(256) k_gemm_dd64(const __grid_constant__ DdBatch bt) {
+// The same products when d is a multiple of 64: a TM x 64 output tile per
+// block (TM = 32: twice the blocks of 64 x 64 tiles, so the d x d products
+// of the fit step spread over all SMs), 4 x 4 outputs per thread.  The
+// k-slab of 32 of op(A) and op(B) is staged k-major in shared memory from
+// 16-byte global loads (the next slab's loads in flight while the current
+// one is used), and each thread reads its 4 rows and 4 columns with one
+// 16-byte load each per k.  Same order of the sums as k_gemm_dd.
+template <int TM>
+__global__ void __launch_bounds__(TM * 4) k_gemm_dd64(const __grid_constant__ DdBatch bt) {
+  constexpr int NT = TM * 4;             // (TM / 4) x 16 threads
+  constexpr int RA = TM * 8 / NT;        // A slab: TM x 32 floats = TM * 8 float4
+  constexpr int RB = 512 / NT;           // B slab: 64 x 32 floats = 512 float4
   const DdJob J = bt.job[blockIdx.z];
   const int d = bt.d;
-  __shared__ __align__(16) float As[32][64];
+  __shared__ __align__(16) float As[32][TM];
   __shared__ __align__(16) float Bs[32][64];
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int i0 = blockIdx.y * 64, j0 = blockIdx.x * 64;
-  // slab loads: 64 x 32 floats of each operand = 512 float4, two per thread
-  float4 ra[2], rb[2];
+  const int i0 = blockIdx.y * TM, j0 = blockIdx.x * 64;
+  float4 ra[RA], rb[RB];
   auto load = [&](int k0) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int q = tid + 256 * h;
+    for (int h = 0; h < RA; ++h) {
+      const int q = tid + NT * h;
       // op(A)[i][l]: plain A is read along l (8 float4 per row), a transposed one along i
-      ra[h] = J.ta ? *reinterpret_cast<const float4*>(J.A + (int64_t)(k0 + (q >> 4)) * d + i0 + 4 * (q & 15))
+      ra[h] = J.ta ? *reinterpret_cast<const float4*>(J.A + (int64_t)(k0 + q / (TM / 4)) * d + i0 + 4 * (q % (TM / 4)))
                    : *reinterpret_cast<const float4*>(J.A + (int64_t)(i0 + (q >> 3)) * d + k0 + 4 * (q & 7));
+    }
+#pragma unroll
+    for (int h = 0; h < RB; ++h) {
+      const int q = tid + NT * h;
       rb[h] = J.tb ? *reinterpret_cast<const float4*>(J.B + (int64_t)(j0 + (q >> 3)) * d + k0 + 4 * (q & 7))
                    : *reinterpret_cast<const float4*>(J.B + (int64_t)(k0 + (q >> 4)) * d + j0 + 4 * (q & 15));
     }
   };
   auto store = [&]() {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int q = tid + 256 * h;
+    for (int h = 0; h < RA; ++h) {
+      const int q = tid + NT * h;
       if (J.ta) {
-        *reinterpret_cast<float4*>(&As[q >> 4][4 * (q & 15)]) = ra[h];
+        *reinterpret_cast<float4*>(&As[q / (TM / 4)][4 * (q % (TM / 4))]) = ra[h];
       } else {
         const int ii = q >> 3, kk = 4 * (q & 7);
         As[kk][ii] = ra[h].x;
@@ -263,6 +272,10 @@ __global__ void __launch_bounds__(256) k_gemm_dd64(const __grid_constant__ DdBat
         As[kk + 2][ii] = ra[h].z;
         As[kk + 3][ii] = ra[h].w;
       }
+    }
+#pragma unroll
+    for (int h = 0; h < RB; ++h) {
+      const int q = tid + NT * h;
       if (J.tb) {
         const int jj = q >> 3, kk = 4 * (q & 7);
         Bs[kk][jj] = rb[h].x;
@@ -558,14 +571,14 @@ sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G
   b1.job[0] = {S, AQ, W1, 0, 0};   // W1 = S A_Q
   b1.job[1] = {AP, S, W2, 0, 0};   // W2 = A_P S
   const bool dd64 = d % 64 == 0;
-  if (dd64) sf::k_gemm_dd64<<<dim3(tiles, tiles, 2), 256, 0, s>>>(b1);
+  if (dd64) sf::k_gemm_dd64<32><<<dim3(tiles, 2 * tiles, 2), 128, 0, s>>>(b1);
   else sf::k_gemm_dd<<<dim3(tiles, tiles, 2), 256, 0, s>>>(b1);
   sf::DdBatch b2{};
   b2.d = d;
   b2.job[0] = {W2, AQ, X, 0, 0};   // X = A_P S A_Q
   b2.job[1] = {W1, S, K1, 0, 1};   // K1 = S A_Q S^T
   b2.job[2] = {S, W2, K2, 1, 0};   // K2 = S^T A_P S
-  if (dd64) sf::k_gemm_dd64<<<dim3(tiles, tiles, 3), 256, 0, s>>>(b2);
+  if (dd64) sf::k_gemm_dd64<32><<<dim3(tiles, 2 * tiles, 3), 128, 0, s>>>(b2);
   else sf::k_gemm_dd<<<dim3(tiles, tiles, 3), 256, 0, s>>>(b2);
   SF_TRY(sf::check_launch("k_gemm_dd"));
   sf::k_fit_combine<<<sf::kCombineBlocks, 256, 0, s>>>(S, X, W1, W2, d, HP, HQ, part);
