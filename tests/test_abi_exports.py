@@ -72,3 +72,33 @@ def test_validation_errors_without_gpu(lib):
     assert lib.sf_slide_window_step(None, None, 0, None, 0, None, None) == native.SF_ERR_INVALID
     # projector queries on NULL
     assert lib.lsp_projector_rows(None) == -1 and lib.lsp_projector_dim(None) == -1
+
+
+def test_workspace_sizes_without_gpu(lib):
+    # the workspace queries are host arithmetic on the shapes
+    a = native.lsp_workspace_bytes(4096, 4096, 512)
+    b = native.lsp_workspace_bytes(4096, 11008, 512)
+    assert 4096 * 512 * 4 <= a < b                    # at least R^T (n x d fp32)
+    f = native.lsp_fit_workspace_bytes(4096, 4096, 512, native.SF_FP32)
+    assert f > a + 4096 * 4096 * 4                    # the compress pair's workspace plus G^T
+    l1 = native.lce_workspace_bytes(8192, 4096, 128256, 4608)
+    assert l1 == native.lce_workspace_bytes(8192, 64, 128256, 4608)   # nothing depends on D
+    assert l1 >= 4608 * 128256 * (4 + 2)             # one chunk of fp32 logits and bf16 gradient
+    # the chunk is clamped to the token count (rounded up to 8)
+    assert native.lce_workspace_bytes(100, 64, 1000, 4096) == native.lce_workspace_bytes(100, 64, 1000, 104)
+    assert native.lce_workspace_bytes(0, 64, 1000, 64) == 0
+
+
+def test_gemm_probe_and_cross_entropy_validation_without_gpu(lib):
+    # argument checks that return before any CUDA call
+    f = ctypes.c_float(1.0)
+    assert lib.sf_gemm_bf16(None, 0, None, 0, None, 1, 1, 1, 1, 1, 1, f, 0, None) == native.SF_ERR_INVALID
+    assert lib.sf_gemm_bf16(16, 2, 16, 0, 16, 8, 8, 8, 8, 8, 8, f, 0, None) == native.SF_ERR_INVALID
+    assert "layout" in native.sf_last_error()
+    assert lib.sf_gemm_abt_bf16(16, 16, 16, 0, 8, 8, 8, 8, 8, f, 0, None) == native.SF_ERR_INVALID
+    assert lib.sf_bench_gather_rate(0, 8, 16, None) == native.SF_ERR_INVALID
+    loss = ctypes.c_double()
+    assert lib.lce_forward_backward(None, 16, 16, 8, 8, 8, 8, -100, ctypes.byref(loss), None, None, 16, 1 << 20,
+                                    None) == native.SF_ERR_INVALID
+    assert lib.lce_forward_backward(16, 16, 16, 8, 8, 8, 12, -100, ctypes.byref(loss), None, None, 16, 1 << 20,
+                                    None) == native.SF_ERR_INVALID       # chunk not a multiple of 8
