@@ -496,13 +496,13 @@ __global__ void k_gather_generic(const TB* __restrict__ B, int64_t ldb, int64_t 
 //              of q * B[j][c]
 // One warp per output column a and 128-column slice of B: the warp fetches
 // 32 entries at a time (one per lane), broadcasts them in order, and each
-// lane reads 4 consecutive columns of row j (16-byte loads, eight rows in
-// flight), so B is read straight from L2 with no staging and no split
+// lane reads 4 consecutive columns of row j (16-byte loads, sixteen rows
+// in flight), so B is read straight from L2 with no staging and no split
 // partials.  The CTA's 8 outputs are transposed through shared memory so
 // yt is written as 32-byte row segments.  Needs B 16-byte aligned with
 // ldb and ncols multiples of 4 (every 16-byte load inside a row).
-constexpr int kRgWarps = 8, kRgCols = 128, kRgUnroll = 8;
-__global__ void __launch_bounds__(32 * kRgWarps) k_rowgather(const float* __restrict__ B, int64_t ldb, int ncols,
+constexpr int kRgWarps = 8, kRgCols = 128, kRgUnroll = 16;
+__global__ void __launch_bounds__(32 * kRgWarps, 2) k_rowgather(const float* __restrict__ B, int64_t ldb, int ncols,
                                                              const int32_t* __restrict__ col_ptr,
                                                              const int32_t* __restrict__ row_idx,
                                                              const float* __restrict__ csc_val, int d,
