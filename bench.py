@@ -16,7 +16,14 @@ Also on the same line:
              around every launch in the timed region.
   lsp        the sparse-projector chain on the seven LLaMA-7B weight
              gradients (compress, compressed AdamW, decompress-apply into
-             bf16 W; d = 512, 8 nonzeros per row), per-kernel times.
+             bf16 W; d = 512, 8 nonzeros per row), per-stage times, the
+             chain replayed from CUDA graphs, the projector fit step, and
+             the measured shared-memory gather rate that bounds the chain's
+             kernels (gather_roof) with each stage's fraction of it.
+  lce        the fused linear cross-entropy on a Llama-3.1-8B output layer
+             (8192 tokens, V 128256), tensor roofline against the sustained
+             bf16 figure (the calls run under the power cap), with clocks.
+  host_update  the same AdamW on the host cores (the pages' placement).
   cpu_baseline  the fp64 oracle on this machine's host cores, on a bounded
              sample of the same workload.
   clocks     SM clocks and throttle reasons sampled during the timed region.
