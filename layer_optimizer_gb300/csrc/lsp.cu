@@ -17,10 +17,12 @@
 //
 // Compress, two gathers (R-first):
 //   stage 1  R^T = (P^T G)^T      k_gather_t over G, A = P      (n x d)
-//   stage 2  S   = (Q^T R^T)^T    k_gather_t over R^T, A = Q    (d x d)
+//   stage 2  S   = (Q^T R^T)^T    k_rowgather over R^T, A = Q   (d x d)
+//            (R^T is small and still in L2: read straight from there;
+//            k_gather_t when its rows are not 16-byte multiples)
 // k_gather_t(A, B) writes Y^T = (A^T B)^T: a CTA owns 128 columns of B and
 // 8 x warps outputs a (columns of A); B streams through shared memory in
-// windows of 64 rows by TMA (cp.async.bulk.tensor), the CTAs of one column
+// windows of 128 rows by TMA (cp.async.bulk.tensor), the CTAs of one column
 // block form a cluster and share every window by TMA multicast, so B is read
 // from L2 once.  A's entries come from a window-major column list (entries
 // of window w and column a, rows ascending, with a prefix table), so a warp
