@@ -16,7 +16,10 @@
 // kGroupParams parameters each, or the rest of the layer): a group's update
 // starts as soon as that group has arrived, its write-back as soon as it is
 // updated, and the next visit to the slot may overwrite a tensor as soon as
-// that tensor's write-back has ended.  It does no arithmetic of its own;
+// that tensor's write-back has ended.  Copies go per array of a group, and
+// tensors whose host and slot arrays both follow one another in memory
+// move as one copy (a layer kept as flat per-array buffers, as flattened
+// optimizer states are, costs one copy per array).  It does no arithmetic of its own;
 // dependencies are CUDA events only, and the host never blocks while
 // enqueueing.
 #include <algorithm>
