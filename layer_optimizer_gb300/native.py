@@ -27,7 +27,8 @@ EXPORTS = [
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
     "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
-    "sf_gemm_abt_bf16", "sf_gemm_bf16", "sf_bench_gather_rate", "lce_workspace_bytes", "lce_forward_backward", "sf_test_device_wait_runs_out",
+    "sf_gemm_abt_bf16", "sf_gemm_bf16", "sf_bench_gather_rate", "lce_workspace_bytes", "lce_forward_backward",
+    "sf_test_device_wait_runs_out",
 ]
 
 
