@@ -497,6 +497,37 @@ sf_status sf_test_device_wait_runs_out(int64_t limit_cycles, void* stream);
  * ctas < 1, iters < 1 or a NULL sink. */
 sf_status sf_bench_gather_rate(int32_t ctas, int64_t iters, float* sink, void* stream);
 
+/* Measurement hook: the tensor-memory (TMEM) gather rate, the survey's
+ * other on-chip roof for the projector kernels (LSP-Offload, method
+ * section: the compress and decompress are sparse products whose dense
+ * operand is read at rows chosen by projector indices).  Launches `ctas`
+ * CTAs of 512 threads, one per SM, each allocating all 512 TMEM columns for
+ * the duration of the launch (released before it ends).  Every thread runs
+ * `iters` steps; a step issues 8 tcgen05.ld.32x32b loads of `x` (1, 2 or 4)
+ * consecutive 32-bit columns of its lane at columns chosen per load, waits
+ * for them and does 8 * x fp32 multiply-adds.  With `entries` != 0 each
+ * load's column and multiplier come from an 8-byte entry in shared memory
+ * (as in a gather kernel), else they are computed in registers.  Writes one
+ * float to sink[cta * 512 + thread] (device, ctas * 512 floats).
+ * Multiply-adds done: ctas * 512 * iters * 8 * x; the caller times the call
+ * (CUDA events on `stream`).  SF_ERR_INVALID for ctas < 1, iters < 1, a NULL
+ * sink or x not in {1, 2, 4}. */
+sf_status sf_bench_tmem_rate(int32_t ctas, int64_t iters, int32_t x, int32_t entries, float* sink, void* stream);
+
+/* Measurement hook: the rate of row gathers served from L2 (the source a
+ * gather reads when its dense operand is not staged on chip).  `buf` is a
+ * device array of `rows` rows of 128 floats (512 bytes, 16-byte aligned);
+ * launches `ctas` CTAs of 256 threads; each warp runs `iters` steps of 16
+ * row loads (one 16-byte load per lane, rows chosen by a per-warp
+ * generator, all 16 in flight) followed by 64 multiply-adds per lane, and
+ * each thread writes one float to sink[cta * 256 + thread] (device, ctas *
+ * 256 floats).  Bytes gathered: ctas * 8 * iters * 16 * 512.  With
+ * rows * 512 bytes well below L2's size and the buffer read once before,
+ * the loads hit L2.  SF_ERR_INVALID for ctas, iters or rows below 1, rows
+ * of 2^32 or more, NULL pointers or an unaligned buf. */
+sf_status sf_bench_l2_gather_rate(int32_t ctas, int64_t iters, const float* buf, int64_t rows, float* sink,
+                                  void* stream);
+
 #ifdef __cplusplus
 }
 #endif

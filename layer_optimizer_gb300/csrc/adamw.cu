@@ -393,17 +393,17 @@ sf_status adamw_layer_step_impl(const sf_tensor* tensors, int n_tensors, const s
     if (tensors[i].numel < 0) return fail(SF_ERR_INVALID, "tensor %d: numel < 0", i);
 
   static_assert(sizeof(LaunchArgs) <= 4096, "kernel parameter block too large");
-  // Arrays in pinned host memory are updated in place over the host link
-  // (zero-copy loads and stores from the register-staged kernel; the bulk
-  // kernel's shared-memory copies are kept for device memory).
+  // Arrays in pinned host memory (or anywhere but this device's memory) are
+  // updated in place with the register-staged kernel's plain loads and
+  // stores (zero-copy over the host link); the bulk kernel's shared-memory
+  // copies read only this device's own memory.
   bool host_resident = false;
   for (int i = 0; i < n_tensors && !host_resident; ++i) {
-    if (tensors[i].numel == 0) continue;
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, tensors[i].master) == cudaSuccess && a.type == cudaMemoryTypeHost)
+    const sf_tensor& t = tensors[i];
+    if (t.numel == 0) continue;
+    if (!on_current_device(t.master) || !on_current_device(t.grad) || !on_current_device(t.exp_avg) ||
+        !on_current_device(t.exp_avg_sq))
       host_resident = true;
-    else
-      cudaGetLastError();
   }
   LaunchArgs L;
   const int grid_cap = sm_count() * blocks_per_sm();

@@ -45,6 +45,18 @@ int sm_count() {
   return cached_sms;
 }
 
+bool on_current_device(const void* p) {
+  if (!p) return false;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
 int64_t default_timeout_ms() {
   const char* s = std::getenv("SF_TIMEOUT_MS");
   if (s && *s) {

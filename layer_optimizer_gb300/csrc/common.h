@@ -61,6 +61,12 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// True when `p` points into device memory of the current device.  Every
+// tensor map (TMA descriptor) this library encodes addresses such memory
+// only; operands elsewhere (pinned host memory, a peer GPU's memory) take a
+// path with plain loads or are rejected.
+bool on_current_device(const void* p);
+
 // Default bound for host waits, in milliseconds (SF_TIMEOUT_MS or 600 s).
 int64_t default_timeout_ms();
 

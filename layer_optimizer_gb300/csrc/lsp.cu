@@ -21,13 +21,23 @@
 //            (R^T is small and still in L2: read straight from there;
 //            k_gather_t when its rows are not 16-byte multiples)
 // k_gather_t(A, B) writes Y^T = (A^T B)^T: a CTA owns 128 columns of B and
-// 8 x warps outputs a (columns of A); B streams through shared memory in
-// windows of 128 rows by TMA (cp.async.bulk.tensor), the CTAs of one column
-// block form a cluster and share every window by TMA multicast, so B is read
-// from L2 once.  A's entries come from a window-major column list (entries
-// of window w and column a, rows ascending, with a prefix table), so a warp
-// finds its (window, a) entries with two 16-byte loads.  Row splits (for
-// grid size) write partial outputs that one reduction sums in split order.
+// 4 x warps outputs a (columns of A; 32 warps, 128 outputs for d >= 128);
+// B streams through shared memory in windows of 128 rows by TMA
+// (cp.async.bulk.tensor); the CTAs that share a column block each load the
+// window themselves (the repeats come from L2).  A's entries come from a
+// window-major column list (entries of window w and column a, rows
+// ascending, with a prefix table), so a warp finds its (window, a) entries
+// with a few broadcast loads.  Row splits (for grid size) write partial
+// outputs that one reduction sums in split order.
+//
+// Measured on GB300 for one 4096 x 4096 fp32 G (stage 1, 134 M multiply-
+// adds): this kernel 46 us; k_rowgather reading G's rows straight from L2
+// instead 61 us (same bits; latency-bound at a quarter of L2's throughput);
+// the shared-memory pipe runs about 60 % busy and the warps wait mostly on
+// shared-memory loads and tile arrival.  Tensor memory (tcgen05.ld) reads
+// faster than shared memory only four columns per lane at a time, and a
+// warp reaches only its quarter of TMEM's lanes, so holding a window there
+// would split every output's accumulators over the quarters.
 //
 // Decompress:
 //   V = dS Q^T (d x n)          k_v: dS^T block resident in shared memory,
@@ -54,6 +64,7 @@ namespace {
 
 constexpr int kWinRows = 128;       // rows of A (and of B) per window
 constexpr int kColsPerCta = 128;    // B columns per gather CTA (4 per lane)
+constexpr int kGatherOut = 4;       // outputs (columns of A) per gather warp
 constexpr int kMaxStages = 4;       // TMA ring depth of the gather kernel (at most)
 constexpr int kTargetCtas = 148;    // grid size aimed at (about one CTA per SM)
 constexpr int kApplyCols = 64;      // W columns per apply CTA (2 per lane)
@@ -280,8 +291,6 @@ struct GatherArgs {
   int32_t wbytes;          // its bytes (8 x warps + 1 ints, padded to 16)
   int32_t ent_off;         // offset of the staged entry slice inside a stage
   int32_t stage_stride;    // bytes between stages in shared memory
-  int32_t slice_rows;      // rows each CTA of the cluster loads (kWinRows / cluster)
-  int32_t cluster;         // CTAs per cluster (1, 2, 4 or 8)
   int32_t vec_out;         // output rows are 16-byte aligned (d % 4 == 0, aligned base)
   int32_t stages;          // depth of the TMA ring
 };
@@ -298,8 +307,26 @@ __device__ __forceinline__ float4 tile_load(uint32_t addr) {
   }
 }
 
+// The same 4 elements as two packed fp32 pairs (first pair in .x).
 template <typename TB>
-__global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtensorMap map, const GatherArgs A) {
+__device__ __forceinline__ ulonglong2 tile_load2(uint32_t addr) {
+  if constexpr (sizeof(TB) == 4) {
+    return lds_u64x2(addr);
+  } else {
+    const uint2 u = lds_u2(addr);
+    return make_ulonglong2(pack_f2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u)),
+                           pack_f2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xFFFF0000u)));
+  }
+}
+
+// One CTA: kGatherOut outputs per warp, as many warps as the projector's
+// output range needs (32 for d >= 128).  There is no producer warp: lane 0
+// of the last warp issues the copies of a stage once every warp has released
+// it, before it computes its own share of the next window, so all warps of
+// the CTA gather (twice the warps per SM of a dedicated producer layout,
+// which keeps the shared-memory loads' latency hidden).
+template <typename TB>
+__global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CUtensorMap map, const GatherArgs A) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // round up to 1024 with arithmetic on the __shared__ array itself, so the
   // compiler keeps the shared address space (plain LDS, not generic loads)
@@ -311,166 +338,163 @@ __global__ void __launch_bounds__(544) k_gather_t(const __grid_constant__ CUtens
   int32_t* flags = hdr + kMaxStages;                                // [0] issued, [1] failed
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ncw = (blockDim.x >> 5) - 1;        // consumer warps; the last warp produces
-  const int C = A.cluster;
-  const uint32_t rank = C > 1 ? cluster_ctarank() : 0;
-  const uint16_t mask = (uint16_t)((1u << C) - 1u);
+  const int nwarps = blockDim.x >> 5;
   const int c0 = blockIdx.x * kColsPerCta;
-  const int a_cta = blockIdx.y * 8 * ncw;
+  const int a_cta = blockIdx.y * kGatherOut * nwarps;
   const int w_begin = blockIdx.z * A.win_per_split;
   const int w_end = min(A.n_win, w_begin + A.win_per_split);
   const int nw = max(0, w_end - w_begin);
+  const bool producer = warp == nwarps - 1 && lane == 0;
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&map);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], ncw * C);
+      mbar_init(&empty[s], nwarps);
     }
     flags[0] = 0;
     flags[1] = 0;
     fence_mbar_init_cluster();
   }
-  if (C > 1) cluster_sync(); else __syncthreads();
+  __syncthreads();
   griddep_launch_dependents();
 
-  if (warp == ncw) {
-    // Producer: one stage = the B tile of a window (rows split over the
-    // cluster and multicast), this CTA's slice of the prefix table and its
-    // entry slice.  A stage is refilled once every consumer warp of every
-    // CTA in the cluster has released it.
-    if (lane == 0) {
-      const int2* gd_row = A.gdesc + (int64_t)blockIdx.y * A.n_win;
-      griddep_wait();            // B may be the previous kernel's output
-      int it = 0;
-      int s = 0;                 // stage of window it, and the phase parity of its ring pass
-      uint32_t pass = 0;
-      int2 gd = nw > 0 ? gd_row[w_begin] : make_int2(0, 0);
-      for (; it < nw; ++it) {
-        if (it >= S && !mbar_wait(&empty[s], pass ^ 1u)) {
-          flags[1] = 1;
-          break;
-        }
-        const int w = w_begin + it;
-        unsigned char* st = smem + (size_t)s * A.stage_stride;
-        hdr[s] = gd.x;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)(A.stage_tx + A.wbytes + gd.y));
-        unsigned char* dst = st + (size_t)rank * A.slice_rows * A.cbx * sizeof(TB);
-        const int y = w * kWinRows + (int)rank * A.slice_rows;
-        if (C > 1) tma_load_2d_multicast(dst, &map, &full[s], c0, y, mask);
-        else tma_load_2d(dst, &map, &full[s], c0, y);
-        bulk_load(st + A.wsl_off, A.wptr + (int64_t)w * A.dp + a_cta, (uint32_t)A.wbytes, &full[s]);
-        if (gd.y > 0) bulk_load(st + A.ent_off, A.went + gd.x, (uint32_t)gd.y, &full[s]);
-        if (it + 1 < nw) gd = gd_row[w + 1];
-        if (++s == S) {
-          s = 0;
-          pass ^= 1u;
-        }
-      }
-      flags[0] = it;
-    }
-  } else {
-    const int a0 = a_cta + 8 * warp;
-    const bool lane_on = 4 * lane < A.cbx;
-    const bool warp_on = a0 < A.dp;
-    const uint32_t smem_base = smem_u32(smem);
-    const uint32_t row_bytes = (uint32_t)A.cbx * (uint32_t)sizeof(TB);
-    const uint32_t lane_off = 4u * (uint32_t)lane * (uint32_t)sizeof(TB);
-    float acc[8][4];
+  // one stage = the B tile of a window, this CTA's slice of the prefix
+  // table and its entry slice
+  const int2* gd_row = A.gdesc + (int64_t)blockIdx.y * A.n_win;
+  auto issue = [&](int it) {
+    const int s = it % S;
+    const int w = w_begin + it;
+    const int2 gd = gd_row[w];
+    unsigned char* st = smem + (size_t)s * A.stage_stride;
+    hdr[s] = gd.x;
+    mbar_arrive_expect_tx(&full[s], (uint32_t)(A.stage_tx + A.wbytes + gd.y));
+    tma_load_2d(st, &map, &full[s], c0, w * kWinRows);
+    bulk_load(st + A.wsl_off, A.wptr + (int64_t)w * A.dp + a_cta, (uint32_t)A.wbytes, &full[s]);
+    if (gd.y > 0) bulk_load(st + A.ent_off, A.went + gd.x, (uint32_t)gd.y, &full[s]);
+  };
+  int issued = 0;
+  if (producer) {
+    griddep_wait();            // B may be the previous kernel's output
+    for (; issued < min(S, nw); ++issued) issue(issued);
+    flags[0] = issued;
+  }
+
+  const int a0 = a_cta + kGatherOut * warp;
+  const bool lane_on = 4 * lane < A.cbx;
+  const bool warp_on = a0 < A.dp;
+  const uint32_t smem_base = smem_u32(smem);
+  const uint32_t row_bytes = (uint32_t)A.cbx * (uint32_t)sizeof(TB);
+  const uint32_t lane_off = 4u * (uint32_t)lane * (uint32_t)sizeof(TB);
+  // the lane's 4 columns of each output as two packed fp32 pairs
+  uint64_t acc[kGatherOut][2];
 #pragma unroll
-    for (int sl = 0; sl < 8; ++sl)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) acc[sl][j] = 0.0f;
-    bool failed = false;
-    int s = 0;
-    uint32_t pass = 0;
-    for (int it = 0; it < nw; ++it) {
-      if (!mbar_wait(&full[s], pass)) {
+  for (int sl = 0; sl < kGatherOut; ++sl) acc[sl][0] = acc[sl][1] = 0ull;
+  bool failed = false;
+  int s = 0;
+  uint32_t pass = 0;
+  const uint32_t full_a = smem_u32(full);
+  for (int it = 0; it < nw; ++it) {
+    // refill the stage of the previous window for window it - 1 + S once
+    // every warp has released it (this warp released it last iteration)
+    if (producer && it >= 1 && issued < nw && !failed) {
+      const int prev = it - 1;
+      if (!mbar_wait_u32(smem_u32(&empty[prev % S]), (uint32_t)(prev / S) & 1u)) {
         failed = true;
         flags[1] = 1;
-        break;
-      }
-      const int w = w_begin + it;
-      if (warp_on && lane_on) {
-        // 32-bit shared addresses: entry i of the stage at ent + 8 i; row r of
-        // the tile, this lane's 4 columns, at lane_tile + r * row_bytes
-        const uint32_t tile = smem_base + (uint32_t)s * (uint32_t)A.stage_stride;
-        const uint32_t bp = tile + (uint32_t)A.wsl_off + 32u * (uint32_t)warp;
-        const int4 lo = lds_i4(bp);
-        const int4 hi = lds_i4(bp + 16);
-        const int32_t last = (int32_t)lds_u32(bp + 32);
-        const int32_t e_base = hdr[s];
-        const uint32_t ent = tile + (uint32_t)A.ent_off - 8u * (uint32_t)e_base;
-        const uint32_t row_adj = tile + lane_off - (uint32_t)(w * kWinRows) * row_bytes;
-        const int bnd[9] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w, last};
-#pragma unroll
-        for (int sl = 0; sl < 8; ++sl) {
-          int e = bnd[sl];
-          const int e_end = bnd[sl + 1];
-          // two entries per step: independent loads in flight
-          for (; e + 1 < e_end; e += 2) {
-            const int2 en0 = lds_i2(ent + 8u * (uint32_t)e);
-            const int2 en1 = lds_i2(ent + 8u * (uint32_t)e + 8u);
-            const float4 x0 = tile_load<TB>(row_adj + (uint32_t)en0.x * row_bytes);
-            const float4 x1 = tile_load<TB>(row_adj + (uint32_t)en1.x * row_bytes);
-            const float v0 = __int_as_float(en0.y), v1 = __int_as_float(en1.y);
-            acc[sl][0] = fmaf(v1, x1.x, fmaf(v0, x0.x, acc[sl][0]));
-            acc[sl][1] = fmaf(v1, x1.y, fmaf(v0, x0.y, acc[sl][1]));
-            acc[sl][2] = fmaf(v1, x1.z, fmaf(v0, x0.z, acc[sl][2]));
-            acc[sl][3] = fmaf(v1, x1.w, fmaf(v0, x0.w, acc[sl][3]));
-          }
-          if (e < e_end) {
-            const int2 en = lds_i2(ent + 8u * (uint32_t)e);
-            const float4 x = tile_load<TB>(row_adj + (uint32_t)en.x * row_bytes);
-            const float v = __int_as_float(en.y);
-            acc[sl][0] = fmaf(v, x.x, acc[sl][0]);
-            acc[sl][1] = fmaf(v, x.y, acc[sl][1]);
-            acc[sl][2] = fmaf(v, x.z, acc[sl][2]);
-            acc[sl][3] = fmaf(v, x.w, acc[sl][3]);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        if (C > 1) {
-          for (int r = 0; r < C; ++r) mbar_arrive_cluster(&empty[s], (uint32_t)r);
-        } else {
-          mbar_arrive_local(&empty[s]);
-        }
-      }
-      if (++s == S) {
-        s = 0;
-        pass ^= 1u;
+      } else {
+        issue(issued++);
+        flags[0] = issued;
       }
     }
-
-    // Y^T[col][a] for the lane's 4 columns and the warp's 8 outputs.
-    if (warp_on && lane_on && !failed) {
-      float* out = A.yt + (int64_t)blockIdx.z * A.split_stride;
-      const bool vec = A.vec_out && (a0 + 8 <= A.d);
+    if (failed || !mbar_wait_u32(full_a + 8u * (uint32_t)s, pass)) {
+      failed = true;
+      flags[1] = 1;
+      break;
+    }
+    const int w = w_begin + it;
+    if (warp_on && lane_on) {
+      // 32-bit shared addresses: entry i of the stage at ent + 8 i; row r of
+      // the tile, this lane's 4 columns, at row_adj + r * row_bytes
+      const uint32_t tile = smem_base + (uint32_t)s * (uint32_t)A.stage_stride;
+      const uint32_t bp = tile + (uint32_t)A.wsl_off + 4u * kGatherOut * (uint32_t)warp;
+      int bnd[kGatherOut + 1];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int col = c0 + 4 * lane + j;
-        if (col >= A.ncols) continue;
-        float* o = out + (int64_t)col * A.d + a0;
-        if (vec) {
-          *reinterpret_cast<float4*>(o) = make_float4(acc[0][j], acc[1][j], acc[2][j], acc[3][j]);
-          *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4][j], acc[5][j], acc[6][j], acc[7][j]);
-        } else {
+      for (int q = 0; q <= kGatherOut; ++q) bnd[q] = (int)lds_u32(bp + 4u * q);
+      const int32_t e_base = hdr[s];
+      const uint32_t ent = tile + (uint32_t)A.ent_off - 8u * (uint32_t)e_base;
+      const uint32_t row_adj = tile + lane_off - (uint32_t)(w * kWinRows) * row_bytes;
 #pragma unroll
-          for (int sl = 0; sl < 8; ++sl)
-            if (a0 + sl < A.d) o[sl] = acc[sl][j];
+      for (int sl = 0; sl < kGatherOut; ++sl) {
+        uint32_t ea = ent + 8u * (uint32_t)bnd[sl];
+        const uint32_t ee = ent + 8u * (uint32_t)bnd[sl + 1];
+        uint64_t a01 = acc[sl][0], a23 = acc[sl][1];
+        // two entries per step: both entry loads, then both tile loads, in flight together
+        for (; ea + 8u < ee; ea += 16u) {
+          const int2 en0 = lds_i2(ea);
+          const int2 en1 = lds_i2(ea + 8u);
+          const ulonglong2 x0 = tile_load2<TB>(row_adj + (uint32_t)en0.x * row_bytes);
+          const ulonglong2 x1 = tile_load2<TB>(row_adj + (uint32_t)en1.x * row_bytes);
+          const float v0 = __int_as_float(en0.y), v1 = __int_as_float(en1.y);
+          const uint64_t vv0 = pack_f2(v0, v0), vv1 = pack_f2(v1, v1);
+          ffma2(a01, x0.x, vv0);
+          ffma2(a23, x0.y, vv0);
+          ffma2(a01, x1.x, vv1);
+          ffma2(a23, x1.y, vv1);
         }
+        if (ea < ee) {
+          const int2 en = lds_i2(ea);
+          const ulonglong2 x = tile_load2<TB>(row_adj + (uint32_t)en.x * row_bytes);
+          const float v = __int_as_float(en.y);
+          const uint64_t vv = pack_f2(v, v);
+          ffma2(a01, x.x, vv);
+          ffma2(a23, x.y, vv);
+        }
+        acc[sl][0] = a01;
+        acc[sl][1] = a23;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive_local(&empty[s]);
+    if (++s == S) {
+      s = 0;
+      pass ^= 1u;
+    }
+  }
+
+  // Y^T[col][a] for the lane's 4 columns and the warp's outputs.
+  if (warp_on && lane_on && !failed) {
+    float res[kGatherOut][4];
+#pragma unroll
+    for (int sl = 0; sl < kGatherOut; ++sl) {
+      const float2 p01 = unpack_f2(acc[sl][0]), p23 = unpack_f2(acc[sl][1]);
+      res[sl][0] = p01.x;
+      res[sl][1] = p01.y;
+      res[sl][2] = p23.x;
+      res[sl][3] = p23.y;
+    }
+    float* out = A.yt + (int64_t)blockIdx.z * A.split_stride;
+    const bool vec = A.vec_out && (a0 + kGatherOut <= A.d);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int col = c0 + 4 * lane + j;
+      if (col >= A.ncols) continue;
+      float* o = out + (int64_t)col * A.d + a0;
+      if (vec) {
+        *reinterpret_cast<float4*>(o) = make_float4(res[0][j], res[1][j], res[2][j], res[3][j]);
+      } else {
+#pragma unroll
+        for (int sl = 0; sl < kGatherOut; ++sl)
+          if (a0 + sl < A.d) o[sl] = res[sl][j];
       }
     }
   }
   __syncthreads();
   if (threadIdx.x == 0 && flags[1]) {
     // a wait ran out: let this CTA's copies still in flight land (bounded)
-    const int issued = flags[0];
-    for (int j = max(0, issued - S); j < issued; ++j) mbar_wait(&full[j % S], (uint32_t)(j / S) & 1u);
+    const int n_issued = flags[0];
+    for (int j = max(0, n_issued - S); j < n_issued; ++j) mbar_wait(&full[j % S], (uint32_t)(j / S) & 1u);
   }
-  if (C > 1) cluster_sync();
 }
 
 // Generic gather for shapes the TMA path cannot take: one thread per output.
@@ -1176,9 +1200,9 @@ __global__ void k_apply_generic(const float* __restrict__ V, int64_t n, int64_t 
 
 GatherPlan plan_gather(int64_t rows, int64_t ncols, int d) {
   GatherPlan p;
-  p.warps = std::min(16, (d + 7) / 8);
-  p.n_ar = (d + 8 * p.warps - 1) / (8 * p.warps);
-  p.cluster = (p.n_ar == 1 || p.n_ar == 2 || p.n_ar == 4 || p.n_ar == 8) ? p.n_ar : 1;
+  // the projector's output range (a_rng = 8 x min(16, ceil(d / 8))), kGatherOut per warp
+  p.warps = 8 * std::min(16, (d + 7) / 8) / kGatherOut;
+  p.n_ar = (d + kGatherOut * p.warps - 1) / (kGatherOut * p.warps);
   p.n_cb = (int)ceil_div<int64_t>(ncols, kColsPerCta);
   p.n_win = (int)ceil_div<int64_t>(rows, kWinRows);
   const int64_t base = (int64_t)p.n_cb * p.n_ar;
@@ -1217,9 +1241,11 @@ size_t gather_smem_estimate(const lsp_projector_s* Ap, size_t es) {
   return 2 * gather_stage_bytes(Ap, es) + 2048;   // the ring needs at least two stages
 }
 
+// A tensor map may be built on B: 16-byte aligned base and rows, and B in
+// the current device's memory (anything else takes the plain-load kernels).
 bool tma_ok(const void* B, int64_t ldb, size_t esize) {
   return (reinterpret_cast<uintptr_t>(B) % 16) == 0 && (ldb * (int64_t)esize) % 16 == 0 &&
-         tensor_map_encoder() != nullptr;
+         tensor_map_encoder() != nullptr && on_current_device(B);
 }
 
 template <typename TB>
@@ -1228,7 +1254,7 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   const int64_t rows = Aproj->rows;
   const int d = Aproj->d;
   const size_t es = sizeof(TB);
-  if (!tma_ok(B, ldb, es) || Aproj->a_rng != 8 * p.warps || gather_smem_estimate(Aproj, es) > kMaxGatherSmem) {
+  if (!tma_ok(B, ldb, es) || Aproj->a_rng != kGatherOut * p.warps || gather_smem_estimate(Aproj, es) > kMaxGatherSmem) {
     const int64_t total = ncols * d;
     k_gather_generic<TB><<<(unsigned)ceil_div<int64_t>(total, 256), 256, 0, stream>>>(
         B, ldb, ncols, d, Aproj->col_ptr, Aproj->row_idx, Aproj->csc_val, yt_final);
@@ -1250,18 +1276,16 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   A.cbx = cbx;
   A.stage_tx = kWinRows * cbx * (int)es;
   A.wsl_off = (int)align_up((size_t)A.stage_tx, 128);
-  A.wbytes = (int)align_up((size_t)(8 * p.warps + 1) * 4, 16);
+  A.wbytes = (int)align_up((size_t)(kGatherOut * p.warps + 1) * 4, 16);
   A.ent_off = (int)align_up((size_t)A.wsl_off + A.wbytes, 128);
   A.stage_stride = (int)align_up((size_t)A.ent_off + Aproj->max_slice_bytes, 1024);
   A.stages = (int)std::min<size_t>(kMaxStages, (kMaxGatherSmem - 2048) / A.stage_stride);
-  A.cluster = p.cluster;
-  A.slice_rows = kWinRows / p.cluster;
   A.vec_out = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(A.yt) % 16 == 0) ? 1 : 0;
 
   CUtensorMap map;
   cuuint64_t dims[2] = {(cuuint64_t)ncols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ldb * (int64_t)es)};
-  cuuint32_t box[2] = {(cuuint32_t)cbx, (cuuint32_t)A.slice_rows};
+  cuuint32_t box[2] = {(cuuint32_t)cbx, (cuuint32_t)kWinRows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = tensor_map_encoder()(&map, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                     2, const_cast<TB*>(B), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1273,18 +1297,14 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&k_gather_t<TB>), kMaxGatherSmem));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.n_cb, (unsigned)p.n_ar, (unsigned)p.splits);
-  cfg.blockDim = dim3(32 * (p.warps + 1));
+  cfg.blockDim = dim3(32 * p.warps);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = (unsigned)p.cluster;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gather_t<TB>, map, A), "launch k_gather_t");
   if (p.splits > 1) {
     const int64_t n_out = ncols * d;

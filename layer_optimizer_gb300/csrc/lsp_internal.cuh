@@ -41,7 +41,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Launch geometry of one gather (pure function of the sizes).
 struct GatherPlan {
-  int warps, n_ar, cluster, n_cb, n_win, splits, win_per_split;
+  int warps, n_ar, n_cb, n_win, splits, win_per_split;
 };
 
 // The two gathers of lsp_compress and the workspace they use.

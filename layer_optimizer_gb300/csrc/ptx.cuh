@@ -1,5 +1,5 @@
-// Inline-PTX helpers for sm_103a: mbarriers, TMA tensor loads (with
-// cluster multicast), cluster addressing and barriers, and a bounded wait.
+// Inline-PTX helpers for sm_103a: mbarriers, TMA tensor loads, cluster
+// addressing and barriers, and a bounded wait.
 //
 // Every wait in this library is bounded: a wait that runs out records an
 // error code in a device word (read back by sf_sync_status) and returns
@@ -38,15 +38,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 
 __device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Arrive on the barrier at the same shared-memory offset in CTA `rank` of
-// the cluster (default release.cta semantics: orders this thread's earlier
-// shared-memory reads before the arrival without a cluster-scope fence).
-__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
-  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
@@ -125,17 +116,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
       ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
-      : "memory");
-}
-
-// 2D tiled TMA load multicast to every CTA in `mask` (same smem offset and
-// same barrier offset in each destination CTA).
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int x,
-                                                      int y, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%3, %4}], [%2], %5;"
-      ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(mask)
       : "memory");
 }
 

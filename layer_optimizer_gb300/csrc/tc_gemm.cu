@@ -590,6 +590,9 @@ sf_status tc_gemm(const void* A, bool a_mn, const void* B, bool b_mn, float* C, 
       (reinterpret_cast<uintptr_t>(B) % 16))
     return fail(SF_ERR_UNSUPPORTED, "A and B need 16-byte aligned bases and rows (lda, ldb multiples of 8)");
   if (!tensor_map_encoder()) return fail(SF_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available");
+  // the tensor maps below may only address this device's own memory
+  if (!on_current_device(A) || !on_current_device(B) || !on_current_device(C))
+    return fail(SF_ERR_INVALID, "A, B and C must be device memory of the current device");
   CUtensorMap ma, mb;
   int a_form = 0, b_form = 0;      // 0 K-major, 1 MN-major in 2D boxes, 2 MN-major in 3D boxes
   if (a_mn) {

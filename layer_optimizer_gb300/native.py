@@ -27,7 +27,7 @@ EXPORTS = [
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
     "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
-    "sf_gemm_abt_bf16", "sf_gemm_bf16", "sf_bench_gather_rate", "lce_workspace_bytes", "lce_forward_backward",
+    "sf_gemm_abt_bf16", "sf_gemm_bf16", "sf_bench_gather_rate", "sf_bench_tmem_rate", "sf_bench_l2_gather_rate", "lce_workspace_bytes", "lce_forward_backward",
     "sf_test_device_wait_runs_out",
 ]
 
@@ -104,6 +104,8 @@ _SIGS = {
     "lsp_projector_export_values": (_ST, [_P, _P, _P]),
     "sf_gemm_abt_bf16": (_ST, [_P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _INT, _P]),
     "sf_bench_gather_rate": (_ST, [_INT, _I64, _P, _P]),
+    "sf_bench_tmem_rate": (_ST, [_INT, _I64, _INT, _INT, _P, _P]),
+    "sf_bench_l2_gather_rate": (_ST, [_INT, _I64, _P, _I64, _P, _P]),
     "sf_gemm_bf16": (_ST, [_P, _INT, _P, _INT, _P, _I64, _I64, _I64, _I64, _I64, _I64, ctypes.c_float, _INT, _P]),
     "lce_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I64, _I64]),
     "sf_test_device_wait_runs_out": (_ST, [_I64, _P]),
@@ -282,6 +284,15 @@ def sf_gemm_bf16(A, a_layout, B, b_layout, C, M, N, K, lda, ldb, ldc, alpha=1.0,
 
 def sf_bench_gather_rate(ctas, iters, sink, stream=None):
     _check(load().sf_bench_gather_rate(int(ctas), int(iters), _addr(sink), _stream(stream)))
+
+
+def sf_bench_tmem_rate(ctas, iters, x, entries, sink, stream=None):
+    _check(load().sf_bench_tmem_rate(int(ctas), int(iters), int(x), int(entries), _addr(sink), _stream(stream)))
+
+
+def sf_bench_l2_gather_rate(ctas, iters, buf, rows, sink, stream=None):
+    _check(load().sf_bench_l2_gather_rate(int(ctas), int(iters), _addr(buf), int(rows), _addr(sink),
+                                          _stream(stream)))
 
 
 def lce_workspace_bytes(n_tokens, d, vocab, chunk):
