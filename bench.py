@@ -1,35 +1,52 @@
 """Benchmark of the per-layer update step on GB300.
 
-Workload (the headline line): the OPT-1.3B-shaped stack, 24 decoder layers
-(hidden 2048, FFN 8192; QKV, out, FC1, FC2 and two LayerNorms per layer,
-50,339,840 params a layer, 1,208,156,160 in all), seeded synthetic bf16
-gradients N(0, 1e-3) and fp32 master weights N(0, 0.02), all resident in
-HBM.  One step = one fused multi-tensor AdamW launch per layer over all 24
-layers, with t advancing per step.  Metric: params updated per second.
+Workload (the headline line): the LLaMA-2-7B-shaped full-parameter step,
+32 decoder layers (hidden 4096, SwiGLU FFN 11008) plus the vocab-32000
+embedding and LM head and the final norm, 6,738,415,616 params, seeded
+synthetic bf16 gradients N(0, 1e-3) and fp32 master weights N(0, 0.02),
+master/m/v all resident in HBM (108 GB with the bf16 gradient and weight
+arrays).  One step = one fused multi-tensor AdamW launch per group in
+sliding (backward) order: LM head, final norm, layers 31..0, embedding;
+t advances per step.  Metric: params updated per second.
 
 Also on the same line:
-  e2e        the same step through the layer-sliding window: the 24 layers
-             live in pinned host memory and stream through 3 device slots
-             (h2d grad/master/m/v, update, d2h master/m/v/weight), copies
-             inside the timed region.
+  e2e        the same step through the layer-sliding window with the fp32
+             states kept resident in HBM: every step the gradients come
+             from pinned host memory and the bf16 weights go back to it
+             (2 + 2 bytes per param over the host link), copies inside the
+             timed region.
   roofline   of the dominant kernel (the fused AdamW), from CUDA events
              around every launch in the timed region.
+  gpu_launches  kernels one step enqueues (counted from a CUDA-graph
+             capture of a step) times the timed steps.
+  opt13      the OPT-1.3B-shaped stack (24 layers, 50,339,840 params each)
+             resident in HBM, and its end-to-end form through the window
+             with every array in pinned host memory (14 + 14 bytes per
+             param over the link, 3 device slots).
+  mistral_window  four Mistral-Large-123B-shaped layers (1.38 B params
+             each) in pinned host memory streamed through 2 device slots,
+             88 visits: link GB/s each way, overlap efficiency, and the
+             update kernel's HBM fraction on one visit alone.
   lsp        the sparse-projector chain on the seven LLaMA-7B weight
              gradients (compress, compressed AdamW, decompress-apply into
              bf16 W; d = 512, 8 nonzeros per row), per-stage times, the
              chain replayed from CUDA graphs, the projector fit step, and
-             the measured shared-memory gather rate that bounds the chain's
-             kernels (gather_roof) with each stage's fraction of it.
+             the measured on-chip gather rates that bound the chain's
+             kernels (shared memory, tensor memory, L2: gather_roof).
   lce        the fused linear cross-entropy on a Llama-3.1-8B output layer
-             (8192 tokens, V 128256), tensor roofline against the sustained
-             bf16 figure (the calls run under the power cap), with clocks.
+             (8192 tokens, V 128256), tensor roofline against the burst
+             bf16 figure (the sustained one when its clock record shows the
+             power cap), with clocks.
   host_update  the same AdamW on the host cores (the pages' placement).
   cpu_baseline  the fp64 oracle on this machine's host cores, on a bounded
-             sample of the same workload.
+             sample of the same workload, with the CPU model, the cores the
+             process may run on and numpy's BLAS threads.
   clocks     SM clocks and throttle reasons sampled during the timed region.
 
-``--impl reference`` times the fp64 oracle instead (the only reference
-implementation of this path), one bounded sample per step.
+``--workload opt-1.3b`` or ``--workload mistral-window`` put one of the
+other two workloads on the headline instead.  ``--impl reference`` times
+the fp64 oracle instead (the only reference implementation of this path),
+one bounded sample per step.
 
 Multi-GPU (torchrun): every rank runs its own replica of the workload on
 its own GPU; there is no collective on the data path.  ``value`` is the
@@ -68,9 +85,11 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-lce", action="store_true")
     ap.add_argument("--layers", type=int, default=24, help="OPT-1.3B layers (24 = the full stack)")
-    ap.add_argument("--workload", default="opt-1.3b", choices=["opt-1.3b", "llama2-7b", "mistral-window"],
-                    help="opt-1.3b: the headline stack; llama2-7b: the full LLaMA-2-7B step resident in HBM; "
-                         "mistral-window: four Mistral-Large layers in pinned host memory through 2 device slots")
+    ap.add_argument("--workload", default="llama2-7b", choices=["llama2-7b", "opt-1.3b", "mistral-window"],
+                    help="llama2-7b: the full LLaMA-2-7B step resident in HBM (headline); opt-1.3b: the 24-layer "
+                         "OPT-1.3B stack; mistral-window: four Mistral-Large layers in pinned host memory through "
+                         "2 device slots")
+    ap.add_argument("--no-c5", action="store_true", help="leave out the Mistral-Large window sub-object")
     ap.add_argument("--profile-small", action="store_true",
                     help="1 layer, 1 warm-up + 1 timed step, no extras: a small case for ncu captures")
     ap.add_argument("--profile-lce", action="store_true",
@@ -149,8 +168,13 @@ def measured_peak_bf16(sustained=False):
     return (FALLBACK_BF16_TFLOPS_SUSTAINED if sustained else FALLBACK_BF16_TFLOPS), "fallback"
 
 
-def kernel_traffic(kernel):
-    """dram bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+def kernel_traffic(kernel, units_per_launch=None):
+    """dram bytes per launch from a committed ncu summary, if the kernel source is unchanged.
+
+    The capture is of one smaller launch; the update's traffic grows in
+    proportion to the params it updates, so with ``units_per_launch`` the
+    captured bytes are scaled to a launch of that many params.
+    """
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -160,6 +184,10 @@ def kernel_traffic(kernel):
     src = os.path.join(ROOT, d["source"])
     if not os.path.exists(src) or hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != d["source_sha"]:
         return None
+    d = dict(d)
+    if units_per_launch and d.get("unit_params_per_launch"):
+        d["bytes_per_launch"] = d["bytes_per_launch"] * units_per_launch / d["unit_params_per_launch"]
+        d["scaled_from_params"] = d["unit_params_per_launch"]
     return d
 
 
@@ -305,18 +333,97 @@ def make_groups(groups, seed=0):
     return out
 
 
-def workload_groups(args):
+def workload_groups(name, layers=24):
     from layer_optimizer_gb300 import synth
-    if args.workload == "llama2-7b":
+    if name == "llama2-7b":
         return synth.llama7_step_order()
-    return [synth.OPT13_LAYER] * args.layers
+    return [synth.OPT13_LAYER] * layers
 
 
-def run_resident(args, world):
+def _cudart():
+    """The CUDA runtime this process already loaded (torch and the library share it)."""
+    for line in open("/proc/self/maps"):
+        if "libcudart.so" in line:
+            return ctypes.CDLL(line.split()[-1])
+    return ctypes.CDLL("libcudart.so")
+
+
+def kernels_per_call(fn, stream):
+    """Kernel launches `fn()` enqueues on `stream`, counted from a CUDA-graph capture.
+
+    The calls are captured (relaxed mode) into a graph that is never
+    launched, so nothing runs and no state changes on the device.
+    """
+    rt = _cudart()
+    rt.cudaStreamBeginCapture.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    rt.cudaStreamEndCapture.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+    rt.cudaGraphGetNodes.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_size_t)]
+    rt.cudaGraphNodeGetType.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int)]
+    rt.cudaGraphDestroy.argtypes = [ctypes.c_void_p]
+    rt.cudaGetLastError.restype = ctypes.c_int
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    if rt.cudaStreamBeginCapture(sp, 2) != 0:      # cudaStreamCaptureModeRelaxed
+        rt.cudaGetLastError()                        # leave no error behind for the next launch
+        return None
+    graph = ctypes.c_void_p()
+    try:
+        fn()
+    finally:
+        rc = rt.cudaStreamEndCapture(sp, ctypes.byref(graph))
+    if rc != 0 or not graph.value:
+        rt.cudaGetLastError()
+        return None
+    n = ctypes.c_size_t(0)
+    rt.cudaGraphGetNodes(graph, None, ctypes.byref(n))
+    nodes = (ctypes.c_void_p * max(1, n.value))()
+    rt.cudaGraphGetNodes(graph, nodes, ctypes.byref(n))
+    kernels = 0
+    for k in range(n.value):
+        t = ctypes.c_int(-1)
+        rt.cudaGraphNodeGetType(nodes[k], ctypes.byref(t))
+        kernels += t.value == 0                      # cudaGraphNodeTypeKernel
+    rt.cudaGraphDestroy(graph)
+    return kernels
+
+
+def release_pinned():
+    """Hand torch's cached pinned host blocks back to the system."""
+    import torch
+    f = getattr(torch._C, "_host_emptyCache", None)
+    if f is not None:
+        f()
+
+
+def cpu_context():
+    """The host the oracle runs on: CPU model, usable cores, numpy's BLAS threads."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            model = None
+    blas = {k: os.environ[k] for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+            if k in os.environ}
+    return {"cpu_model": model or "unknown", "affinity_cores": len(os.sched_getaffinity(0)),
+            "os_cpu_count": os.cpu_count(),
+            "blas_threads": blas or "library default (all usable cores); the elementwise oracle runs single-threaded"}
+
+
+def run_resident(args, world, groups, keep=False):
     import torch
 
     from layer_optimizer_gb300 import native, synth
-    groups = workload_groups(args)
     layers = make_groups(groups)
     params_per_step = sum(synth.layer_numel(g) for g in groups)
     hp = native.hparams(**HP)
@@ -328,12 +435,14 @@ def run_resident(args, world):
     step = [0]
     n_groups = len(groups)
 
-    def one_step(evs=None):
-        step[0] += 1
+    def one_step(evs=None, t=None, sp=sptr):
+        if t is None:
+            step[0] += 1
+            t = step[0]
         for li, a in enumerate(arrs):
             if evs is not None:
                 evs[li][0].record(stream)
-            st = lib.sf_adamw_layer_step(a, len(descs[li]), ctypes.byref(hp), step[0], sptr)
+            st = lib.sf_adamw_layer_step(a, len(descs[li]), ctypes.byref(hp), t, sp)
             if st != 0:
                 raise native.SfError(st, native.sf_last_error())
             if evs is not None:
@@ -342,6 +451,8 @@ def run_resident(args, world):
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
+    side = torch.cuda.Stream()          # graph capture needs a stream other than the legacy default one
+    per_step = kernels_per_call(lambda: one_step(t=step[0] + 1, sp=side.cuda_stream), side)
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_groups)]
            for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -358,10 +469,98 @@ def run_resident(args, world):
     total_ms = t0.elapsed_time(t1)
     launch_ms = [a.elapsed_time(b) for row in evs for (a, b) in row]
     group_params = [synth.layer_numel(g) for g in groups] * args.steps
-    del layers
+    out = dict(total_ms=total_ms, launch_ms=launch_ms, params_per_step=params_per_step, group_params=group_params,
+               launches=per_step * args.steps if per_step is not None else None, kernels_per_step=per_step,
+               clocks=clk.summary(), steps_done=step[0])
+    if keep:
+        out["layers"] = layers
+    else:
+        del layers
+        torch.cuda.empty_cache()
+    return out
+
+
+def resident_summary(res, args, world):
+    """Value, step time and roofline of a resident run (whole job over the slowest rank)."""
+    total_ms = max_over_ranks(res["total_ms"], world)
+    lm = res["launch_ms"]
+    peak, kind = measured_peak_hbm()
+    achieved = ADAM_BYTES_PER_PARAM * sum(res["group_params"]) / (sum(lm) / 1e3) / 1e9
+    traffic = kernel_traffic("adamw_bulk_kernel", sum(res["group_params"]) / len(res["group_params"]))
+    return {
+        "value": job_value(world, res["params_per_step"], args.steps, total_ms),
+        "ms_per_step": total_ms / args.steps,
+        "roofline": {"bound": "hbm", "kernel": "adamw_bulk_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{kind} ({'of measured' if kind == 'measured' else 'of fallback'})",
+                     "bytes_per_launch": ADAM_BYTES_PER_PARAM * sum(res["group_params"]) / len(res["group_params"]),
+                     "avg_launch_ms": sum(lm) / len(lm),
+                     "traffic": traffic["bytes_per_launch"] if traffic else None},
+    }
+
+
+def run_e2e_states_resident(args, world, groups, layers, start_step):
+    """The resident step through the window: gradients in, bf16 weights out, fp32 states in HBM.
+
+    Each group's gradient and weight arrays are flat pinned host buffers
+    (the gradient holds the same bits as the resident run's); master, m and
+    v are the resident run's device arrays, which the window updates in
+    place.  Three device slots hold one group's gradient and weight each.
+    """
+    import torch
+
+    from layer_optimizer_gb300 import native, synth
+    bf16 = torch.bfloat16
+    host, keep = [], []
+    for gi, grp in enumerate(groups):
+        n = synth.layer_numel(grp)
+        hg = torch.empty(n, dtype=bf16, pin_memory=True)
+        hw = torch.empty(n, dtype=bf16, pin_memory=True)
+        keep += [hg, hw]
+        off, ts = 0, []
+        for ti, (_, c) in enumerate(grp):
+            dg = layers[gi][ti]
+            hg[off:off + c].copy_(dg[0])
+            ts.append([hg[off:off + c], dg[1], dg[2], dg[3], hw[off:off + c]])
+            off += c
+        host.append(ts)
+    torch.cuda.synchronize()
+    # slot tensor i sits at its offset in the largest group; its capacity is
+    # the largest tensor i of any group (a one-tensor group such as the LM
+    # head overlaps the larger group's later tensors, which it never uses)
+    n_t = max(len(g) for g in groups)
+    big = max(groups, key=synth.layer_numel)
+    offs = [sum(c for _, c in big[:i]) for i in range(len(big))]
+    offs += [offs[-1]] * (n_t - len(offs))
+    caps = [max(g[i][1] for g in groups if len(g) > i) for i in range(n_t)]
+    slot_elems = max(o + c for o, c in zip(offs, caps))
+    n_slots = 3
+    slot_bufs = [(torch.empty(slot_elems, dtype=bf16, device="cuda"), torch.empty(slot_elems, dtype=bf16, device="cuda"))
+                 for _ in range(n_slots)]
+    slots = [[native.make_tensor(fg[o:o + c], None, None, None, fw[o:o + c], numel=c) for o, c in zip(offs, caps)]
+             for fg, fw in slot_bufs]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = native.sf_window_create(slots, *streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in host])
+    order = list(range(len(groups)))
+    steps = (ctypes.c_int64 * len(groups))(*([start_step] * len(groups)))
+    hp = native.hparams(**HP)
+    native.sf_slide_window_step(win, hl, order, hp, steps)
+    win.sync()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        native.sf_slide_window_step(win, hl, order, hp, steps)
+    win.sync()
+    wall = time.perf_counter() - t0
+    barrier(world)
+    params = sum(synth.layer_numel(g) for g in groups)
+    win.close()
+    del host, keep, slots, slot_bufs
+    release_pinned()
     torch.cuda.empty_cache()
-    return dict(total_ms=total_ms, launch_ms=launch_ms, params_per_step=params_per_step, group_params=group_params,
-                launches=args.steps * n_groups, clocks=clk.summary())
+    return dict(wall_s=wall, params_per_step=params, h2d=2 * params, d2h=2 * params)
 
 
 def link_probe(nbytes=2 << 30, reps=5):
@@ -639,6 +838,38 @@ def run_lsp(args, matrices=None):
         gather_rate = nsm * 512 * iters * 8 / (ra.elapsed_time(rb) / 1e3)
     except Exception as ex:
         gather_rate = f"gather-rate probe failed: {str(ex)[:120]}"
+    # the other on-chip source: tensor memory (tcgen05.ld of 1, 2 or 4
+    # columns per lane at columns chosen per load, entries from shared
+    # memory), and row gathers straight from L2 (a 48 MB buffer)
+    other_roofs = {}
+    try:
+        def timed_call(fn):
+            fn()
+            torch.cuda.synchronize()
+            ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            fn()
+            eb.record(stream)
+            torch.cuda.synchronize()
+            return ea.elapsed_time(eb) / 1e3
+        tm = {}
+        for x in (1, 2, 4):
+            it = (1 << 14) // x
+            t = timed_call(lambda: native.sf_bench_tmem_rate(nsm, it, x, 1, sink, stream))
+            tm[f"x{x}_macs_per_s"] = nsm * 512 * it * 8 * x / t
+        other_roofs["tmem"] = dict(tm, probe="sf_bench_tmem_rate: 16 warps per SM, 8 tcgen05.ld.32x32b.xN per "
+                                             "wait, column and multiplier per load from a shared-memory entry")
+        rows = 48 * 2048
+        buf = torch.rand(rows, 128, device="cuda")
+        sk = torch.empty(nsm * 2 * 256, device="cuda")
+        t = timed_call(lambda: native.sf_bench_l2_gather_rate(nsm * 2, 256, buf, rows, sk, stream))
+        l2_bytes = nsm * 2 * 8 * 256 * 16 * 512
+        other_roofs["l2_rows"] = {"GBps": l2_bytes / t / 1e9, "macs_per_s_fp32": l2_bytes / 4 / t,
+                                  "probe": "sf_bench_l2_gather_rate: 512-byte rows of a 48 MB buffer, 16 loads in "
+                                           "flight per lane, 2 CTAs of 8 warps per SM"}
+        del buf, sk
+    except Exception as ex:
+        other_roofs = {"error": f"tmem / L2 probes failed: {str(ex)[:120]}"}
     n_params = sum(m * n for (_, m, n, *_r) in mats)
     comp_t = sum(p[2] for p in per) / reps
     ad_t = sum(p[3] for p in per) / reps
@@ -678,7 +909,8 @@ def run_lsp(args, matrices=None):
             "decompress_frac": dec_macs / (dec_t / 1e3) / gather_rate,
             "probe": "sf_bench_gather_rate: 16 warps per SM, 2 entries + 2 float4 tile loads + 8 FMA per step"}
     else:
-        out["gather_roof"] = gather_rate
+        out["gather_roof"] = {"error": gather_rate}
+    out["gather_roof"].update(other_roofs)
     out["ms_per_chain_all7_graph_streams"] = graph_ms_streams
     out["ms_per_chain_all7_host_moments_window"] = host_ms
     if isinstance(host_ms, float):
@@ -732,16 +964,23 @@ def run_lce(args, N=8192, D=4096, V=128256, chunk=4608):
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     flops = 6.0 * N * V * D
-    peak, kind = measured_peak_bf16(sustained=True)
+    # the calls are a burst of well under a second: the burst figure is the
+    # denominator unless this leg's own clock record shows the power cap
+    clocks = clk.summary()
+    capped = "sw_power_cap" in clocks.get("reasons", [])
+    peak, kind = measured_peak_bf16(sustained=capped)
     burst, _ = measured_peak_bf16()
+    sustained, _ = measured_peak_bf16(sustained=True)
     out = {"workload": f"Llama-3.1-8B output layer: {N} tokens, D {D}, V {V}, chunks of {chunk}; bf16 H and W, "
                        "fp32 dH and dW",
            "ms": ms, "tokens_per_s": N / (ms / 1e3),
            "roofline": {"bound": "tensor", "achieved": flops / ms / 1e9, "peak": peak, "unit": "TFLOP/s",
-                        "frac": flops / ms / 1e9 / peak, "peak_kind": f"{kind} sustained (of {kind})",
-                        "frac_of_burst_peak": flops / ms / 1e9 / burst, "flops_per_call": flops},
+                        "frac": flops / ms / 1e9 / peak,
+                        "peak_kind": f"{kind} {'sustained (power cap seen)' if capped else 'burst'} (of {kind})",
+                        "frac_of_sustained_peak": flops / ms / 1e9 / sustained, "flops_per_call": flops,
+                        "timed_region_ms": ms * reps},
            "logits_bytes_full": N * V * 4, "workspace_bytes": wsb, "loss": float(loss.item()), "calls": reps,
-           "clocks": clk.summary()}
+           "clocks": clocks}
     del H, W, dH, dW, ws
     torch.cuda.empty_cache()
     return out
@@ -759,13 +998,14 @@ def host_update_rate(steps=3):
                       torch.empty(n, dtype=torch.bfloat16)])
     ts = [native.make_tensor(*t) for t in layer]
     hp = native.hparams(**HP)
-    native.sf_adamw_host_step(ts, hp, 1)
+    threads = len(os.sched_getaffinity(0))
+    native.sf_adamw_host_step(ts, hp, 1, threads)
     t0 = time.perf_counter()
     for k in range(steps):
-        native.sf_adamw_host_step(ts, hp, k + 2)
+        native.sf_adamw_host_step(ts, hp, k + 2, threads)
     el = (time.perf_counter() - t0) / steps
     n = synth.layer_numel(synth.OPT13_LAYER)
-    return {"params_per_s": n / el, "GBps": ADAM_BYTES_PER_PARAM * n / el / 1e9, "threads": os.cpu_count(),
+    return {"params_per_s": n / el, "GBps": ADAM_BYTES_PER_PARAM * n / el / 1e9, "threads": threads,
             "sample": f"one OPT-1.3B layer ({n} params) in host memory, {steps} steps",
             "note": "SlideFormer's own placement of the update (host cores), same arithmetic and bits as the GPU"}
 
@@ -857,9 +1097,33 @@ def run_mistral_window(args, world):
     per_layer = synth.layer_numel(layer)
     win.close()
     del host, slots
+    release_pinned()
     torch.cuda.empty_cache()
     return dict(wall_s=wall, visits=n_visits, params_per_visit=per_layer, setup_s=setup_s,
                 t_h2d_ms=t_h2d, t_update_ms=t_upd, t_d2h_ms=t_d2h, clocks=clk.summary(), steps=list(steps))
+
+
+def mistral_summary(r, world):
+    """The Mistral-Large window's numbers: rate, link GB/s each way, overlap efficiency, update alone."""
+    wall = max_over_ranks(r["wall_s"], world)
+    params = world * r["params_per_visit"] * r["visits"]
+    link_bytes = 14 * r["params_per_visit"] * r["visits"]
+    bound = max(r["t_h2d_ms"], r["t_update_ms"], r["t_d2h_ms"])
+    peak, kind = measured_peak_hbm()
+    upd_gbs = ADAM_BYTES_PER_PARAM * r["params_per_visit"] / (r["t_update_ms"] / 1e3) / 1e9
+    return {
+        "workload": "Mistral-Large-123B layer (hidden 12288, 96 q / 8 kv heads of 128, SwiGLU FFN 28672; "
+                    "1,384,144,896 params); 4 layers in pinned host memory (88.6 GB), 2 device slots, 88 visits "
+                    "cycling layers 0..3 (22 updates per layer); 3 streams",
+        "value": params / wall, "unit": "params/s", "ms_per_sweep": wall * 1e3, "visits": r["visits"],
+        "h2d_bytes_per_sweep": link_bytes, "d2h_bytes_per_sweep": link_bytes,
+        "link": {"h2d_GBps": link_bytes / wall / 1e9, "d2h_GBps": link_bytes / wall / 1e9,
+                 "one_visit_alone_ms": {"h2d": r["t_h2d_ms"], "update": r["t_update_ms"], "d2h": r["t_d2h_ms"]},
+                 "overlap_efficiency": r["visits"] * bound / 1e3 / wall},
+        "update_alone": {"kernel": "adamw_bulk_kernel", "GBps": upd_gbs, "frac_of_hbm_peak": upd_gbs / peak,
+                         "peak": peak, "peak_kind": kind},
+        "clocks": r["clocks"], "setup_s": r["setup_s"], "steps_per_layer": r["steps"],
+    }
 
 
 def main_window(args, rank, world):
@@ -867,37 +1131,61 @@ def main_window(args, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     from layer_optimizer_gb300 import native
     native.load()
-    r = run_mistral_window(args, world)
-    wall = max_over_ranks(r["wall_s"], world)
-    params = world * r["params_per_visit"] * r["visits"]
-    link_bytes = 14 * r["params_per_visit"] * r["visits"]
-    bound = max(r["t_h2d_ms"], r["t_update_ms"], r["t_d2h_ms"])
-    peak, kind = measured_peak_hbm()
-    upd_gbs = ADAM_BYTES_PER_PARAM * r["params_per_visit"] / (r["t_update_ms"] / 1e3) / 1e9
+    m = mistral_summary(run_mistral_window(args, world), world)
     line = {
         "metric": "params updated/s (layer-sliding window, Mistral-Large-123B layer)",
-        "value": params / wall, "unit": "params/s", "n_gpus": world, "steps": 1, "warmup": 1,
-        "ms_per_step": wall * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "value": m["value"], "unit": "params/s", "n_gpus": world, "steps": 1, "warmup": 1,
+        "ms_per_step": m["ms_per_sweep"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 (bf16 grad in, bf16 weight out)",
         "data": "synthetic (seeded N(0,1e-3) bf16 grads fixed in the host slots, N(0,0.02) fp32 masters)",
-        "config": {"workload": "Mistral-Large-123B layer (hidden 12288, 96 q / 8 kv heads of 128, SwiGLU FFN 28672; "
-                               "1,384,144,896 params); 4 layers in pinned host memory (88.6 GB), 2 device slots, "
-                               "88 visits cycling layers 0..3 (22 updates per layer); 3 streams",
-                   "step": "one 88-visit sweep", "warm-up": "one visit per layer",
+        "config": {"workload": m["workload"], "step": "one 88-visit sweep", "warm-up": "one visit per layer",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "gpu_launches": r["visits"],
-        "e2e": {"value": params / wall, "unit": "params/s", "h2d_bytes_per_step": link_bytes,
-                "d2h_bytes_per_step": link_bytes, "path": "sf_slide_window_step (the measured path itself)"},
-        "link": {"h2d_GBps": link_bytes / wall / 1e9, "d2h_GBps": link_bytes / wall / 1e9,
-                 "one_visit_alone_ms": {"h2d": r["t_h2d_ms"], "update": r["t_update_ms"], "d2h": r["t_d2h_ms"]},
-                 "overlap_efficiency": r["visits"] * bound / 1e3 / wall},
+        "gpu_launches": m["visits"],
+        "e2e": {"value": m["value"], "unit": "params/s", "h2d_bytes_per_step": m["h2d_bytes_per_sweep"],
+                "d2h_bytes_per_step": m["d2h_bytes_per_sweep"],
+                "path": "sf_slide_window_step (the measured path itself)"},
+        "link": m["link"],
         "roofline": {"bound": "host link", "kernel": "adamw_bulk_kernel (in the window)",
-                     "update_alone_GBps": upd_gbs, "update_frac_of_hbm_peak": upd_gbs / peak,
-                     "peak": peak, "peak_kind": kind},
-        "clocks": r["clocks"], "setup_s": r["setup_s"], "steps_per_layer": r["steps"],
+                     "update_alone_GBps": m["update_alone"]["GBps"],
+                     "update_frac_of_hbm_peak": m["update_alone"]["frac_of_hbm_peak"],
+                     "peak": m["update_alone"]["peak"], "peak_kind": m["update_alone"]["peak_kind"]},
+        "clocks": m["clocks"], "setup_s": m["setup_s"], "steps_per_layer": m["steps_per_layer"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+LLAMA_CFG = ("LLaMA-2-7B: 32 layers (hidden 4096, 32 heads, SwiGLU FFN 11008) + embedding + LM head (vocab "
+             "32000) + final norm = 6,738,415,616 params; bf16 grads, fp32 master/m/v resident in HBM; one fused "
+             "AdamW launch per group in sliding order (head, norm, layers 31..0, embedding)")
+OPT_CFG = ("OPT-1.3B stack: 24 layers x 50,339,840 params (hidden 2048, FFN 8192, QKV/O/FC1/FC2 + 2 LayerNorms), "
+           "one fused AdamW launch per layer")
+
+
+def opt13_sub(args, world):
+    """The OPT-1.3B stack: resident rate and roofline, and its window form with every array on the host."""
+    groups = workload_groups("opt-1.3b", args.layers)
+    res = run_resident(args, world, groups)
+    out = {"workload": OPT_CFG, "params_per_step": res["params_per_step"], "steps": args.steps,
+           "clocks": res["clocks"], "l2": "inputs larger than L2 (1.41 GB per launch)"}
+    out.update(resident_summary(res, args, world))
+    out["unit"] = "params/s"
+    if not args.no_e2e:
+        e = run_e2e(args, world)
+        wall = max_over_ranks(e["wall_s"], world)
+        out["e2e_window"] = {
+            "value": world * e["params_per_step"] * args.steps / wall, "unit": "params/s",
+            "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+            "path": "sf_slide_window_step: 24 pinned host layers (flat per-array buffers, every array on the host), "
+                    "3 device slots, 3 streams",
+            "link_GBps_each_way": e["h2d"] * args.steps / wall / 1e9,
+            "same_buffers_plain_copies_GBps_each_way": e["raw_copy_GBps_each_way"]}
+        try:
+            out["e2e_window"]["link_probe"] = link_probe()
+        except Exception as ex:
+            out["e2e_window"]["link_probe"] = {"error": str(ex)[:200]}
+        release_pinned()
+    return out
 
 
 def main_ours(args, rank, world):
@@ -905,42 +1193,28 @@ def main_ours(args, rank, world):
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     from layer_optimizer_gb300 import native
     native.load()
-    res = run_resident(args, world)
-    total_ms = max_over_ranks(res["total_ms"], world)
-    ms_per_step = total_ms / args.steps
-    value = job_value(world, res["params_per_step"], args.steps, total_ms)
-    lm = res["launch_ms"]
-    avg_launch_ms = sum(lm) / len(lm)
-    bytes_per_launch = ADAM_BYTES_PER_PARAM * sum(res["group_params"]) / len(res["group_params"])
-    # algorithmic bytes of all launches over their summed durations
-    achieved = ADAM_BYTES_PER_PARAM * sum(res["group_params"]) / (sum(lm) / 1e3) / 1e9
-    peak, kind = measured_peak_hbm()
-    # layers above 2^20 aligned elements run the bulk-copy kernel (one launch per layer)
-    kname = "adamw_bulk_kernel"
-    traffic = kernel_traffic(kname)
-    if args.workload == "llama2-7b":
+    llama = args.workload == "llama2-7b"
+    groups = workload_groups(args.workload, args.layers)
+    res = run_resident(args, world, groups, keep=llama and not args.no_e2e)
+    summ = resident_summary(res, args, world)
+    if llama:
         metric = "params updated/s (fused AdamW, LLaMA-2-7B full step)"
-        cfg = {"workload": "LLaMA-2-7B: 32 layers (hidden 4096, SwiGLU FFN 11008) + embedding + LM head "
-                           "(vocab 32000) + final norm = 6,738,415,616 params resident in HBM, one fused AdamW "
-                           "launch per group in sliding order (head, norm, layers 31..0, embedding)",
-               "groups": len(workload_groups(args)), "params_per_step": res["params_per_step"],
+        cfg = {"workload": LLAMA_CFG, "groups": len(groups), "params_per_step": res["params_per_step"],
                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-               "l2": "inputs larger than L2"}
+               "l2": "inputs larger than L2 (up to 4.1 GB per launch)"}
     else:
         metric = "params updated/s (fused AdamW, OPT-1.3B stack)"
-        cfg = {"workload": "OPT-1.3B stack: 24 layers x 50,339,840 params (hidden 2048, FFN 8192, "
-                           "QKV/O/FC1/FC2 + 2 LayerNorms), one fused AdamW launch per layer",
-               "layers": args.layers, "params_per_step": res["params_per_step"],
+        cfg = {"workload": OPT_CFG, "layers": args.layers, "params_per_step": res["params_per_step"],
                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                "l2": "inputs larger than L2 (1.41 GB per launch)"}
     line = {
         "metric": metric,
-        "value": value,
+        "value": summ["value"],
         "unit": "params/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
+        "ms_per_step": summ["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -948,36 +1222,53 @@ def main_ours(args, rank, world):
         "data": "synthetic (seeded N(0,1e-3) bf16 grads, N(0,0.02) fp32 masters)",
         "config": cfg,
         "gpu_launches": res["launches"],
-        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved,
-                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": f"{kind} ({'of measured' if kind == 'measured' else 'of fallback'})",
-                     "bytes_per_launch": bytes_per_launch, "avg_launch_ms": avg_launch_ms,
-                     "traffic": traffic["bytes_per_launch"] if traffic else None},
+        "kernels_per_step": res["kernels_per_step"],
+        "roofline": summ["roofline"],
         "clocks": res["clocks"],
     }
-    if not args.no_e2e and args.workload == "opt-1.3b":
-        e = run_e2e(args, world)
-        wall = max_over_ranks(e["wall_s"], world)
-        line["e2e"] = {"value": world * e["params_per_step"] * args.steps / wall, "unit": "params/s",
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
-                       "path": "sf_slide_window_step: 24 pinned host layers (flat per-array buffers), 3 device slots, 3 streams",
-                       "link_GBps_each_way": e["h2d"] * args.steps / wall / 1e9,
-                       "same_buffers_plain_copies_GBps_each_way": e["raw_copy_GBps_each_way"]}
+    if not args.no_e2e:
+        if llama:
+            e = run_e2e_states_resident(args, world, groups, res.pop("layers"), res["steps_done"])
+            wall = max_over_ranks(e["wall_s"], world)
+            line["e2e"] = {"value": world * e["params_per_step"] * args.steps / wall, "unit": "params/s",
+                           "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                           "path": "sf_slide_window_step with master/m/v resident in HBM: each step every "
+                                   "group's bf16 gradients come from pinned host memory and its bf16 weights go "
+                                   "back (3 device slots, 3 streams)",
+                           "link_GBps_each_way": e["h2d"] * args.steps / wall / 1e9}
+        else:
+            e = run_e2e(args, world)
+            wall = max_over_ranks(e["wall_s"], world)
+            line["e2e"] = {"value": world * e["params_per_step"] * args.steps / wall, "unit": "params/s",
+                           "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"],
+                           "path": "sf_slide_window_step: 24 pinned host layers (flat per-array buffers), 3 device "
+                                   "slots, 3 streams",
+                           "link_GBps_each_way": e["h2d"] * args.steps / wall / 1e9,
+                           "same_buffers_plain_copies_GBps_each_way": e["raw_copy_GBps_each_way"]}
+            release_pinned()
+    res.pop("layers", None)
+    torch.cuda.empty_cache()
+    if llama:
         try:
-            line["e2e"]["link_probe"] = link_probe()
+            line["opt13"] = opt13_sub(args, world)
         except Exception as ex:
-            line["e2e"]["link_probe"] = {"error": str(ex)[:200]}
-    if not args.no_lsp and rank == 0 and args.workload == "opt-1.3b":
+            line["opt13"] = {"error": str(ex)[:300]}
+        if not args.no_c5:
+            try:
+                line["mistral_window"] = mistral_summary(run_mistral_window(args, world), world)
+            except Exception as ex:
+                line["mistral_window"] = {"error": str(ex)[:300]}
+    if not args.no_lsp and rank == 0:
         try:
             line["lsp"] = run_lsp(args)
         except Exception as ex:  # the line still prints; the failure is recorded on it
             line["lsp"] = {"error": str(ex)[:300]}
-    if not args.no_lce and rank == 0 and args.workload == "opt-1.3b":
+    if not args.no_lce and rank == 0:
         try:
             line["lce"] = run_lce(args)
         except Exception as ex:
             line["lce"] = {"error": str(ex)[:300]}
-    if not args.no_cpu and rank == 0 and args.workload == "opt-1.3b":
+    if not args.no_cpu and rank == 0:
         line["host_update"] = host_update_rate()
         # the oracle beside the other two workloads (bounded samples)
         if isinstance(line.get("lsp"), dict) and "error" not in line["lsp"]:
@@ -987,8 +1278,10 @@ def main_ours(args, rank, world):
     if not args.no_cpu and rank == 0:
         v, done, el = oracle_params_per_s()
         line["cpu_baseline"] = {"value": v, "unit": "params/s", "cores": 1, "kind": "oracle",
-                                "sample": f"fp64 numpy AdamW on 2^21-param chunks of an OPT-1.3B tensor, "
-                                          f"{done} params in {el:.1f} s (elementwise numpy: one thread)"}
+                                "sample": f"fp64 numpy AdamW on 2^21-param chunks of a "
+                                          f"{'LLaMA-2-7B q' if llama else 'OPT-1.3B'} tensor, {done} params in "
+                                          f"{el:.1f} s (elementwise numpy: one thread)"}
+        line["cpu_baseline"].update(cpu_context())
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -1006,13 +1299,15 @@ def main_reference(args, rank, world):
     value = total_done / total_el
     line = {
         "impl": "reference",
-        "metric": "params updated/s (fused AdamW, OPT-1.3B stack)",
+        "metric": ("params updated/s (fused AdamW, LLaMA-2-7B full step)" if args.workload == "llama2-7b"
+                   else "params updated/s (fused AdamW, OPT-1.3B stack)"),
         "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "OPT-1.3B stack (bounded sample: one 2^21-param chunk per step)"},
+        "config": {"workload": (LLAMA_CFG if args.workload == "llama2-7b" else OPT_CFG) +
+                   " (bounded sample: one 2^21-param chunk per step)"},
         "cpu_baseline": {"value": value, "unit": "params/s", "cores": 1, "kind": "oracle",
-                         "sample": "one 2^21-param chunk of an OPT-1.3B tensor per step"},
+                         "sample": "one 2^21-param chunk of a weight tensor per step"},
         "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -1021,8 +1316,9 @@ def main_reference(args, rank, world):
 def main():
     args = parse()
     if args.profile_small:
+        args.workload = "opt-1.3b"
         args.layers, args.steps, args.warmup = 1, 1, 1
-        args.no_e2e = args.no_lsp = args.no_cpu = True
+        args.no_e2e = args.no_lsp = args.no_cpu = args.no_lce = True
     if args.profile_lce:
         import torch
         from layer_optimizer_gb300 import native

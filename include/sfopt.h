@@ -200,10 +200,11 @@ sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G,
  * cudaFree, no allocating library routine.
  *  - Shapes whose lsp_workspace_bytes(m, n, d) exceeds the array are
  *    rejected with SF_ERR_UNSUPPORTED and a message (for example
- *    d = 512 covers n up to about 11,000 columns).
- *  - The first call on a device looks up the array's device address on the
- *    current device (cudaGetSymbolAddress) and caches it; make that first
- *    call before any stream capture.
+ *    d = 512 covers n up to 16,384 columns).
+ *  - Every call looks up the array's device address on the current device
+ *    (cudaGetSymbolAddress), so the address stays right after a device
+ *    reset; the first call on a device may also load the library's device
+ *    code there, so make that first call before any stream capture.
  *  - Every call, on any stream, shares the one array, which keeps the last
  *    call's contents: calls that overlap on the GPU race and give undefined
  *    results.  Serialise them (one stream, or events).  Nothing in the
@@ -366,10 +367,17 @@ sf_status lsp_projector_export_values(lsp_projector p, float* val, void* stream)
  * consecutive tensors whose host arrays and slot arrays both follow one
  * another in memory move as one copy (a layer kept as flat per-array
  * buffers moves as one copy per array); the bytes moved are the same.
- * Host-layer pointers must be pinned (page-locked) host memory.  The call
- * returns when everything is enqueued; `steps` (int64 [n_layers], host) is
- * updated on return.  Host buffers of a layer must not be touched until its
- * copies have ended (sf_window_sync).
+ * Host-layer pointers must be pinned (page-locked) host memory, except that
+ * any array of a layer may instead be device memory of the current device
+ * (for instance fp32 master weights and moments kept resident in HBM while
+ * gradients come from and bf16 weights go back to pinned host memory): such
+ * an array is updated in place, is neither copied in nor written back, and
+ * the slot's buffer for it is not used and may be NULL (a slot buffer may be
+ * NULL only for arrays that every layer passing through keeps in device
+ * memory; SF_ERR_INVALID otherwise).  The call returns when everything is
+ * enqueued; `steps` (int64 [n_layers], host) is updated on return.  Host
+ * buffers of a layer must not be touched until its copies have ended
+ * (sf_window_sync).
  * ---------------------------------------------------------------------- */
 typedef struct sf_window_s* sf_window;
 

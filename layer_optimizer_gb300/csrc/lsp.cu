@@ -1217,13 +1217,17 @@ CompressPlan plan_compress(int64_t m, int64_t n, int d) {
   CompressPlan c;
   c.g1 = plan_gather(m, n, d);
   c.g2 = plan_gather(n, d, d);
+  // stage 2 reads R^T (at the workspace's 256-byte aligned start) with the
+  // row gather whenever its rows are 16-byte multiples; only otherwise does
+  // it take the staged gather, whose row splits need partials
+  c.stage2_rows = d % 4 == 0;
   size_t off = 0;
   c.off_rt = off;
   off = align_up(off + (size_t)n * d * 4, 256);
   c.off_rtp = off;
   if (c.g1.splits > 1) off = align_up(off + (size_t)c.g1.splits * n * d * 4, 256);
   c.off_sp = off;
-  if (c.g2.splits > 1) off = align_up(off + (size_t)c.g2.splits * d * d * 4, 256);
+  if (!c.stage2_rows && c.g2.splits > 1) off = align_up(off + (size_t)c.g2.splits * d * d * 4, 256);
   c.bytes = off;
   return c;
 }
@@ -1540,28 +1544,16 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SF_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
-// Device address of the scratch array on the current device, looked up once
-// per device with that device current.  In host code the array's name is only
-// a host-side stand-in, never a device address, so it is never passed to a kernel.
+// Device address of the scratch array on the current device.  In host code
+// the array's name is only a host-side stand-in, never a device address, so
+// it is never passed to a kernel.  The address is looked up on every call
+// (a lookup costs little next to a compress): a cached one would go stale
+// when the device is reset and the library's device code loaded anew.
 sf_status noalloc_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kNoAllocMaxDevices)
-    return fail(SF_ERR_UNSUPPORTED, "lsp_compress_noalloc supports device ids below %d (got %d)", kNoAllocMaxDevices,
-                dev);
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
-    g_noalloc_ptr[dev] = p;
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+  *out = p;
   return SF_OK;
 }
 

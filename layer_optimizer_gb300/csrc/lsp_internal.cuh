@@ -47,6 +47,7 @@ struct GatherPlan {
 // The two gathers of lsp_compress and the workspace they use.
 struct CompressPlan {
   GatherPlan g1, g2;
+  bool stage2_rows;     // stage 2 as the row gather straight from L2 (no partials)
   size_t off_rt, off_rtp, off_sp, bytes;
 };
 

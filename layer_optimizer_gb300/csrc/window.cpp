@@ -19,7 +19,11 @@
 // that tensor's write-back has ended.  Copies go per array of a group, and
 // tensors whose host and slot arrays both follow one another in memory
 // move as one copy (a layer kept as flat per-array buffers, as flattened
-// optimizer states are, costs one copy per array).  It does no arithmetic of its own;
+// optimizer states are, costs one copy per array).  An array of a layer that
+// already lives in this device's memory (say fp32 master weights and
+// moments kept resident in HBM while gradients arrive from and bf16 weights
+// return to the host) is updated in place and never copied: the window then
+// moves only the host-resident arrays.  It does no arithmetic of its own;
 // dependencies are CUDA events only, and the host never blocks while
 // enqueueing.
 #include <algorithm>
@@ -40,11 +44,15 @@ struct sf_window_s {
   std::vector<std::vector<sf_tensor>> slots;
   cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
   // per (slot, tensor): events of the group that starts at that tensor:
-  // its copies landed / its update ended / its write-back ended
-  std::vector<cudaEvent_t> ev_in, ev_done, ev_free;
-  // per (slot, tensor): index (into ev_free) of the write-back event of the
-  // group that last held that tensor of the slot; -1 = never used
-  std::vector<int> free_ev;
+  // its copies landed / its update ended
+  std::vector<cudaEvent_t> ev_in, ev_done;
+  // per (slot, tensor): the write-back of the group that last held that
+  // tensor of the slot has ended (recorded for every tensor of the group),
+  // and the number of that group's recording (0 = never used), so a group
+  // waits once per distinct earlier group
+  std::vector<cudaEvent_t> ev_free;
+  std::vector<int64_t> free_gen;
+  int64_t gen = 0;
   std::vector<cudaEvent_t> ev_layer;   // write-back of a host layer has landed
   std::vector<bool> layer_pending;
   int64_t visits = 0;                  // running visit counter (slot rotation)
@@ -88,21 +96,23 @@ inline size_t part_bytes(Part k) { return (k == kGrad || k == kWeight) ? 2 : 4; 
 // Tensors whose host arrays and slot arrays both follow one another in
 // memory (a layer kept as flat per-array buffers, as flattened optimizer
 // states are) move as one copy: one descriptor instead of one per tensor.
-// A tensor without that array (a NULL weight) ends a run and is skipped.
-sf_status copy_runs(const sf_host_layer& L, const std::vector<sf_tensor>& slot, int t0, int t1, Part k,
-                    cudaMemcpyKind kind, cudaStream_t s, const char* what) {
+// A tensor without that array (a NULL weight) or whose array is resident in
+// device memory (bit k of resident[t]) ends a run and is skipped.
+sf_status copy_runs(const sf_host_layer& L, const std::vector<sf_tensor>& slot, const uint8_t* resident, int t0,
+                    int t1, Part k, cudaMemcpyKind kind, cudaStream_t s, const char* what) {
   const size_t es = part_bytes(k);
+  auto moves = [&](int t) { return part_ptr(L.tensors[t], k) != nullptr && !((resident[t] >> k) & 1); };
   int t = t0;
   while (t < t1) {
     char* h = static_cast<char*>(part_ptr(L.tensors[t], k));
     char* d = static_cast<char*>(part_ptr(slot[t], k));
-    if (!h) {
+    if (!moves(t)) {
       ++t;
       continue;
     }
     size_t bytes = es * (size_t)L.tensors[t].numel;
     int u = t + 1;
-    while (u < t1 && part_ptr(L.tensors[u], k) == h + bytes && part_ptr(slot[u], k) == d + bytes) {
+    while (u < t1 && moves(u) && part_ptr(L.tensors[u], k) == h + bytes && part_ptr(slot[u], k) == d + bytes) {
       bytes += es * (size_t)L.tensors[u].numel;
       ++u;
     }
@@ -124,7 +134,7 @@ sf_status new_event(cudaEvent_t* e) {
   return r == cudaSuccess ? SF_OK : sf::cuda_fail(r, "cudaEventCreate");
 }
 
-sf_status check_layer(const sf_window_s* w, const sf_host_layer& L, int li) {
+sf_status check_layer(const sf_window_s* w, const sf_host_layer& L, int li, const uint8_t* resident) {
   if (L.n_tensors < 0 || L.n_tensors > w->n_tensors)
     return sf::fail(SF_ERR_INVALID, "layer %d: %d tensors, window slots hold %d", li, L.n_tensors,
                     w->n_tensors);
@@ -140,11 +150,26 @@ sf_status check_layer(const sf_window_s* w, const sf_host_layer& L, int li) {
       if (h.numel > d.numel)
         return sf::fail(SF_ERR_INVALID, "layer %d tensor %d: numel %lld exceeds slot capacity %lld",
                         li, t, (long long)h.numel, (long long)d.numel);
-      if (h.weight && !d.weight)
-        return sf::fail(SF_ERR_INVALID, "layer %d tensor %d: slot has no weight buffer", li, t);
+      // a slot array may be NULL only where the layer's array is device-resident
+      for (int k = kGrad; k <= kWeight; ++k)
+        if (part_ptr(h, (Part)k) && !((resident[t] >> k) & 1) && !part_ptr(d, (Part)k))
+          return sf::fail(SF_ERR_INVALID, "layer %d tensor %d: array %d is in host memory but the slot has no buffer "
+                                          "for it", li, t, k);
     }
   }
   return SF_OK;
+}
+
+// Bit k of out[t]: array k of tensor t of the layer is in this device's memory.
+void residency(const sf_host_layer& L, uint8_t* out) {
+  for (int t = 0; t < L.n_tensors; ++t) {
+    uint8_t r = 0;
+    for (int k = kGrad; k <= kWeight; ++k) {
+      const void* p = part_ptr(L.tensors[t], (Part)k);
+      if (p && sf::on_current_device(p)) r |= (uint8_t)(1u << k);
+    }
+    out[t] = r;
+  }
 }
 
 }  // namespace
@@ -179,7 +204,7 @@ sf_status sf_window_create(int n_slots, const sf_tensor* const* device_slots, in
   w->ev_in.assign(ne, nullptr);
   w->ev_done.assign(ne, nullptr);
   w->ev_free.assign(ne, nullptr);
-  w->free_ev.assign(ne, -1);
+  w->free_gen.assign(ne, 0);
   for (int e = 0; e < ne; ++e) {
     sf_status st = SF_OK;
     if ((st = new_event(&w->ev_in[e])) != SF_OK || (st = new_event(&w->ev_done[e])) != SF_OK ||
@@ -207,8 +232,12 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
   for (int v = 0; v < n_order; ++v)
     if (order[v] < 0 || order[v] >= n_layers)
       return sf::fail(SF_ERR_INVALID, "order[%d] = %d out of [0, %d)", v, order[v], n_layers);
+  // which arrays of each layer are already in this device's memory
+  std::vector<uint8_t> resident((size_t)n_layers * std::max(1, w->n_tensors), 0);
   for (int l = 0; l < n_layers; ++l) {
-    SF_TRY(check_layer(w, layers[l], l));
+    if (layers[l].n_tensors > 0 && layers[l].n_tensors <= w->n_tensors && layers[l].tensors)
+      residency(layers[l], resident.data() + (size_t)l * w->n_tensors);
+    SF_TRY(check_layer(w, layers[l], l, resident.data() + (size_t)l * w->n_tensors));
     if (steps[l] < 0) return sf::fail(SF_ERR_INVALID, "steps[%d] < 0", l);
   }
   if ((int)w->ev_layer.size() < n_layers) {
@@ -226,6 +255,8 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
     const std::vector<sf_tensor>& slot = w->slots[s];
     const int eb = s * w->n_tensors;          // this slot's events
     const int64_t step = steps[l] + 1;
+    // arrays already in this device's memory are used in place
+    const uint8_t* res = resident.data() + (size_t)l * w->n_tensors;
 
     // the previous write-back of this layer must have landed before it is read again
     if (w->layer_pending[l])
@@ -238,36 +269,48 @@ sf_status sf_slide_window_step(sf_window w, const sf_host_layer* layers, int n_l
 
       // h2d: the slot's tensors of this group are free (one wait per distinct
       // earlier group that held them), then copy in
-      int last = -2;
+      int64_t last = -1;
       for (int t = t0; t < t1; ++t) {
-        const int e = w->free_ev[eb + t];
-        if (e >= 0 && e != last) SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_free[e], 0), "wait slot tensor free");
-        last = e;
+        const int64_t g = w->free_gen[eb + t];
+        if (g > 0 && g != last)
+          SF_CUDA_TRY(cudaStreamWaitEvent(w->h2d, w->ev_free[eb + t], 0), "wait slot tensor free");
+        last = g;
       }
-      SF_TRY(copy_runs(L, slot, t0, t1, kGrad, cudaMemcpyHostToDevice, w->h2d, "h2d grad"));
-      SF_TRY(copy_runs(L, slot, t0, t1, kMaster, cudaMemcpyHostToDevice, w->h2d, "h2d master"));
-      SF_TRY(copy_runs(L, slot, t0, t1, kExpAvg, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg"));
-      SF_TRY(copy_runs(L, slot, t0, t1, kExpAvgSq, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg_sq"));
+      SF_TRY(copy_runs(L, slot, res, t0, t1, kGrad, cudaMemcpyHostToDevice, w->h2d, "h2d grad"));
+      SF_TRY(copy_runs(L, slot, res, t0, t1, kMaster, cudaMemcpyHostToDevice, w->h2d, "h2d master"));
+      SF_TRY(copy_runs(L, slot, res, t0, t1, kExpAvg, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg"));
+      SF_TRY(copy_runs(L, slot, res, t0, t1, kExpAvgSq, cudaMemcpyHostToDevice, w->h2d, "h2d exp_avg_sq"));
       SF_CUDA_TRY(cudaEventRecord(w->ev_in[eb + t0], w->h2d), "record ev_in");
 
-      // compute: the fused update of the group
+      // compute: the fused update of the group, on the slot's copy of each
+      // array or on the array itself where it is device-resident
       SF_CUDA_TRY(cudaStreamWaitEvent(w->comp, w->ev_in[eb + t0], 0), "wait ev_in");
       for (int t = t0; t < t1; ++t) {
+        const sf_tensor& h = L.tensors[t];
+        const uint8_t r = res[t];
         dev[t] = slot[t];
-        dev[t].numel = L.tensors[t].numel;
-        if (!L.tensors[t].weight) dev[t].weight = nullptr;
+        dev[t].numel = h.numel;
+        if (r & (1u << kGrad)) dev[t].grad = h.grad;
+        if (r & (1u << kMaster)) dev[t].master = h.master;
+        if (r & (1u << kExpAvg)) dev[t].exp_avg = h.exp_avg;
+        if (r & (1u << kExpAvgSq)) dev[t].exp_avg_sq = h.exp_avg_sq;
+        if (!h.weight) dev[t].weight = nullptr;
+        else if (r & (1u << kWeight)) dev[t].weight = h.weight;
       }
       SF_TRY(sf::adamw_layer_step_impl(dev.data() + t0, t1 - t0, hp, step, w->comp));
       SF_CUDA_TRY(cudaEventRecord(w->ev_done[eb + t0], w->comp), "record ev_done");
 
       // d2h: write the group back; each tensor of the slot is free when its copies end
       SF_CUDA_TRY(cudaStreamWaitEvent(w->d2h, w->ev_done[eb + t0], 0), "wait ev_done");
-      SF_TRY(copy_runs(L, slot, t0, t1, kMaster, cudaMemcpyDeviceToHost, w->d2h, "d2h master"));
-      SF_TRY(copy_runs(L, slot, t0, t1, kExpAvg, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg"));
-      SF_TRY(copy_runs(L, slot, t0, t1, kExpAvgSq, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg_sq"));
-      SF_TRY(copy_runs(L, slot, t0, t1, kWeight, cudaMemcpyDeviceToHost, w->d2h, "d2h weight"));
-      SF_CUDA_TRY(cudaEventRecord(w->ev_free[eb + t0], w->d2h), "record ev_free");
-      for (int t = t0; t < t1; ++t) w->free_ev[eb + t] = eb + t0;
+      SF_TRY(copy_runs(L, slot, res, t0, t1, kMaster, cudaMemcpyDeviceToHost, w->d2h, "d2h master"));
+      SF_TRY(copy_runs(L, slot, res, t0, t1, kExpAvg, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg"));
+      SF_TRY(copy_runs(L, slot, res, t0, t1, kExpAvgSq, cudaMemcpyDeviceToHost, w->d2h, "d2h exp_avg_sq"));
+      SF_TRY(copy_runs(L, slot, res, t0, t1, kWeight, cudaMemcpyDeviceToHost, w->d2h, "d2h weight"));
+      const int64_t g = ++w->gen;
+      for (int t = t0; t < t1; ++t) {
+        SF_CUDA_TRY(cudaEventRecord(w->ev_free[eb + t], w->d2h), "record ev_free");
+        w->free_gen[eb + t] = g;
+      }
       t0 = t1;
     }
     steps[l] = step;

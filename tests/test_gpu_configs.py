@@ -37,7 +37,7 @@ def _check_step(pre, post, g64, t, what):
 
 
 def test_llama2_7b_full_step_sampled():
-    """All 6,738,415,616 params resident; two steps in sliding order."""
+    """All 6,738,415,616 params resident; the workload's ten steps in sliding order, fresh gradients each step."""
     groups = synth.llama7_step_order()
     assert sum(synth.layer_numel(g) for g in groups) == 6738415616
     rng = np.random.default_rng(0)
@@ -52,7 +52,7 @@ def test_llama2_7b_full_step_sampled():
         bufs.append(ts)
         idx.append(ix)
     hp = native.hparams(**HP)
-    for t in (1, 2):
+    for t in range(1, 11):
         pre = []
         for li, grp in enumerate(groups):
             for ti, (_, n) in enumerate(grp):
@@ -85,7 +85,13 @@ def _host_gb():
 
 @pytest.mark.skipif(_host_gb() < 160, reason="needs ~90 GB of pinned host memory")
 def test_mistral_large_window_sampled():
-    """Four 1.38 B-param layers in pinned host memory, 2 device slots, two sweeps."""
+    """Four 1.38 B-param layers in pinned host memory, 2 device slots, the full 88-visit sweep.
+
+    The gradients stay fixed in the host slots, so each layer takes 22
+    AdamW steps with the same g; the oracle runs the same 22 steps on the
+    sampled elements (chained: the fp32 state may drift from the fp64 one by
+    one rounding per step).
+    """
     layer = synth.MISTRAL_LAYER
     caps = [n for _, n in layer]
     rng = np.random.default_rng(1)
@@ -114,17 +120,27 @@ def test_mistral_large_window_sampled():
     hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in host])
     steps = (ctypes.c_int64 * 4)()
     hp = native.hparams(**HP)
-    for sweep in (1, 2):
-        pre = [[(f64(b[1][ix]), f64(b[2][ix]), f64(b[3][ix]), f64(b[0][ix].float())) for b, ix in zip(L, I)]
-               for L, I in zip(host, idx)]
-        native.sf_slide_window_step(win, hl, [0, 1, 2, 3], hp, steps)
-        win.sync()
-        assert list(steps) == [sweep] * 4
-        for li in range(4):
-            for ti, (b, ix) in enumerate(zip(host[li], idx[li])):
-                th, m, v, g64 = pre[li][ti]
-                _check_step((th, m, v), (b[1][ix], b[2][ix], b[3][ix], bits(b[4][ix])), g64, sweep,
-                            f"layer {li} tensor {ti} sweep {sweep}")
+    pre = [[(f64(b[1][ix]), f64(b[2][ix]), f64(b[3][ix]), f64(b[0][ix].float())) for b, ix in zip(L, I)]
+           for L, I in zip(host, idx)]
+    native.sf_slide_window_step(win, hl, [v % 4 for v in range(88)], hp, steps)
+    win.sync()
+    assert list(steps) == [22] * 4
+    for li in range(4):
+        for ti, (b, ix) in enumerate(zip(host[li], idx[li])):
+            th, m, v, g64 = pre[li][ti]
+            st = oa.AdamWState(th, m, v)
+            for t in range(1, 23):
+                oa.adamw_step(st, g64, t, **HP)
+            what = f"layer {li} tensor {ti} after 22 visits"
+            check_close(f"{what} master", b[1][ix], st.theta, st.theta_abs, TOL_STATE * 22)
+            check_close(f"{what} m", b[2][ix], st.m, st.m_abs, TOL_STATE * 22)
+            check_close(f"{what} v", b[3][ix], st.v, st.v_abs, TOL_STATE * 22)
+            # chained: the bf16 weight is the kernel's own fp32 master rounded
+            # to nearest even (exactly), the master being within the bound above
+            check_bf16(f"{what} w", bits(b[4][ix]), f64(b[1][ix]), max_ulp=0)
     win.close()
     del host, slots
     torch.cuda.empty_cache()
+    f = getattr(torch._C, "_host_emptyCache", None)
+    if f is not None:
+        f()

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from _util import f64
+from _util import check_close, f64
 from layer_optimizer_gb300 import native, synth
 from oracle.lce import lce
 
@@ -120,9 +120,14 @@ def test_lce_rejects_and_flags():
 @pytest.mark.slow
 def test_lce_llama31_head_full_size_sampled():
     # the benchmark's configuration: 8192 tokens of a Llama-3.1-8B output
-    # layer in chunks of 4608; rows of dH checked against the oracle one by
-    # one, and dW through a property that holds at any size: every row of
-    # dZ sums to zero, so the sum of dW over the vocabulary is zero
+    # layer in chunks of 4608.  The oracle takes every token's log-sum-exp
+    # in fp64 over vocabulary chunks (the 8192 x 128256 logits are never
+    # held), then gives rows of dH (tokens at the chunk edges and an
+    # unlabelled one) and rows of dW (vocabulary ids at tile edges and ids
+    # that are labels), each compared element by element with the kernels'.
+    # dW also keeps a property that holds at any size: every row of dZ sums
+    # to zero, so the sum of dW over the vocabulary is zero.
+    from oracle.lce import lce_rows, token_lse
     N, D, V, chunk = 8192, 4096, 128256, 4608
     H = synth.fill_normal_(torch.empty(N, D, dtype=torch.bfloat16, device=DEV), 1.0, synth.sub_seed(31, 0))
     W = synth.fill_normal_(torch.empty(V, D, dtype=torch.bfloat16, device=DEV), 0.02, synth.sub_seed(31, 1))
@@ -132,24 +137,25 @@ def test_lce_llama31_head_full_size_sampled():
     y[::97] = -100
     loss, dH, dW = _run(H, W, y, chunk)
     n = int((y != -100).sum())
-    rows = [0, 1, 97, 4607, 4608, 5000, N - 1]
-    W64 = f64(W)
-    Hs = f64(H[rows])
-    Z = Hs @ W64.T
-    Z -= Z.max(axis=1, keepdims=True)
-    Pr = np.exp(Z)
-    Pr /= Pr.sum(axis=1, keepdims=True)
-    ys = y[rows].cpu().numpy()
-    dZ = np.where((ys != -100)[:, None], Pr, 0.0)
-    for r, yy in enumerate(ys):
-        if yy != -100:
-            dZ[r, yy] -= 1.0
-    dZ /= n
-    ref, mag = dZ @ W64, np.abs(dZ) @ np.abs(W64)
-    err = np.abs(f64(dH[rows]) - ref)
-    assert not (err > TOL_GRAD * mag + 1e-30).any(), float((err / (mag + 1e-30)).max())
+    H64, W32, y_np = f64(H), W.float().cpu().numpy(), y.cpu().numpy()
+    lse = token_lse(H64, W32, chunk=8192)
+    trows = [0, 1, 97, 4607, 4608, 5000, N - 1]
+    vrows = [0, 1, 255, 256, 65535, V - 1, int(y_np[3]), int(y_np[4700])]
+    ref = lce_rows(H64, W32, y_np, lse, trows, vrows)
+    assert ref["n"] == n
+    check_close("dH rows", dH[trows], ref["dH"], ref["dH_abs"], TOL_GRAD)
+    check_close("dW rows", dW[vrows], ref["dW"], ref["dW_abs"], TOL_GRAD)
     assert not dH[97].any()                               # an unlabelled token has no gradient
     colsum = dW.double().sum(dim=0)
     bound = TOL_GRAD * (2.0 / n) * H.double().abs().sum(dim=0) + 1e-12
     assert bool((colsum.abs() <= bound).all()), float((colsum.abs() / bound).max())
+    # the loss from the same log-sum-exps: mean over labelled tokens of lse - z_y,
+    # within the bound of the small-size tests with each row's largest |H||W|^T
+    # term sum bounded above by |H_i| . max_v |W_v| (no full product needed)
+    lab = np.flatnonzero(y_np != -100)
+    z_y = np.einsum("ij,ij->i", H64[lab], W32[y_np[lab]].astype(np.float64))
+    want = float(np.mean(lse[lab] - z_y))
+    row_bound = np.abs(H64) @ np.abs(W32).max(axis=0).astype(np.float64)
+    bound = 1e-5 * row_bound.mean() * 2 + 1e-6 * np.abs(lse).mean()
+    assert abs(loss - want) <= bound, (loss, want, bound)
     assert 0.0 < loss < 2 * np.log(V)

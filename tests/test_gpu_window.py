@@ -248,3 +248,52 @@ def test_window_flat_layers_copy_as_runs_bitwise():
             if t[4] is not None:
                 assert torch.equal(t[4].view(torch.int16), r[4].cpu().view(torch.int16))
     win.close()
+
+
+def test_window_with_device_resident_states_moves_only_grads_and_weights():
+    # fp32 master, m and v live in HBM; gradients come from and bf16 weights go
+    # back to pinned host memory; the slots hold only grad and weight buffers
+    sizes = [4099, 17, 65536, 3]
+    layers = []
+    for l in range(3):
+        L = _host_layer(sizes, 90 + l)
+        layers.append([[t[0], t[1].to(DEV), t[2].to(DEV), t[3].to(DEV), t[4]] for t in L])
+    ref_in = [[[x.clone() if x is not None else None for x in t] for t in L] for L in layers]
+    torch.cuda.synchronize()          # the clones are taken before the window's streams touch the states
+    order = [0, 1, 2, 2, 0, 1, 1]
+    bufs = [[(torch.empty(c, dtype=torch.bfloat16, device=DEV), torch.empty(c, dtype=torch.bfloat16, device=DEV))
+             for c in sizes] for _ in range(2)]          # kept alive: the window holds raw addresses
+    slots = [[native.make_tensor(g, None, None, None, w, numel=g.numel()) for g, w in sb] for sb in bufs]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = native.sf_window_create(slots, *streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L] for L in layers])
+    steps = (ctypes.c_int64 * 3)()
+    native.sf_slide_window_step(win, hl, order, native.hparams(**HP), steps)
+    win.sync()
+    torch.cuda.synchronize()
+    ref, ref_steps = _resident_reference(ref_in, order)
+    assert list(steps) == ref_steps
+    for L, R in zip(layers, ref):
+        for t, r in zip(L, R):
+            for k in (1, 2, 3):
+                assert t[k].is_cuda
+                assert torch.equal(t[k].view(torch.int32), r[k].view(torch.int32))
+            assert not t[4].is_cuda
+            assert torch.equal(t[4].view(torch.int16), r[4].cpu().view(torch.int16))
+    win.close()
+    del bufs
+
+
+def test_window_rejects_host_array_without_slot_buffer():
+    sizes = [1024]
+    L = _host_layer(sizes, 95)                       # master in pinned host memory
+    g, w = torch.empty(1024, dtype=torch.bfloat16, device=DEV), torch.empty(1024, dtype=torch.bfloat16, device=DEV)
+    slots = [[native.make_tensor(g, None, None, None, w, numel=1024)]]
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    win = native.sf_window_create(slots, *streams)
+    hl = native.host_layers([[native.make_tensor(*t) for t in L]])
+    steps = (ctypes.c_int64 * 1)()
+    with pytest.raises(native.SfError, match="slot has no buffer"):
+        native.sf_slide_window_step(win, hl, [0], native.hparams(**HP), steps)
+    assert list(steps) == [0]
+    win.close()

@@ -77,3 +77,22 @@ def test_gradient_rows_sum_to_zero_and_ignored_rows_are_zero():
     assert res["n"] == 6
     assert np.all(np.abs(res["dH"]) <= res["dH_abs"] * (1 + 1e-12))
     assert np.all(np.abs(res["dW"]) <= res["dW_abs"] * (1 + 1e-12))
+
+
+@pytest.mark.parametrize("N,D,V,chunk,ignore", [(7, 5, 33, 8, 2), (16, 4, 100, 100, 0), (3, 6, 17, 5, 3)])
+def test_chunked_lse_and_sampled_rows_match_the_whole_row_oracle(N, D, V, chunk, ignore):
+    # the sampled form the full-size checks use: the per-token log-sum-exp
+    # over vocabulary chunks, then dH rows and dW rows from it, against the
+    # oracle that holds every logit (ragged last chunk, unlabelled tokens)
+    from oracle.lce import lce_rows, token_lse
+    H, W, y = _case(N, D, V, 100 + N + V, ignore)
+    full = lce(H, W, y)
+    lse = token_lse(H, W, chunk=chunk)
+    assert np.allclose(lse, full["lse"], rtol=1e-13, atol=1e-13)
+    trows = [0, N - 1, N // 2]
+    vrows = [0, V - 1, V // 3, int(y[y != -100][0]) if (y != -100).any() else 1]
+    part = lce_rows(H, W, y, lse, trows, vrows)
+    assert np.allclose(part["dH"], full["dH"][trows], rtol=1e-11, atol=1e-14)
+    assert np.allclose(part["dH_abs"], full["dH_abs"][trows], rtol=1e-11, atol=1e-14)
+    assert np.allclose(part["dW"], full["dW"][vrows], rtol=1e-11, atol=1e-14)
+    assert np.allclose(part["dW_abs"], full["dW_abs"][vrows], rtol=1e-11, atol=1e-14)
