@@ -792,9 +792,57 @@ def run_lsp(args, matrices=None):
         lw.sync()
         host_ms = (time.perf_counter() - t0) / reps * 1e3
         lw.close()
-        del slots, items
+        del slots
     except Exception as ex:
         host_ms = f"host-moment window failed: {str(ex)[:120]}"
+        items = None
+    # LSP-Offload's own placement: S to the host, the compressed AdamW on the
+    # host cores, dS back (3 slots: the host round trip of one matrix
+    # overlaps the next ones' compress), then a timeline of one pass
+    host_upd = None
+    try:
+        if items is None:
+            raise RuntimeError("no layer list")
+        for it in items:
+            it["m_host"].zero_()
+            it["v_host"].zero_()
+        wsb_max = max(x[9] for x in mats)
+        hslots = [(torch.zeros(d, d, device="cuda"), torch.zeros(d, d, device="cuda"), torch.zeros(d, d).pin_memory(),
+                   torch.zeros(d, d).pin_memory(), torch.empty(wsb_max, dtype=torch.uint8, device="cuda"), wsb_max)
+                  for _ in range(3)]
+        wstreams = [torch.cuda.Stream() for _ in range(3)]
+        hw = native.lsp_window_create_host_update(hslots, d, *wstreams)
+        lay = native.lsp_layers(items)
+        lsteps = (ctypes.c_int64 * len(items))()
+        order = list(range(len(items)))
+        for _ in range(args.warmup):
+            native.lsp_slide_window_step(hw, lay, order, hp, lsteps)
+        hw.sync()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            native.lsp_slide_window_step(hw, lay, order, hp, lsteps)
+        hw.sync()
+        hu_ms = (time.perf_counter() - t0) / reps * 1e3
+        native.lsp_window_timeline_start(hw, len(items))
+        native.lsp_slide_window_step(hw, lay, order, hp, lsteps)
+        tl = native.lsp_window_timeline_read(hw, len(items))
+        hw.close()
+        wall = max(v[8] for v in tl) - min(v[0] for v in tl)
+        gpu = sum((v[1] - v[0]) + (v[8] - v[7]) for v in tl)
+        link = sum((v[3] - v[2]) + (v[6] - v[5]) for v in tl)
+        host = sum(v[4] - v[3] for v in tl)
+        host_upd = {"ms_per_chain_all7": hu_ms, "params_per_s": sum(m * n for (_, m, n, *_r) in mats) / (hu_ms / 1e3),
+                    "link_bytes_each_way_per_chain": 4 * d * d * len(items),
+                    "host_threads": min(8, len(os.sched_getaffinity(0))),
+                    "timeline_one_pass_ms": {"wall": wall, "gpu_compress_and_apply": gpu, "link_copies": link,
+                                             "host_updates": host,
+                                             "overlap_efficiency": max(gpu, link, host) / wall if wall > 0 else None},
+                    "timeline_visits": [[round(x, 4) for x in v] for v in tl],
+                    "timeline_points": "compress start, end; S to host start, end; host update end; dS to device "
+                                       "start, end; decompress-apply start, end (ms)"}
+        del hslots
+    except Exception as ex:
+        host_upd = {"error": f"host-update window failed: {str(ex)[:160]}"}
     # projector fit step (gradient descent on the stored values of P and Q
     # for the reconstruction error of G), once per matrix, after everything
     # above so that the changed values touch no other measurement
@@ -913,6 +961,7 @@ def run_lsp(args, matrices=None):
     out["gather_roof"].update(other_roofs)
     out["ms_per_chain_all7_graph_streams"] = graph_ms_streams
     out["ms_per_chain_all7_host_moments_window"] = host_ms
+    out["host_update_window"] = host_upd
     if isinstance(host_ms, float):
         out["params_updated_per_s_host_moments_window"] = n_params / (host_ms / 1e3)
     if isinstance(graph_ms_streams, float):

@@ -127,7 +127,8 @@ sf_status sf_adamw_layer_step(const sf_tensor* tensors, int n_tensors,
  * device kernels.  Identical arithmetic to sf_adamw_layer_step (no
  * floating-point contraction, the same fused multiply-adds), so IEEE hosts
  * produce the same bits as the GPU for finite inputs.  n_threads <= 0 uses
- * every hardware thread.  Synchronous: returns when the update is done. */
+ * one thread per core this process may run on (its CPU affinity set).
+ * Synchronous: returns when the update is done. */
 sf_status sf_adamw_host_step(const sf_tensor* tensors, int n_tensors,
                              const sf_adamw_hparams* hp, int64_t step,
                              int n_threads);
@@ -459,9 +460,67 @@ sf_status lsp_slide_window_step(lsp_window w, const lsp_layer* layers,
                                 int n_layers, const int32_t* order, int n_order,
                                 const sf_adamw_hparams* hp, int64_t* steps);
 
+/* The same window with the compressed AdamW on the host cores, LSP-Offload's
+ * own placement of the update (method section: the CPU computes in the
+ * compressed space; abstract: layer-wise communication schedule).  For every
+ * entry l = order[u] (slot s = running visit count mod n_slots):
+ *   compute: lsp_compress(P, Q, G) -> slot S           (device)
+ *   d2h:     S -> slot S_host (pinned host)
+ *   host:    a host function ordered after that copy runs the compressed
+ *            AdamW (step = ++steps[l], no weight decay) on the host cores on
+ *            m_host, v_host of layer l in place, writing dS to slot dS_host
+ *   h2d:     dS_host -> slot dS                           (device)
+ *   compute: lsp_decompress_apply(P, Q, dS, W)
+ * The compress of the next n_slots - 1 visits is enqueued before a visit's
+ * decompress-apply, so a layer's host round trip overlaps the next layers'
+ * GPU work (n_slots >= 2 for any overlap).  Per layer the host link carries
+ * S down and dS up (d*d*4 bytes each way) and no moments.  The host
+ * arithmetic is the device kernel's (same operations, same order, no
+ * floating-point contraction), so results are bitwise those of
+ * lsp_adamw_compressed on device-resident moments.
+ *   n_threads: host threads of the update (<= 0: up to 8 of the cores this
+ *   process may run on); the window starts them here and stops them in
+ *   lsp_window_destroy.
+ * lsp_slide_window_step, lsp_window_sync and lsp_window_destroy take either
+ * kind of window.  The m_host / v_host of a layer and the host staging
+ * buffers must not be touched until lsp_window_sync has returned. */
+typedef struct {
+  float* S;        /* device fp32 [d][d] */
+  float* dS;       /* device fp32 [d][d] */
+  float* S_host;   /* pinned host fp32 [d][d]: S on its way to the host update */
+  float* dS_host;  /* pinned host fp32 [d][d]: dS on its way back */
+  void* ws;        /* device workspace (256-byte aligned) */
+  size_t ws_bytes;
+} lsp_host_slot;
+
+sf_status lsp_window_create_host_update(int n_slots, const lsp_host_slot* slots,
+                                        int32_t d, int n_threads,
+                                        void* h2d_stream, void* compute_stream,
+                                        void* d2h_stream, lsp_window* out);
+
+/* Measurement hook of a host-update window: a timeline of its visits.
+ * lsp_window_timeline_start waits for the window's work, then makes the
+ * next `capacity` visits (over any number of lsp_slide_window_step calls)
+ * record 9 timing events each; capacity 0 switches it off.
+ * lsp_window_timeline_read waits for the window's work and writes, for up
+ * to `capacity` recorded visits in visit order, 9 floats per visit into
+ * `ms` (host), milliseconds after the first visit's first point: compress
+ * start and end (compute stream), S-to-host copy start and end and host
+ * update end (d2h stream; the update starts when the copy ends), dS copy
+ * start and end (h2d stream), decompress-apply start and end (compute
+ * stream); *n_visits = the visits written.  Overlap shows as one visit's
+ * copies and host update lying inside other visits' compress and
+ * decompress-apply.  SF_ERR_INVALID for a device-update window, a NULL
+ * pointer or a capacity outside [0, 2^20]. */
+sf_status lsp_window_timeline_start(lsp_window w, int capacity);
+sf_status lsp_window_timeline_read(lsp_window w, float* ms, int capacity, int* n_visits);
+
 /* Bounded wait (as sf_window_sync) for everything the window enqueued. */
 sf_status lsp_window_sync(lsp_window w, int64_t timeout_ms);
 
+/* Waits (bounded) for the window's work, then frees its events and host
+ * threads.  If the wait runs out (SF_ERR_TIMEOUT) the window is kept, since
+ * work still in flight may use it; call lsp_window_destroy again later. */
 sf_status lsp_window_destroy(lsp_window w);
 
 /* ------------------------------------------------------------------------

@@ -5,6 +5,8 @@
 #include <mutex>
 #include <utility>
 
+#include <sched.h>
+
 #include <chrono>
 #include <cmath>
 #include <cstdlib>
@@ -55,6 +57,17 @@ bool on_current_device(const void* p) {
     return false;
   }
   return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+int usable_cores() {
+  cpu_set_t set;
+  CPU_ZERO(&set);
+  if (sched_getaffinity(0, sizeof set, &set) == 0) {
+    const int n = CPU_COUNT(&set);
+    if (n > 0) return n;
+  }
+  const unsigned h = std::thread::hardware_concurrency();
+  return h > 0 ? (int)h : 1;
 }
 
 int64_t default_timeout_ms() {

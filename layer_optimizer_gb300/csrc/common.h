@@ -133,6 +133,14 @@ sf_status tc_gemm(const void* A, bool a_mn, const void* B, bool b_mn, float* C, 
 sf_status make_adam_consts(const sf_adamw_hparams* hp, int64_t step, bool with_decay,
                            AdamConsts* out);
 
+// The compressed AdamW step on the host cores for elements [b, e) of fp32
+// S, m, v -> dS (host_adamw.cpp): bitwise the device kernel's results.
+void host_adamw_compressed(const float* S, float* m, float* v, float* dS, int64_t b, int64_t e,
+                           const AdamConsts& c);
+
+// Cores this process may run on (its CPU affinity set), at least 1.
+int usable_cores();
+
 }  // namespace sf
 
 #define SF_TRY(expr)                      \

@@ -61,6 +61,26 @@ void update_range(const sf_tensor& t, int64_t b, int64_t e, const sf::AdamConsts
 
 }  // namespace
 
+namespace sf {
+
+// The compressed AdamW step (adamw.cu, adamw_compressed_kernel) on elements
+// [b, e) of fp32 S, m, v -> dS on the host: the same operations in the same
+// order, so the same bits.
+void host_adamw_compressed(const float* S, float* m, float* v, float* dS, int64_t b, int64_t e,
+                           const AdamConsts& c) {
+  for (int64_t i = b; i < e; ++i) {
+    const float g = S[i];
+    const float mm = std::fmaf(c.beta1, m[i], c.one_minus_beta1 * g);
+    const float vv = std::fmaf(c.beta2, v[i], c.one_minus_beta2 * (g * g));
+    const float denom = std::fmaf(std::sqrt(vv), c.inv_sqrt_bc2, c.eps);
+    m[i] = mm;
+    v[i] = vv;
+    dS[i] = c.step_size * (mm / denom);
+  }
+}
+
+}  // namespace sf
+
 extern "C" {
 
 sf_status sf_adamw_host_step(const sf_tensor* tensors, int n_tensors, const sf_adamw_hparams* hp, int64_t step,
@@ -83,7 +103,7 @@ sf_status sf_adamw_host_step(const sf_tensor* tensors, int n_tensors, const sf_a
   }
   start[n_tensors] = total;
   if (total == 0) return SF_OK;
-  int nt = n_threads > 0 ? n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
+  int nt = n_threads > 0 ? n_threads : sf::usable_cores();
   nt = (int)std::min<int64_t>(nt, std::max<int64_t>(1, total / 65536));
 
   // thread k owns global elements [k*total/nt, (k+1)*total/nt)

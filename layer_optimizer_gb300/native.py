@@ -26,8 +26,10 @@ EXPORTS = [
     "sf_window_destroy", "sf_sync_status", "sf_last_error", "sf_version",
     "sf_test_fail_copy_after", "lsp_compress_noalloc",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
+    "lsp_window_create_host_update", "lsp_window_timeline_start", "lsp_window_timeline_read",
     "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
-    "sf_gemm_abt_bf16", "sf_gemm_bf16", "sf_bench_gather_rate", "sf_bench_tmem_rate", "sf_bench_l2_gather_rate", "lce_workspace_bytes", "lce_forward_backward",
+    "sf_gemm_abt_bf16", "sf_gemm_bf16", "sf_bench_gather_rate", "sf_bench_tmem_rate", "sf_bench_l2_gather_rate",
+    "lce_workspace_bytes", "lce_forward_backward",
     "sf_test_device_wait_runs_out",
 ]
 
@@ -50,6 +52,11 @@ class sf_tensor(ctypes.Structure):
 
 class sf_host_layer(ctypes.Structure):
     _fields_ = [("tensors", ctypes.POINTER(sf_tensor)), ("n_tensors", ctypes.c_int)]
+
+
+class lsp_host_slot(ctypes.Structure):
+    _fields_ = [("S", ctypes.c_void_p), ("dS", ctypes.c_void_p), ("S_host", ctypes.c_void_p),
+                ("dS_host", ctypes.c_void_p), ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
 
 
 class lsp_slot(ctypes.Structure):
@@ -94,6 +101,10 @@ _SIGS = {
     "sf_test_fail_copy_after": (None, [_I64]),
     "sf_adamw_host_step": (_ST, [ctypes.POINTER(sf_tensor), _INT, ctypes.POINTER(sf_adamw_hparams), _I64, _INT]),
     "lsp_window_create": (_ST, [_INT, ctypes.POINTER(lsp_slot), _I32, _P, _P, _P, ctypes.POINTER(_P)]),
+    "lsp_window_create_host_update": (_ST, [_INT, ctypes.POINTER(lsp_host_slot), _I32, _INT, _P, _P, _P,
+                                            ctypes.POINTER(_P)]),
+    "lsp_window_timeline_start": (_ST, [_P, _INT]),
+    "lsp_window_timeline_read": (_ST, [_P, _P, _INT, ctypes.POINTER(_INT)]),
     "lsp_slide_window_step": (_ST, [_P, ctypes.POINTER(lsp_layer), _INT, ctypes.POINTER(_I32), _INT,
                                     ctypes.POINTER(sf_adamw_hparams), ctypes.POINTER(_I64)]),
     "lsp_window_sync": (_ST, [_P, _I64]),
@@ -396,6 +407,30 @@ def lsp_window_create(slots, d, h2d_stream, compute_stream, d2h_stream):
     _check(load().lsp_window_create(len(slots), arr, d, _stream(h2d_stream), _stream(compute_stream),
                                     _stream(d2h_stream), ctypes.byref(h)))
     return LspWindow(h.value, arr)
+
+
+def lsp_window_create_host_update(slots, d, h2d_stream, compute_stream, d2h_stream, n_threads=0):
+    """``slots``: list of (S, dS, S_host, dS_host, ws, ws_bytes): device S, dS, ws; pinned host staging."""
+    arr = (lsp_host_slot * max(1, len(slots)))()
+    for i, (S, dS, Sh, dSh, ws, wsb) in enumerate(slots):
+        arr[i] = lsp_host_slot(_addr(S), _addr(dS), _addr(Sh), _addr(dSh), _addr(ws), wsb)
+    h = ctypes.c_void_p()
+    _check(load().lsp_window_create_host_update(len(slots), arr, d, int(n_threads), _stream(h2d_stream),
+                                                _stream(compute_stream), _stream(d2h_stream), ctypes.byref(h)))
+    return LspWindow(h.value, arr)
+
+
+def lsp_window_timeline_start(window, capacity):
+    _check(load().lsp_window_timeline_start(window.handle, int(capacity)))
+
+
+def lsp_window_timeline_read(window, capacity):
+    """Per recorded visit: [compress start, end, S copy start, end, host update end, dS copy start, end,
+    apply start, end] in ms after the first point."""
+    buf = (ctypes.c_float * max(1, capacity * 9))()
+    n = ctypes.c_int(0)
+    _check(load().lsp_window_timeline_read(window.handle, buf, int(capacity), ctypes.byref(n)))
+    return [list(buf[v * 9:(v + 1) * 9]) for v in range(n.value)]
 
 
 def lsp_layers(items):

@@ -1,7 +1,7 @@
 """Parity of the sparse-projector path with the fp64 oracle (GPU).
 
-Covers the bookkeeping (bit-exact), compress (TMA + cluster path and the
-generic path), the compressed AdamW step, and decompress-apply into fp32
+Covers the bookkeeping (bit-exact), compress (the TMA-staged gather, the
+plain-load path, a gradient in pinned host memory), the compressed AdamW step, and decompress-apply into fp32
 (with bf16 mirror) and bf16 weights, on shapes that span several tiles and
 ragged tails, plus the full LLaMA-7B projector workload.
 """
@@ -74,14 +74,30 @@ COMPRESS_CASES = [
     (33, 7, 16, 16, torch.bfloat16),      # generic, k = d
     (64, 128, 16, 2, torch.float32),
     (100, 128, 8, 3, torch.float32),      # ragged rows (window tail)
-    (1000, 1000, 64, 4, torch.float32),   # ragged rows and columns
+    (1000, 1000, 64, 4, torch.float32),   # ragged rows and columns, row splits
     (1024, 1024, 64, 4, torch.bfloat16),  # the one-linear-layer workload
-    (333, 264, 512, 8, torch.float32),    # d = 512: 4-CTA clusters with multicast
-    (260, 136, 200, 3, torch.bfloat16),   # d = 200: 2-CTA clusters, ragged a-range
-    (150, 96, 300, 5, torch.float32),     # d = 300: 3 a-ranges, no multicast
+    (333, 264, 512, 8, torch.float32),    # d = 512: 4 ranges of 128 outputs (32 warps each)
+    (260, 136, 200, 3, torch.bfloat16),   # d = 200: a full and a ragged output range
+    (150, 96, 300, 5, torch.float32),     # d = 300: 3 output ranges
     (129, 64, 12, 3, torch.float32),      # d not a multiple of 8
     (50, 40, 30, 3, torch.float32),       # d not a multiple of 4: stage 2 as the staged gather
 ]
+
+
+@pytest.mark.parametrize("m,n,d,k,dt", [(333, 264, 512, 8, torch.float32), (1024, 1024, 64, 4, torch.bfloat16)])
+def test_compress_reads_pinned_host_gradient_with_plain_loads(m, n, d, k, dt):
+    # tensor maps address only this device's memory: a G in pinned host
+    # memory takes the plain-load gather over the host link, same result
+    P, Pr = _make(m, d, k, 40 + m)
+    Q, Qr = _make(n, d, k, 50 + n)
+    G = synth.normal((m, n), 1e-3, 60 + m + n, dtype=dt).pin_memory()
+    S = torch.full((d, d), float("nan"), device=DEV)
+    ws, nb = _ws(m, n, d)
+    native.lsp_compress(P, Q, G, native.SF_FP32 if dt == torch.float32 else native.SF_BF16, m, n, S, ws, nb)
+    torch.cuda.synchronize()
+    native.sf_sync_status()
+    S_ref, S_abs = ol.compress(Pr, Qr, f64(G.float()))
+    check_close("S (pinned host G)", S, S_ref, S_abs, TOL_LSP)
 
 
 @pytest.mark.parametrize("m,n,d,k,dt", COMPRESS_CASES)
