@@ -735,6 +735,89 @@ __global__ void __launch_bounds__(32 * kVWarps) k_v(const float* __restrict__ dS
   }
 }
 
+// dst[c][a] = src[a][c] for a d x d fp32 matrix, 32 x 32 tiles through
+// padded shared memory (both sides coalesced).
+__global__ void k_transpose_dd(const float* __restrict__ src, int d, float* __restrict__ dst) {
+  __shared__ float t[32][33];
+  griddep_launch_dependents();
+  griddep_wait();                // src is dS from the compressed step
+  const int c0 = blockIdx.x * 32, a0 = blockIdx.y * 32;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int a = a0 + r, c = c0 + threadIdx.x;
+    t[r][threadIdx.x] = (a < d && c < d) ? src[(int64_t)a * d + c] : 0.0f;
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int c = c0 + r, a = a0 + threadIdx.x;
+    if (c < d && a < d) dst[(int64_t)c * d + a] = t[threadIdx.x][r];
+  }
+}
+
+// V[a][j] = sum_l q_{j,l} dS[a][c_{j,l}] (k = 8) reading dS^T (dst[c][a])
+// straight from L1 / L2, with no staging: lanes along a (two rows a each, a
+// warp covers 64 consecutive a), so every entry is one 256-byte load of a
+// row segment of dS^T; a warp takes 8 columns j at a time (the entries are
+// warp-uniform 32-byte loads of Q's ELL rows, all 64 row loads of a group in
+// flight) and writes each a's 8 values as one 32-byte segment of V's row.
+// The sums run over l in order from zero, the same as k_v.
+constexpr int kVrWarps = 8, kVrGroupsPerWarp = 1;
+__global__ void __launch_bounds__(32 * kVrWarps) k_v_rows(const float* __restrict__ dSt, int d,
+                                                          const int32_t* __restrict__ qidx,
+                                                          const float* __restrict__ qval, int64_t n,
+                                                          float* __restrict__ V) {
+  __shared__ int2 ebuf_all[kVrWarps][kVGroup * 8];
+  griddep_launch_dependents();
+  griddep_wait();                // dS^T comes from the transpose
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int2* ebuf = ebuf_all[warp];
+  const uint32_t ebuf_a = smem_u32(ebuf);
+  const int a = blockIdx.y * 64 + 2 * lane;         // this lane's rows a, a + 1 (d % 64 == 0)
+  const int64_t n_groups = n / kVGroup;
+  const float* drow = dSt + a;
+  for (int64_t g = (int64_t)blockIdx.x * kVrWarps + warp; g < n_groups; g += (int64_t)gridDim.x * kVrWarps) {
+    const int64_t j0 = g * kVGroup;
+    // the group's 64 entries (8 columns x 8) through the warp's buffer: one
+    // coalesced 8-byte load of ids and of values per lane
+    const int2 ids = __ldg(reinterpret_cast<const int2*>(qidx + j0 * 8) + lane);
+    const float2 vals = __ldg(reinterpret_cast<const float2*>(qval + j0 * 8) + lane);
+    __syncwarp();
+    ebuf[2 * lane] = make_int2(ids.x, __float_as_int(vals.x));
+    ebuf[2 * lane + 1] = make_int2(ids.y, __float_as_int(vals.y));
+    __syncwarp();
+    float2 acc[kVGroup];
+#pragma unroll
+    for (int ub = 0; ub < kVGroup; ub += 2) {
+      // two columns' 16 row loads in flight at once
+      float2 x[2][8];
+      float q[2][8];
+#pragma unroll
+      for (int uu = 0; uu < 2; ++uu)
+#pragma unroll
+        for (int l = 0; l < 8; ++l) {
+          const int2 en = lds_i2(ebuf_a + 8u * (uint32_t)((ub + uu) * 8 + l));
+          q[uu][l] = __int_as_float(en.y);
+          x[uu][l] = __ldg(reinterpret_cast<const float2*>(drow + (int64_t)en.x * d));
+        }
+#pragma unroll
+      for (int uu = 0; uu < 2; ++uu) {
+        float2 sacc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int l = 0; l < 8; ++l) {
+          sacc.x = fmaf(q[uu][l], x[uu][l].x, sacc.x);
+          sacc.y = fmaf(q[uu][l], x[uu][l].y, sacc.y);
+        }
+        acc[ub + uu] = sacc;
+      }
+    }
+    float* v0r = V + (int64_t)a * n + j0;
+    float* v1r = v0r + n;
+    *reinterpret_cast<float4*>(v0r) = make_float4(acc[0].x, acc[1].x, acc[2].x, acc[3].x);
+    *reinterpret_cast<float4*>(v0r + 4) = make_float4(acc[4].x, acc[5].x, acc[6].x, acc[7].x);
+    *reinterpret_cast<float4*>(v1r) = make_float4(acc[0].y, acc[1].y, acc[2].y, acc[3].y);
+    *reinterpret_cast<float4*>(v1r + 4) = make_float4(acc[4].y, acc[5].y, acc[6].y, acc[7].y);
+  }
+}
+
 __global__ void k_v_generic(const float* __restrict__ dS, int d, const int32_t* __restrict__ qidx,
                             const float* __restrict__ qval, int k, int64_t n, float* __restrict__ V) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -1232,7 +1315,8 @@ CompressPlan plan_compress(int64_t m, int64_t n, int d) {
   return c;
 }
 
-size_t decompress_bytes(int64_t n, int d) { return align_up((size_t)d * n * 4, 256); }
+// V (d x n fp32), then dS^T (d x d fp32) for the row-gather form of V.
+size_t decompress_bytes(int64_t n, int d) { return align_up((size_t)d * n * 4, 256) + align_up((size_t)d * d * 4, 256); }
 
 constexpr size_t kMaxGatherSmem = 220 * 1024;
 
@@ -1614,7 +1698,20 @@ sf_status lsp_decompress_apply(lsp_projector P, lsp_projector Q, const float* dS
     const int64_t gy = std::max<int64_t>(1, std::min<int64_t>(n_groups, nsm / n_ab));
     const int64_t cols_per_cta = ceil_div<int64_t>(n_groups, gy) * sf::kVGroup;
     const int64_t gy_used = ceil_div<int64_t>(n, cols_per_cta);
-    if (Q->k <= sf::kVMaxK) {
+    float* dSt = reinterpret_cast<float*>(static_cast<char*>(ws) + sf::align_up((size_t)d * n * 4, 256));
+    const bool rows_form = Q->k == 8 && d % 64 == 0 && n % sf::kVGroup == 0 &&
+                           (reinterpret_cast<uintptr_t>(V) % 16) == 0;
+    if (rows_form) {
+      // dS^T once (1 MB at d = 512), then V by row gathers of it
+      SF_CUDA_TRY(sf::launch_pdl(sf::k_transpose_dd, dim3((unsigned)ceil_div(d, 32), (unsigned)ceil_div(d, 32)),
+                                 dim3(32, 8), 0, s, dS, d, dSt),
+                  "launch k_transpose_dd");
+      const int64_t n_groups = n / sf::kVGroup;
+      const int64_t gx = std::max<int64_t>(1, ceil_div<int64_t>(n_groups, (int64_t)sf::kVrWarps * sf::kVrGroupsPerWarp));
+      SF_CUDA_TRY(sf::launch_pdl(sf::k_v_rows, dim3((unsigned)gx, (unsigned)(d / 64)), dim3(32 * sf::kVrWarps), 0, s,
+                                 dSt, d, Q->ell_idx, Q->ell_val, n, V),
+                  "launch k_v_rows");
+    } else if (Q->k <= sf::kVMaxK) {
       const size_t smem_v = sf::v_smem_bytes(d);
       SF_TRY(sf::allow_dynamic_smem(reinterpret_cast<const void*>(&sf::k_v), sf::v_smem_bytes(sf::kMaxFastD)));
       SF_CUDA_TRY(sf::launch_pdl(sf::k_v, dim3((unsigned)n_ab, (unsigned)gy_used), dim3(32 * sf::kVWarps), smem_v, s,

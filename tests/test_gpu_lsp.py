@@ -173,6 +173,8 @@ DECOMPRESS_CASES = [
     (1, 1, 1, 1), (7, 33, 8, 2), (64, 128, 16, 2), (100, 130, 8, 3), (1000, 1000, 64, 4),
     (333, 264, 512, 8), (129, 63, 12, 3), (40, 50, 600, 4),   # d > 512: generic path
     (64, 96, 64, 16), (100, 72, 40, 12),                       # k > 8: generic V, fast apply
+    (96, 520, 64, 8), (200, 136, 128, 8),                      # V as row gathers of dS^T (k = 8, d % 64 = 0)
+    (100, 132, 64, 8),                                         # k = 8 but n % 8 != 0: V from the staged block
 ]
 
 
