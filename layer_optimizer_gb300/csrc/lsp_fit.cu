@@ -8,6 +8,7 @@
 
 #include "common.h"
 #include "lsp_internal.cuh"
+#include "ptx.cuh"
 
 using sf::ceil_div;
 using sf::fail;
@@ -225,94 +226,169 @@ __global__ void __launch_bounds__(256) k_gemm_dd(const __grid_constant__ DdBatch
     }
 }
 
-// The same products when d is a multiple of 64: a TM x 64 output tile per
-// block (TM = 32: twice the blocks of 64 x 64 tiles, so the d x d products
-// of the fit step spread over all SMs), 4 x 4 outputs per thread.  The
-// k-slab of 32 of op(A) and op(B) is staged k-major in shared memory from
-// 16-byte global loads (the next slab's loads in flight while the current
-// one is used), and each thread reads its 4 rows and 4 columns with one
-// 16-byte load each per k.  Same order of the sums as k_gemm_dd.
-template <int TM>
-__global__ void __launch_bounds__(TM * 4) k_gemm_dd64(const __grid_constant__ DdBatch bt) {
-  constexpr int NT = TM * 4;             // (TM / 4) x 16 threads
-  constexpr int RA = TM * 8 / NT;        // A slab: TM x 32 floats = TM * 8 float4
-  constexpr int RB = 512 / NT;           // B slab: 64 x 32 floats = 512 float4
+// The same products when d is a multiple of 64: a 64 x 64 output tile per
+// block of 64 threads, 8 x 8 outputs per thread accumulated as packed fp32
+// pairs (fma.rn.f32x2: the same bits as fmaf).  Thread (ty, tx) owns rows
+// 4 ty + {0..3} and 32 + 4 ty + {0..3} and the same columns with tx, so each
+// 16-byte shared load of a k-row of op(A) or op(B) by a warp falls in one
+// wavefront.  The k-slab of 32 is staged k-major from 16-byte global loads
+// (the next slab's loads in flight while the current one is used); an
+// operand stored along k (plain A, transposed B) is loaded one row per
+// thread and written transposed with scalar stores that hit 32 distinct
+// banks.
+//
+// SPLIT > 1 (d a multiple of 32 SPLIT): the sum over l is cut into SPLIT
+// equal parts, one per CTA of a cluster of SPLIT along x, so a d x d product
+// runs SPLIT times the blocks.  Each CTA sums its part in order, parks its
+// 64 x 64 partial tile in shared memory, and after a cluster barrier CTA r
+// adds its 64 / SPLIT rows of the tile over the SPLIT partials in rank
+// order, reading its peers' shared memory, then stores them.  With SPLIT = 1
+// every output sums l = 0 .. d-1 in order with one accumulator, as
+// k_gemm_dd does.
+template <int SPLIT>
+__global__ void __launch_bounds__(64) k_gemm_dd64(const __grid_constant__ DdBatch bt) {
+  static_assert(64 % SPLIT == 0, "the tile rows split evenly over the cluster");
   const DdJob J = bt.job[blockIdx.z];
   const int d = bt.d;
-  __shared__ __align__(16) float As[32][TM];
+  __shared__ __align__(16) float As[32][64];
   __shared__ __align__(16) float Bs[32][64];
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int i0 = blockIdx.y * TM, j0 = blockIdx.x * 64;
-  float4 ra[RA], rb[RB];
+  const int tid = threadIdx.x, tx = tid & 7, ty = tid >> 3;
+  const int i0 = blockIdx.y * 64, j0 = (blockIdx.x / SPLIT) * 64;
+  const int part = d / SPLIT, l0 = (int)(blockIdx.x % SPLIT) * part;
+  float4 ra[8], rb[8];
+  // stored along k: thread t reads row t of the slab (8 pieces of 4 k);
+  // stored along the output index: piece q = t + 64 h is k-row q / 16,
+  // outputs 4 (q % 16) .. + 3
   auto load = [&](int k0) {
 #pragma unroll
-    for (int h = 0; h < RA; ++h) {
-      const int q = tid + NT * h;
-      // op(A)[i][l]: plain A is read along l (8 float4 per row), a transposed one along i
-      ra[h] = J.ta ? *reinterpret_cast<const float4*>(J.A + (int64_t)(k0 + q / (TM / 4)) * d + i0 + 4 * (q % (TM / 4)))
-                   : *reinterpret_cast<const float4*>(J.A + (int64_t)(i0 + (q >> 3)) * d + k0 + 4 * (q & 7));
-    }
-#pragma unroll
-    for (int h = 0; h < RB; ++h) {
-      const int q = tid + NT * h;
-      rb[h] = J.tb ? *reinterpret_cast<const float4*>(J.B + (int64_t)(j0 + (q >> 3)) * d + k0 + 4 * (q & 7))
+    for (int h = 0; h < 8; ++h) {
+      const int q = tid + 64 * h;
+      ra[h] = J.ta ? *reinterpret_cast<const float4*>(J.A + (int64_t)(k0 + (q >> 4)) * d + i0 + 4 * (q & 15))
+                   : *reinterpret_cast<const float4*>(J.A + (int64_t)(i0 + tid) * d + k0 + 4 * h);
+      rb[h] = J.tb ? *reinterpret_cast<const float4*>(J.B + (int64_t)(j0 + tid) * d + k0 + 4 * h)
                    : *reinterpret_cast<const float4*>(J.B + (int64_t)(k0 + (q >> 4)) * d + j0 + 4 * (q & 15));
     }
   };
   auto store = [&]() {
 #pragma unroll
-    for (int h = 0; h < RA; ++h) {
-      const int q = tid + NT * h;
+    for (int h = 0; h < 8; ++h) {
+      const int q = tid + 64 * h;
       if (J.ta) {
-        *reinterpret_cast<float4*>(&As[q / (TM / 4)][4 * (q % (TM / 4))]) = ra[h];
+        *reinterpret_cast<float4*>(&As[q >> 4][4 * (q & 15)]) = ra[h];
       } else {
-        const int ii = q >> 3, kk = 4 * (q & 7);
-        As[kk][ii] = ra[h].x;
-        As[kk + 1][ii] = ra[h].y;
-        As[kk + 2][ii] = ra[h].z;
-        As[kk + 3][ii] = ra[h].w;
+        As[4 * h][tid] = ra[h].x;
+        As[4 * h + 1][tid] = ra[h].y;
+        As[4 * h + 2][tid] = ra[h].z;
+        As[4 * h + 3][tid] = ra[h].w;
       }
-    }
-#pragma unroll
-    for (int h = 0; h < RB; ++h) {
-      const int q = tid + NT * h;
       if (J.tb) {
-        const int jj = q >> 3, kk = 4 * (q & 7);
-        Bs[kk][jj] = rb[h].x;
-        Bs[kk + 1][jj] = rb[h].y;
-        Bs[kk + 2][jj] = rb[h].z;
-        Bs[kk + 3][jj] = rb[h].w;
+        Bs[4 * h][tid] = rb[h].x;
+        Bs[4 * h + 1][tid] = rb[h].y;
+        Bs[4 * h + 2][tid] = rb[h].z;
+        Bs[4 * h + 3][tid] = rb[h].w;
       } else {
         *reinterpret_cast<float4*>(&Bs[q >> 4][4 * (q & 15)]) = rb[h];
       }
     }
   };
-  float acc[4][4];
+  // acc[r][p]: row r (0-3: 4 ty + r, 4-7: 32 + 4 ty + r - 4), column pair p
+  // (0, 1: 4 tx + {0, 1}, {2, 3}; 2, 3: 32 + 4 tx + ...)
+  uint64_t acc[8][4];
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+  for (int r = 0; r < 8; ++r)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[r][c] = 0.0f;
-  load(0);
-  for (int k0 = 0; k0 < d; k0 += 32) {
+    for (int c = 0; c < 4; ++c) acc[r][c] = 0ull;
+  load(l0);
+  for (int k0 = l0; k0 < l0 + part; k0 += 32) {
     __syncthreads();
     store();
     __syncthreads();
-    if (k0 + 32 < d) load(k0 + 32);
+    if (k0 + 32 < l0 + part) load(k0 + 32);
 #pragma unroll
     for (int kk = 0; kk < 32; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[kk][4 * ty]);
-      const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][4 * tx]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+      const float4 a0 = *reinterpret_cast<const float4*>(&As[kk][4 * ty]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&As[kk][32 + 4 * ty]);
+      const ulonglong2 b0 = *reinterpret_cast<const ulonglong2*>(&Bs[kk][4 * tx]);
+      const ulonglong2 b1 = *reinterpret_cast<const ulonglong2*>(&Bs[kk][32 + 4 * tx]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(av[r], bv[c], acc[r][c]);
+      for (int r = 0; r < 8; ++r) {
+        const uint64_t aa = pack_f2(av[r], av[r]);
+        ffma2(acc[r][0], b0.x, aa);
+        ffma2(acc[r][1], b0.y, aa);
+        ffma2(acc[r][2], b1.x, aa);
+        ffma2(acc[r][3], b1.y, aa);
+      }
     }
   }
+  // this thread's outputs as rows of two float4 (columns 4 tx.., 32 + 4 tx..)
+  auto row_of = [&](int r) { return r < 4 ? 4 * ty + r : 32 + 4 * ty + r - 4; };
+  auto piece = [&](int r, int half) {
+    const float2 lo = unpack_f2(acc[r][2 * half]), hi = unpack_f2(acc[r][2 * half + 1]);
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+  };
+  if constexpr (SPLIT == 1) {
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
-    *reinterpret_cast<float4*>(J.C + (int64_t)(i0 + 4 * ty + r) * d + j0 + 4 * tx) =
-        make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+    for (int r = 0; r < 8; ++r) {
+      float* c = J.C + (int64_t)(i0 + row_of(r)) * d + j0;
+      *reinterpret_cast<float4*>(c + 4 * tx) = piece(r, 0);
+      *reinterpret_cast<float4*>(c + 32 + 4 * tx) = piece(r, 1);
+    }
+  } else {
+    __shared__ __align__(16) float Ps[64][64];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      *reinterpret_cast<float4*>(&Ps[row_of(r)][4 * tx]) = piece(r, 0);
+      *reinterpret_cast<float4*>(&Ps[row_of(r)][32 + 4 * tx]) = piece(r, 1);
+    }
+    cluster_sync();              // every partial tile of the cluster written
+    constexpr int kRows = 64 / SPLIT;
+    const uint32_t rank = cluster_ctarank();
+    for (int e = tid; e < kRows * 16; e += 64) {
+      const int row = (int)rank * kRows + e / 16, c4 = e % 16;
+      const uint32_t local = smem_u32(&Ps[row][4 * c4]);
+      float4 v = ld_dsmem_f4(mapa_shared(local, 0));
+#pragma unroll
+      for (int q = 1; q < SPLIT; ++q) {
+        const float4 w = ld_dsmem_f4(mapa_shared(local, (uint32_t)q));
+        v.x += w.x;
+        v.y += w.y;
+        v.z += w.z;
+        v.w += w.w;
+      }
+      *reinterpret_cast<float4*>(J.C + (int64_t)(i0 + row) * d + j0 + 4 * c4) = v;
+    }
+    cluster_sync();              // peers done reading this CTA's tile
+  }
+}
+
+constexpr int kDdSplit = 4;
+
+// The products of one batch (its first `jobs` entries) on stream s: split
+// over clusters when d is a multiple of 32 kDdSplit, one block per tile when
+// d is a multiple of 64, else the general kernel.
+sf_status launch_dd(const DdBatch& bt, int jobs, cudaStream_t s) {
+  const int d = bt.d;
+  const unsigned tiles = (unsigned)ceil_div(d, 64);
+  if (d % (32 * kDdSplit) == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles * kDdSplit, tiles, (unsigned)jobs);
+    cfg.blockDim = dim3(64);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kDdSplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gemm_dd64<kDdSplit>, bt), "launch k_gemm_dd64");
+  } else if (d % 64 == 0) {
+    k_gemm_dd64<1><<<dim3(tiles, tiles, (unsigned)jobs), 64, 0, s>>>(bt);
+  } else {
+    k_gemm_dd<<<dim3(tiles, tiles, (unsigned)jobs), 256, 0, s>>>(bt);
+  }
+  return check_launch("k_gemm_dd");
 }
 
 // H_P = 2 S - X (= S + C with C = S - X, X = A_P S A_Q), H_Q = H_P^T, and
@@ -410,6 +486,60 @@ __global__ void __launch_bounds__(256) k_fit_rowgrad(const float* __restrict__ X
       kt += __shfl_xor_sync(0xffffffffu, kt, o);
     }
     if (lane == 0) g[r * k + s] = -2.0f * (p - kt);
+  }
+}
+
+// The same gradients when d is a multiple of 128 and k <= 8, with the lanes
+// along d in 16-byte pieces: each lane reads 4 consecutive elements of X[r]
+// and of the k rows of H per step, all nine loads issued before the
+// multiply-adds, so a warp has d / 128 steps of loads in flight instead of
+// d / 32.  Each lane sums its pieces in order; the lanes combine in a fixed
+// butterfly.
+__global__ void __launch_bounds__(256) k_fit_rowgrad4(const float* __restrict__ X, int64_t rows, int d,
+                                                      const int32_t* __restrict__ idx, const float* __restrict__ val,
+                                                      int k, const float* __restrict__ H, const float* __restrict__ K,
+                                                      float* __restrict__ g) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  const float* x = X + r * d;
+  const int32_t* ir = idx + r * k;
+  const float* vr = val + r * k;
+  const float* h[8];
+  float p[8];
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    h[s] = H + (int64_t)(s < k ? ir[s] : ir[0]) * d;
+    p[s] = 0.0f;
+  }
+  for (int u = 4 * lane; u < d; u += 128) {
+    const float4 xu = *reinterpret_cast<const float4*>(x + u);
+    float4 hu[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      if (s < k) hu[s] = *reinterpret_cast<const float4*>(h[s] + u);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      if (s < k) {
+        p[s] = fmaf(xu.x, hu[s].x, p[s]);
+        p[s] = fmaf(xu.y, hu[s].y, p[s]);
+        p[s] = fmaf(xu.z, hu[s].z, p[s]);
+        p[s] = fmaf(xu.w, hu[s].w, p[s]);
+      }
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    if (s >= k) break;
+    float kt = 0.0f;
+    if (lane < k) kt = vr[lane] * K[(int64_t)ir[lane] * d + ir[s]];
+    float ps = p[s];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      kt += __shfl_xor_sync(0xffffffffu, kt, o);
+    }
+    if (lane == 0) g[r * k + s] = -2.0f * (ps - kt);
   }
 }
 
@@ -565,30 +695,32 @@ sf_status lsp_projector_fit_step(lsp_projector P, lsp_projector Q, const void* G
   sf::k_gram_sparse<<<gram_grid, 32 * sf::kGramWarps, gram_smem, s>>>(Q->col_ptr, Q->row_idx, Q->csc_val,
                                                                        Q->ell_idx, Q->ell_val, Q->k, d, AQ);
   SF_TRY(sf::check_launch("k_gram_sparse"));
-  const unsigned tiles = (unsigned)ceil_div(d, 64);
   sf::DdBatch b1{};
   b1.d = d;
   b1.job[0] = {S, AQ, W1, 0, 0};   // W1 = S A_Q
   b1.job[1] = {AP, S, W2, 0, 0};   // W2 = A_P S
-  const bool dd64 = d % 64 == 0;
-  if (dd64) sf::k_gemm_dd64<32><<<dim3(tiles, 2 * tiles, 2), 128, 0, s>>>(b1);
-  else sf::k_gemm_dd<<<dim3(tiles, tiles, 2), 256, 0, s>>>(b1);
+  SF_TRY(sf::launch_dd(b1, 2, s));
   sf::DdBatch b2{};
   b2.d = d;
   b2.job[0] = {W2, AQ, X, 0, 0};   // X = A_P S A_Q
   b2.job[1] = {W1, S, K1, 0, 1};   // K1 = S A_Q S^T
   b2.job[2] = {S, W2, K2, 1, 0};   // K2 = S^T A_P S
-  if (dd64) sf::k_gemm_dd64<32><<<dim3(tiles, 2 * tiles, 3), 128, 0, s>>>(b2);
-  else sf::k_gemm_dd<<<dim3(tiles, tiles, 3), 256, 0, s>>>(b2);
-  SF_TRY(sf::check_launch("k_gemm_dd"));
+  SF_TRY(sf::launch_dd(b2, 3, s));
   sf::k_fit_combine<<<sf::kCombineBlocks, 256, 0, s>>>(S, X, W1, W2, d, HP, HQ, part);
   SF_TRY(sf::check_launch("k_fit_combine"));
 
   // gradients at the stored positions, the loss, then the step
-  sf::k_fit_rowgrad<<<(unsigned)ceil_div<int64_t>(m, 8), 256, 0, s>>>(T, m, d, P->ell_idx, P->ell_val, P->k, HP, K1,
-                                                                      gP);
-  sf::k_fit_rowgrad<<<(unsigned)ceil_div<int64_t>(n, 8), 256, 0, s>>>(U, n, d, Q->ell_idx, Q->ell_val, Q->k, HQ, K2,
-                                                                      gQ);
+  auto rowgrad = [&](const float* X, int64_t rows, const lsp_projector_s* A, const float* H, const float* K,
+                     float* g) {
+    const unsigned grid = (unsigned)ceil_div<int64_t>(rows, 8);
+    if (d % 128 == 0 && A->k <= 8 && reinterpret_cast<uintptr_t>(X) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(H) % 16 == 0)
+      sf::k_fit_rowgrad4<<<grid, 256, 0, s>>>(X, rows, d, A->ell_idx, A->ell_val, A->k, H, K, g);
+    else
+      sf::k_fit_rowgrad<<<grid, 256, 0, s>>>(X, rows, d, A->ell_idx, A->ell_val, A->k, H, K, g);
+  };
+  rowgrad(T, m, P, HP, K1, gP);
+  rowgrad(U, n, Q, HQ, K2, gQ);
   SF_TRY(sf::check_launch("k_fit_rowgrad"));
   if (loss) {
     sf::k_fit_loss<<<1, 1024, 0, s>>>(g2, f.n_g2, part, sf::kCombineBlocks, loss);

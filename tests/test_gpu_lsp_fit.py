@@ -53,6 +53,8 @@ def _gradient(m, n, g_dtype, seed):
     (256, 384, 32, 2, native.SF_BF16),
     (130, 264, 96, 3, native.SF_FP32),      # rows not a multiple of 4: generic gather for G Q
     (1024, 1024, 64, 4, native.SF_BF16),    # the one-linear-layer projector shape
+    (640, 520, 128, 5, native.SF_FP32),     # d x d products split over clusters, one slab per part
+    (384, 1000, 256, 8, native.SF_BF16),    # rows of G^T Q in 16-byte pieces, k = 8
     (4096, 4096, 512, 8, native.SF_FP32),   # a LLaMA-7B attention matrix
 ])
 def test_fit_step_matches_oracle(m, n, d, k, g_dtype):
