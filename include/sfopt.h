@@ -201,7 +201,7 @@ sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G,
  * cudaFree, no allocating library routine.
  *  - Shapes whose lsp_workspace_bytes(m, n, d) exceeds the array are
  *    rejected with SF_ERR_UNSUPPORTED and a message (for example
- *    d = 512 covers n up to 16,384 columns).
+ *    d = 512 covers n up to 14,640 columns for any m).
  *  - Every call looks up the array's device address on the current device
  *    (cudaGetSymbolAddress), so the address stays right after a device
  *    reset; the first call on a device may also load the library's device

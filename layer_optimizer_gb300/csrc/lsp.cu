@@ -67,6 +67,7 @@ constexpr int kColsPerCta = 128;    // B columns per gather CTA (4 per lane)
 constexpr int kGatherOut = 4;       // outputs (columns of A) per gather warp
 constexpr int kMaxStages = 4;       // TMA ring depth of the gather kernel (at most)
 constexpr int kTargetCtas = 148;    // grid size aimed at (about one CTA per SM)
+constexpr int kWaveCtas = 152;      // gather CTAs of one wave on a GB300 (one per SM)
 constexpr int kApplyCols = 64;      // W columns per apply CTA (2 per lane)
 constexpr int kVRows = 64;          // a rows per V CTA (2 per lane)
 constexpr int kMaxFastD = 512;      // shared-memory tiles of k_v / k_apply hold d <= 512
@@ -279,8 +280,15 @@ struct GatherArgs {
   const int32_t* wptr;
   const int2* went;
   const int2* gdesc;
-  float* yt;               // [split][ncols][d]
+  float* yt;               // [ncols][d]: Y^T (or split 0's partial, see direct0)
+  float* part;             // partial outputs of row splits (see direct0)
   int64_t split_stride;    // elements between split outputs
+  int32_t direct0;         // 1: split 0 writes Y^T and split z >= 1 partial z - 1; 0: split z writes partial z
+  int32_t out_c0;          // first column a partial holds
+  int32_t main_tiles;      // > 0: 1D grid, whole tiles then the split tail (see k_gather_t)
+  int32_t cb_main;         // column blocks done whole (1D grid)
+  int32_t n_cb, n_ar;      // column blocks, output ranges (1D grid)
+  int32_t tail_wps;        // windows per split of the tail (1D grid)
   int32_t ncols;           // columns of B
   int32_t d, dp;           // columns of A (outputs a)
   int32_t n_win;           // windows of A / B rows
@@ -339,10 +347,31 @@ __global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CU
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  const int c0 = blockIdx.x * kColsPerCta;
-  const int a_cta = blockIdx.y * kGatherOut * nwarps;
-  const int w_begin = blockIdx.z * A.win_per_split;
-  const int w_end = min(A.n_win, w_begin + A.win_per_split);
+  // the block's tile: column block cb, output range ar, row split z.  On a
+  // 1D grid (A.main_tiles > 0) blocks [0, main_tiles) take the first cb_main
+  // column blocks whole (whole waves of the GPU) and the rest split the
+  // windows of the remaining column blocks, so the last wave is not left
+  // with a few whole tiles.
+  int cb = blockIdx.x, ar = blockIdx.y, z = blockIdx.z, wps = A.win_per_split;
+  if (A.main_tiles > 0) {
+    const int b = blockIdx.x;
+    if (b < A.main_tiles) {
+      cb = b % A.cb_main;
+      ar = b / A.cb_main;
+      z = 0;
+      wps = A.n_win;
+    } else {
+      const int t = b - A.main_tiles, tail_cbs = A.n_cb - A.cb_main;
+      cb = A.cb_main + t % tail_cbs;
+      ar = (t / tail_cbs) % A.n_ar;
+      z = t / (tail_cbs * A.n_ar);
+      wps = A.tail_wps;
+    }
+  }
+  const int c0 = cb * kColsPerCta;
+  const int a_cta = ar * kGatherOut * nwarps;
+  const int w_begin = z * wps;
+  const int w_end = min(A.n_win, w_begin + wps);
   const int nw = max(0, w_end - w_begin);
   const bool producer = warp == nwarps - 1 && lane == 0;
 
@@ -361,7 +390,7 @@ __global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CU
 
   // one stage = the B tile of a window, this CTA's slice of the prefix
   // table and its entry slice
-  const int2* gd_row = A.gdesc + (int64_t)blockIdx.y * A.n_win;
+  const int2* gd_row = A.gdesc + (int64_t)ar * A.n_win;
   auto issue = [&](int it) {
     const int s = it % S;
     const int w = w_begin + it;
@@ -473,13 +502,15 @@ __global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CU
       res[sl][2] = p23.x;
       res[sl][3] = p23.y;
     }
-    float* out = A.yt + (int64_t)blockIdx.z * A.split_stride;
+    const bool to_yt = z == 0 && A.direct0;
+    float* out = to_yt ? A.yt : A.part + (int64_t)(z - A.direct0) * A.split_stride;
+    const int oc0 = to_yt ? 0 : A.out_c0;
     const bool vec = A.vec_out && (a0 + kGatherOut <= A.d);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int col = c0 + 4 * lane + j;
       if (col >= A.ncols) continue;
-      float* o = out + (int64_t)col * A.d + a0;
+      float* o = out + (int64_t)(col - oc0) * A.d + a0;
       if (vec) {
         *reinterpret_cast<float4*>(o) = make_float4(res[0][j], res[1][j], res[2][j], res[3][j]);
       } else {
@@ -601,6 +632,19 @@ __global__ void k_reduce_splits(const float* __restrict__ part, int splits, int6
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
     float s = 0.0f;
     for (int k = 0; k < splits; ++k) s += part[k * stride + e];
+    out[e] = s;
+  }
+}
+
+// out[e] = out[e] + part[0][e] + part[1][e] + ..., added in that order (the
+// split tail of a 1D gather grid: split 0 wrote out itself).
+__global__ void k_add_splits(const float* __restrict__ part, int n_part, int64_t stride, int64_t n,
+                             float* __restrict__ out) {
+  griddep_launch_dependents();
+  griddep_wait();
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    float s = out[e];
+    for (int k = 0; k < n_part; ++k) s += part[k * stride + e];
     out[e] = s;
   }
 }
@@ -1292,6 +1336,25 @@ GatherPlan plan_gather(int64_t rows, int64_t ncols, int d) {
   int splits = (int)std::max<int64_t>(1, std::min<int64_t>(p.n_win, kTargetCtas / std::max<int64_t>(1, base)));
   p.win_per_split = (int)ceil_div<int64_t>(p.n_win, splits);
   p.splits = (int)ceil_div<int64_t>(p.n_win, p.win_per_split);
+  p.partial_bytes = p.splits > 1 ? align_up((size_t)p.splits * ncols * d * 4, 256) : 0;
+  // more tiles than one wave: whole waves of whole tiles, then the column
+  // blocks left over split by windows when that at least halves the last
+  // wave's length (a pure function of the sizes, like the rest)
+  p.cb_main = p.n_cb;
+  p.tail_splits = 1;
+  p.tail_wps = p.n_win;
+  if (p.splits == 1 && base > kWaveCtas && kWaveCtas % p.n_ar == 0) {
+    const int64_t cb_main = base / kWaveCtas * (kWaveCtas / p.n_ar);
+    const int64_t tail_tiles = (p.n_cb - cb_main) * p.n_ar;
+    const int64_t ts = tail_tiles > 0 ? std::min<int64_t>(p.n_win, kWaveCtas / tail_tiles) : 1;
+    if (ts >= 2) {
+      p.cb_main = (int)cb_main;
+      p.tail_wps = (int)ceil_div<int64_t>(p.n_win, ts);
+      p.tail_splits = (int)ceil_div<int64_t>(p.n_win, p.tail_wps);
+      const int64_t tail_cols = ncols - cb_main * kColsPerCta;
+      p.partial_bytes = align_up((size_t)(p.tail_splits - 1) * tail_cols * d * 4, 256);
+    }
+  }
   return p;
 }
 
@@ -1308,9 +1371,9 @@ CompressPlan plan_compress(int64_t m, int64_t n, int d) {
   c.off_rt = off;
   off = align_up(off + (size_t)n * d * 4, 256);
   c.off_rtp = off;
-  if (c.g1.splits > 1) off = align_up(off + (size_t)c.g1.splits * n * d * 4, 256);
+  off += c.g1.partial_bytes;
   c.off_sp = off;
-  if (!c.stage2_rows && c.g2.splits > 1) off = align_up(off + (size_t)c.g2.splits * d * d * 4, 256);
+  if (!c.stage2_rows) off += c.g2.partial_bytes;
   c.bytes = off;
   return c;
 }
@@ -1354,8 +1417,18 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   A.wptr = Aproj->wptr;
   A.went = Aproj->went;
   A.gdesc = Aproj->gdesc;
-  A.yt = p.splits > 1 ? yt_partial : yt_final;
-  A.split_stride = ncols * d;
+  const bool tail = p.tail_splits > 1;
+  const int64_t tail_c0 = (int64_t)p.cb_main * kColsPerCta;
+  A.yt = yt_final;
+  A.part = yt_partial;
+  A.direct0 = p.splits > 1 ? 0 : 1;
+  A.split_stride = tail ? (ncols - tail_c0) * d : ncols * d;
+  A.out_c0 = tail ? (int32_t)tail_c0 : 0;
+  A.main_tiles = tail ? p.cb_main * p.n_ar : 0;
+  A.cb_main = p.cb_main;
+  A.n_cb = p.n_cb;
+  A.n_ar = p.n_ar;
+  A.tail_wps = p.tail_wps;
   A.ncols = (int32_t)ncols;
   A.d = d;
   A.dp = Aproj->dp;
@@ -1384,7 +1457,8 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   const size_t smem = (size_t)A.stages * A.stage_stride + 2 * kMaxStages * sizeof(uint64_t) + kMaxStages * 4 + 8 + 1024;
   SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&k_gather_t<TB>), kMaxGatherSmem));
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.n_cb, (unsigned)p.n_ar, (unsigned)p.splits);
+  cfg.gridDim = tail ? dim3((unsigned)(A.main_tiles + (p.n_cb - p.cb_main) * p.n_ar * p.tail_splits))
+                     : dim3((unsigned)p.n_cb, (unsigned)p.n_ar, (unsigned)p.splits);
   cfg.blockDim = dim3(32 * p.warps);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -1394,6 +1468,14 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gather_t<TB>, map, A), "launch k_gather_t");
+  if (tail) {
+    const int64_t n_out = (ncols - tail_c0) * d;
+    const int blocks = (int)std::min<int64_t>(ceil_div<int64_t>(n_out, 256), (int64_t)sm_count() * 4);
+    SF_CUDA_TRY(launch_pdl(k_add_splits, dim3(blocks), dim3(256), 0, stream, yt_partial, p.tail_splits - 1,
+                           n_out, n_out, yt_final + tail_c0 * d),
+                "launch k_add_splits");
+    return SF_OK;
+  }
   if (p.splits > 1) {
     const int64_t n_out = ncols * d;
     const int blocks = (int)std::min<int64_t>(ceil_div<int64_t>(n_out, 256), (int64_t)sm_count() * 4);

@@ -600,7 +600,7 @@ FitPlan plan_fit(int64_t m, int64_t n, int d, size_t es, int kP, int kQ) {
   f.off_t = off;
   off = align_up(off + (size_t)m * d * 4, 256);
   f.off_tp = off;
-  if (f.gt.splits > 1) off = align_up(off + (size_t)f.gt.splits * m * d * 4, 256);
+  off += f.gt.partial_bytes;
   f.off_dd = off;
   off = align_up(off + (size_t)10 * d * d * 4, 256);
   f.off_gp = off;

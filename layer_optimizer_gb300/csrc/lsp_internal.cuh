@@ -42,6 +42,10 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Launch geometry of one gather (pure function of the sizes).
 struct GatherPlan {
   int warps, n_ar, n_cb, n_win, splits, win_per_split;
+  // tail_splits > 1: a 1D grid, column blocks [0, cb_main) whole, the rest
+  // split tail_splits ways over tail_wps windows each
+  int cb_main, tail_splits, tail_wps;
+  size_t partial_bytes;   // partials either form needs
 };
 
 // The two gathers of lsp_compress and the workspace they use.

@@ -81,6 +81,8 @@ COMPRESS_CASES = [
     (150, 96, 300, 5, torch.float32),     # d = 300: 3 output ranges
     (129, 64, 12, 3, torch.float32),      # d not a multiple of 8
     (50, 40, 30, 3, torch.float32),       # d not a multiple of 4: stage 2 as the staged gather
+    (300, 5000, 512, 8, torch.float32),   # 160 tiles: one whole wave, 2 column blocks split 3 ways (ragged last)
+    (700, 9800, 256, 4, torch.bfloat16),  # 154 tiles: one whole wave, 1 ragged column block split 6 ways
 ]
 
 
