@@ -564,8 +564,8 @@ sf_status sf_test_device_wait_runs_out(int64_t limit_cycles, void* stream);
  * ctas < 1, iters < 1 or a NULL sink. */
 sf_status sf_bench_gather_rate(int32_t ctas, int64_t iters, float* sink, void* stream);
 
-/* Measurement hook: the tensor-memory (TMEM) gather rate, the second
- * other on-chip roof for the projector kernels (LSP-Offload, method
+/* Measurement hook: the tensor-memory (TMEM) gather rate, another
+ * on-chip roof for the projector kernels (LSP-Offload, method
  * section: the compress and decompress are sparse products whose dense
  * operand is read at rows chosen by projector indices).  Launches `ctas`
  * CTAs of 512 threads, one per SM, each allocating all 512 TMEM columns for
