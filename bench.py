@@ -386,6 +386,29 @@ def kernels_per_call(fn, stream):
     return kernels
 
 
+def host_mem_available():
+    """Bytes of host memory the kernel reports as available (MemAvailable), or None."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
+def pinned_leg_fits(bytes_per_rank, local_ranks, available, headroom=1.3):
+    """Whether every rank on this node can pin `bytes_per_rank` of host memory at once.
+
+    `available` is MemAvailable read before any rank pinned anything; the
+    ranks of one node share it.  Unknown memory counts as not enough.
+    """
+    if available is None:
+        return False
+    return bytes_per_rank * local_ranks * headroom <= available
+
+
 def release_pinned():
     """Hand torch's cached pinned host blocks back to the system."""
     import torch
@@ -1219,7 +1242,10 @@ def opt13_sub(args, world):
            "clocks": res["clocks"], "l2": "inputs larger than L2 (1.41 GB per launch)"}
     out.update(resident_summary(res, args, world))
     out["unit"] = "params/s"
-    if not args.no_e2e:
+    if not args.no_e2e and world > 1:
+        out["e2e_window"] = {"skipped": "every array of the stack in pinned host memory (19.3 GB per rank): "
+                                        "run in the single-GPU line only"}
+    elif not args.no_e2e:
         e = run_e2e(args, world)
         wall = max_over_ranks(e["wall_s"], world)
         out["e2e_window"] = {
@@ -1244,7 +1270,14 @@ def main_ours(args, rank, world):
     native.load()
     llama = args.workload == "llama2-7b"
     groups = workload_groups(args.workload, args.layers)
-    res = run_resident(args, world, groups, keep=llama and not args.no_e2e)
+    # host memory before any rank pins anything: the legs that pin host
+    # buffers on every rank must fit all ranks of this node at once
+    avail = host_mem_available()
+    local_ranks = int(os.environ.get("LOCAL_WORLD_SIZE", world))
+    params = sum(n for g in groups for _, n in g)
+    e2e_pinned = params * 4 if llama else params * 16          # bf16 grads + weights; or every array
+    run_e2e_leg = not args.no_e2e and (world == 1 or pinned_leg_fits(e2e_pinned, local_ranks, avail))
+    res = run_resident(args, world, groups, keep=llama and run_e2e_leg)
     summ = resident_summary(res, args, world)
     if llama:
         metric = "params updated/s (fused AdamW, LLaMA-2-7B full step)"
@@ -1275,7 +1308,10 @@ def main_ours(args, rank, world):
         "roofline": summ["roofline"],
         "clocks": res["clocks"],
     }
-    if not args.no_e2e:
+    if not args.no_e2e and not run_e2e_leg:
+        line["e2e"] = {"skipped": f"needs {e2e_pinned / 1e9:.1f} GB of pinned host memory on each of "
+                                  f"{local_ranks} ranks; {(avail or 0) / 1e9:.1f} GB available on this node"}
+    elif not args.no_e2e:
         if llama:
             e = run_e2e_states_resident(args, world, groups, res.pop("layers"), res["steps_done"])
             wall = max_over_ranks(e["wall_s"], world)
@@ -1302,7 +1338,10 @@ def main_ours(args, rank, world):
             line["opt13"] = opt13_sub(args, world)
         except Exception as ex:
             line["opt13"] = {"error": str(ex)[:300]}
-        if not args.no_c5:
+        if not args.no_c5 and world > 1:
+            line["mistral_window"] = {"skipped": "the Mistral-Large window pins 88.6 GB of host memory per rank; "
+                                                 "it runs in the single-GPU line only"}
+        elif not args.no_c5:
             try:
                 line["mistral_window"] = mistral_summary(run_mistral_window(args, world), world)
             except Exception as ex:

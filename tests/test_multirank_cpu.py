@@ -65,3 +65,16 @@ def test_reference_arm_prints_once_under_two_ranks():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_pinned_legs_must_fit_every_rank_of_the_node():
+    sys.path.insert(0, ROOT)
+    import bench
+    gb = 10 ** 9
+    # the LLaMA-2-7B end-to-end leg pins 27 GB (bf16 grads and weights) per rank
+    assert bench.pinned_leg_fits(27 * gb, 1, 200 * gb)
+    assert bench.pinned_leg_fits(27 * gb, 4, 200 * gb) is True       # 140 GB with headroom
+    assert bench.pinned_leg_fits(27 * gb, 8, 200 * gb) is False      # 281 GB with headroom
+    assert bench.pinned_leg_fits(1, 1, None) is False                # unknown memory: not enough
+    avail = bench.host_mem_available()
+    assert avail is None or avail > 0
