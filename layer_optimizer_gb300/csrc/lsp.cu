@@ -193,36 +193,29 @@ __global__ void k_place(const int32_t* __restrict__ idx, const float* __restrict
 }
 
 // Column order by (nnz bucket, column id); bucket 0 = empty, else ceil(log2 nnz) + 1.
+// One block, a thread per column (d <= 1024): each column's key is
+// (bucket, id), unique, and its place in the order is the number of smaller
+// keys, counted over all columns from shared memory.
 __global__ void k_bucket_perm(const int32_t* __restrict__ col_ptr, int d, int32_t* __restrict__ perm) {
-  __shared__ int32_t wsum[32];
-  __shared__ int32_t run;
+  __shared__ int32_t key[1024];
   const int c = threadIdx.x;
-  int bucket = -1;
+  int my = INT32_MAX;
   if (c < d) {
     const int nnz = col_ptr[c + 1] - col_ptr[c];
-    bucket = 0;
+    int bucket = 0;
     if (nnz > 0) {
       int b = 0;
       while ((1 << b) < nnz) ++b;
       bucket = b + 1;
     }
+    my = bucket * 1024 + c;
   }
-  if (c == 0) run = 0;
+  key[c] = my;
   __syncthreads();
-  const int warp = c >> 5, lane = c & 31, nw = blockDim.x >> 5;
-  for (int b = 0; b <= 33; ++b) {
-    const bool f = bucket == b;
-    const unsigned bal = __ballot_sync(0xffffffffu, f);
-    if (lane == 0) wsum[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0;
-    for (int i = 0; i < warp; ++i) before += wsum[i];
-    int total = 0;
-    for (int i = 0; i < nw; ++i) total += wsum[i];
-    if (f) perm[run + before + __popc(bal & ((1u << lane) - 1u))] = c;
-    __syncthreads();
-    if (c == 0) run += total;
-    __syncthreads();
+  if (c < d) {
+    int rank = 0;
+    for (int i = 0; i < d; ++i) rank += key[i] < my ? 1 : 0;
+    perm[rank] = c;
   }
 }
 
