@@ -34,7 +34,7 @@ def _ws(m, n, d):
 # ---------------------------------------------------------------- bookkeeping
 
 @pytest.mark.parametrize("rows,d,k", [(1, 1, 1), (37, 8, 3), (1024, 64, 4), (4096, 512, 8), (11008, 512, 8),
-                                      (200, 12, 5), (130, 1024, 2)])
+                                      (200, 12, 5), (130, 1024, 2), (100, 128, 64)])
 def test_bookkeeping_bit_exact(rows, d, k):
     h, ref = _make(rows, d, k, rows + d)
     cp = torch.empty(d + 1, dtype=torch.int32, device=DEV)
@@ -83,6 +83,9 @@ COMPRESS_CASES = [
     (50, 40, 30, 3, torch.float32),       # d not a multiple of 4: stage 2 as the staged gather
     (300, 5000, 512, 8, torch.float32),   # 160 tiles: one whole wave, 2 column blocks split 3 ways (ragged last)
     (700, 9800, 256, 4, torch.bfloat16),  # 154 tiles: one whole wave, 1 ragged column block split 6 ways
+    (300, 264, 1024, 8, torch.float32),   # d at its maximum: 8 output ranges
+    (200, 160, 128, 64, torch.float32),   # k at its maximum: slices too large for the ring, plain loads
+    (150, 136, 64, 32, torch.bfloat16),   # k = 32
 ]
 
 
@@ -177,6 +180,9 @@ DECOMPRESS_CASES = [
     (64, 96, 64, 16), (100, 72, 40, 12),                       # k > 8: generic V, fast apply
     (96, 520, 64, 8), (200, 136, 128, 8),                      # V as row gathers of dS^T (k = 8, d % 64 = 0)
     (100, 132, 64, 8),                                         # k = 8 but n % 8 != 0: V from the staged block
+    (100, 72, 1024, 8),                                        # d at its maximum: generic path
+    (80, 96, 128, 64),                                         # k at its maximum: generic V and apply
+    (90, 70, 64, 32),                                          # k = 32: fast apply, one row per group
 ]
 
 
