@@ -194,6 +194,34 @@ def test_opt13_stack_sampled():
         del bufs
 
 
+@pytest.mark.slow
+def test_tensor_beyond_2_31_elements_sampled():
+    """One tensor of 2^31 + 4099 elements (34 GB of arrays), offset by 3 elements so it has a scalar head
+    and tail around the bulk-copied middle; checked on sampled elements, across the 2^31 boundary."""
+    n, o = 2 ** 31 + 4099, 3
+    g = synth.fill_normal_(torch.empty(n + o, dtype=torch.bfloat16, device=DEV), 1e-3, synth.sub_seed(41, 0))[o:]
+    p = synth.fill_normal_(torch.empty(n + o, device=DEV), 0.02, synth.sub_seed(41, 1))[o:]
+    m = torch.zeros(n + o, device=DEV)[o:]
+    v = torch.zeros(n + o, device=DEV)[o:]
+    w = torch.empty(n + o, dtype=torch.bfloat16, device=DEV)[o:]
+    rng = np.random.default_rng(41)
+    ix = torch.from_numpy(np.unique(np.concatenate([
+        rng.integers(0, n, 1 << 16), np.arange(64), np.arange(n - 4096, n),
+        np.arange(2 ** 31 - 64, 2 ** 31 + 64)]))).to(DEV)
+    th, g64 = f64(p[ix]), f64(g[ix].float())
+    native.sf_adamw_layer_step([native.make_tensor(g, p, m, v, w)], native.hparams(**HP), 1)
+    torch.cuda.synchronize()
+    st = oa.AdamWState(th)
+    oa.adamw_step(st, g64, 1, **HP)
+    check_close("master", p[ix], st.theta, st.theta_abs, TOL_STATE)
+    check_close("m", m[ix], st.m, st.m_abs, TOL_STATE)
+    check_close("v", v[ix], st.v, st.v_abs, TOL_STATE)
+    check_bf16("w", bits(w[ix]), st.theta)
+    del g, p, m, v, w
+    torch.cuda.empty_cache()
+    native.sf_sync_status()
+
+
 def test_checkpoint_resume_bitwise():
     """Three steps uninterrupted equal: one step, save to host, reload into new buffers, two steps."""
     n = 200003
