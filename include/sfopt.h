@@ -188,6 +188,30 @@ sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G,
                        sf_dtype g_dtype, int64_t m, int64_t n, float* S,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* The matrices of one layer compressed in one call: S_i = P_i^T G_i Q_i for
+ * i < count, the same results, bit for bit, as count lsp_compress calls
+ * (every tile is computed as in its own launch).  The first stages of all
+ * matrices whose G has one element type run in one launch, matrices with
+ * the most row windows first, then all second stages in one launch, so the
+ * GPU is filled across the layer's matrices instead of once per matrix (the
+ * pages apply the projector step to every weight matrix of a layer).
+ *   P, Q, G, g_dtype, m, n, S : arrays of count entries (host memory), each
+ *       entry as the same argument of lsp_compress; every projector has the
+ *       same d.
+ *   ws : device scratch, 256-byte aligned, at least
+ *       lsp_compress_layer_workspace_bytes(count, m, n, d) bytes (the
+ *       matrices' compress workspaces one after another); the caller owns it.
+ * Errors: SF_ERR_INVALID for count < 1, a NULL array or entry, rows that do
+ * not match m or n, projectors of different d, a small or misaligned
+ * workspace; otherwise as lsp_compress.  Asynchronous on `stream`. */
+size_t lsp_compress_layer_workspace_bytes(int count, const int64_t* m,
+                                          const int64_t* n, int32_t d);
+sf_status lsp_compress_layer(int count, const lsp_projector* P,
+                             const lsp_projector* Q, const void* const* G,
+                             const int32_t* g_dtype, const int64_t* m,
+                             const int64_t* n, float* const* S, void* ws,
+                             size_t ws_bytes, void* stream);
+
 /* lsp_compress for callers that cannot allocate device memory or hand the
  * library a workspace: callers under a framework whose caching allocator owns
  * the device memory pool, latency-critical loops where cudaMalloc's implicit

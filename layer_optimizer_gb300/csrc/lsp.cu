@@ -54,6 +54,7 @@
 #include <algorithm>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "common.h"
 #include "lsp_internal.cuh"
@@ -326,8 +327,44 @@ __device__ __forceinline__ ulonglong2 tile_load2(uint32_t addr) {
 // it, before it computes its own share of the next window, so all warps of
 // the CTA gather (twice the warps per SM of a dedicated producer layout,
 // which keeps the shared-memory loads' latency hidden).
+//
+// The tile of a CTA: column block cb, output range ar, row split z of wps
+// windows.  On a 1D grid (A.main_tiles > 0) blocks [0, main_tiles) take the
+// first cb_main column blocks whole (whole waves of the GPU) and the rest
+// split the windows of the remaining column blocks, so the last wave is not
+// left with a few whole tiles; otherwise block b of a flattened grid is
+// (b % n_cb, b / n_cb % n_ar, b / (n_cb n_ar)), the order in which the
+// hardware walks a 3D grid.
+struct GatherTile {
+  int cb, ar, z, wps;
+};
+
+__device__ __forceinline__ GatherTile tile_of_block(const GatherArgs& A, int b) {
+  GatherTile t;
+  if (A.main_tiles > 0) {
+    if (b < A.main_tiles) {
+      t.cb = b % A.cb_main;
+      t.ar = b / A.cb_main;
+      t.z = 0;
+      t.wps = A.n_win;
+    } else {
+      const int r = b - A.main_tiles, tail_cbs = A.n_cb - A.cb_main;
+      t.cb = A.cb_main + r % tail_cbs;
+      t.ar = (r / tail_cbs) % A.n_ar;
+      t.z = r / (tail_cbs * A.n_ar);
+      t.wps = A.tail_wps;
+    }
+  } else {
+    t.cb = b % A.n_cb;
+    t.ar = (b / A.n_cb) % A.n_ar;
+    t.z = b / (A.n_cb * A.n_ar);
+    t.wps = A.win_per_split;
+  }
+  return t;
+}
+
 template <typename TB>
-__global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CUtensorMap map, const GatherArgs A) {
+__device__ __forceinline__ void gather_tile(const CUtensorMap* map, const GatherArgs& A, const GatherTile tile) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // round up to 1024 with arithmetic on the __shared__ array itself, so the
   // compiler keeps the shared address space (plain LDS, not generic loads)
@@ -340,27 +377,7 @@ __global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CU
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
-  // the block's tile: column block cb, output range ar, row split z.  On a
-  // 1D grid (A.main_tiles > 0) blocks [0, main_tiles) take the first cb_main
-  // column blocks whole (whole waves of the GPU) and the rest split the
-  // windows of the remaining column blocks, so the last wave is not left
-  // with a few whole tiles.
-  int cb = blockIdx.x, ar = blockIdx.y, z = blockIdx.z, wps = A.win_per_split;
-  if (A.main_tiles > 0) {
-    const int b = blockIdx.x;
-    if (b < A.main_tiles) {
-      cb = b % A.cb_main;
-      ar = b / A.cb_main;
-      z = 0;
-      wps = A.n_win;
-    } else {
-      const int t = b - A.main_tiles, tail_cbs = A.n_cb - A.cb_main;
-      cb = A.cb_main + t % tail_cbs;
-      ar = (t / tail_cbs) % A.n_ar;
-      z = t / (tail_cbs * A.n_ar);
-      wps = A.tail_wps;
-    }
-  }
+  const int cb = tile.cb, ar = tile.ar, z = tile.z, wps = tile.wps;
   const int c0 = cb * kColsPerCta;
   const int a_cta = ar * kGatherOut * nwarps;
   const int w_begin = z * wps;
@@ -369,7 +386,7 @@ __global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CU
   const bool producer = warp == nwarps - 1 && lane == 0;
 
   if (threadIdx.x == 0) {
-    prefetch_tensormap(&map);
+    prefetch_tensormap(map);
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], nwarps);
@@ -391,7 +408,7 @@ __global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CU
     unsigned char* st = smem + (size_t)s * A.stage_stride;
     hdr[s] = gd.x;
     mbar_arrive_expect_tx(&full[s], (uint32_t)(A.stage_tx + A.wbytes + gd.y));
-    tma_load_2d(st, &map, &full[s], c0, w * kWinRows);
+    tma_load_2d(st, map, &full[s], c0, w * kWinRows);
     bulk_load(st + A.wsl_off, A.wptr + (int64_t)w * A.dp + a_cta, (uint32_t)A.wbytes, &full[s]);
     if (gd.y > 0) bulk_load(st + A.ent_off, A.went + gd.x, (uint32_t)gd.y, &full[s]);
   };
@@ -521,6 +538,34 @@ __global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CU
   }
 }
 
+template <typename TB>
+__global__ void __launch_bounds__(1024, 1) k_gather_t(const __grid_constant__ CUtensorMap map,
+                                                      const __grid_constant__ GatherArgs A) {
+  const GatherTile t = A.main_tiles > 0 ? tile_of_block(A, blockIdx.x)
+                                        : GatherTile{(int)blockIdx.x, (int)blockIdx.y, (int)blockIdx.z, A.win_per_split};
+  gather_tile<TB>(&map, A, t);
+}
+
+// Several gathers of the same block shape in one launch (the matrices of a
+// layer): block b belongs to the gather whose [block_begin, block_end) holds
+// it and runs that gather's tile of the same index, so every tile is
+// computed exactly as in its own launch.
+constexpr int kMaxLayerMats = 8;
+struct MultiGatherArgs {
+  CUtensorMap map[kMaxLayerMats];
+  GatherArgs a[kMaxLayerMats];
+  int32_t block_end[kMaxLayerMats];
+  int32_t count;
+};
+
+template <typename TB>
+__global__ void __launch_bounds__(1024, 1) k_gather_t_multi(const __grid_constant__ MultiGatherArgs M) {
+  int i = 0;
+  while (i + 1 < M.count && (int)blockIdx.x >= M.block_end[i]) ++i;
+  const int b = (int)blockIdx.x - (i > 0 ? M.block_end[i - 1] : 0);
+  gather_tile<TB>(&M.map[i], M.a[i], tile_of_block(M.a[i], b));
+}
+
 // Generic gather for shapes the TMA path cannot take: one thread per output.
 template <typename TB>
 __global__ void k_gather_generic(const TB* __restrict__ B, int64_t ldb, int64_t ncols, int d,
@@ -552,17 +597,28 @@ __global__ void k_gather_generic(const TB* __restrict__ B, int64_t ldb, int64_t 
 // yt is written as 32-byte row segments.  Needs B 16-byte aligned with
 // ldb and ncols multiples of 4 (every 16-byte load inside a row).
 constexpr int kRgWarps = 8, kRgCols = 128, kRgUnroll = 16;
-__global__ void __launch_bounds__(32 * kRgWarps, 2) k_rowgather(const float* __restrict__ B, int64_t ldb, int ncols,
-                                                             const int32_t* __restrict__ col_ptr,
-                                                             const int32_t* __restrict__ row_idx,
-                                                             const float* __restrict__ csc_val, int d,
-                                                             float* __restrict__ yt) {
+struct RowGatherArgs {
+  const float* B;
+  int64_t ldb;
+  int ncols;
+  const int32_t* col_ptr;
+  const int32_t* row_idx;
+  const float* csc_val;
+  int d;
+  float* yt;
+};
+
+__device__ __forceinline__ void rowgather_block(const float* __restrict__ B, int64_t ldb, int ncols,
+                                                const int32_t* __restrict__ col_ptr,
+                                                const int32_t* __restrict__ row_idx,
+                                                const float* __restrict__ csc_val, int d, float* __restrict__ yt,
+                                                int bx, int by) {
   __shared__ float tile[kRgWarps][kRgCols + 4];
   griddep_launch_dependents();
   griddep_wait();                // B is the previous kernel's output
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int a0 = blockIdx.x * kRgWarps, a = a0 + warp;
-  const int c0 = blockIdx.y * kRgCols, c = c0 + 4 * lane;
+  const int a0 = bx * kRgWarps, a = a0 + warp;
+  const int c0 = by * kRgCols, c = c0 + 4 * lane;
   const bool col_on = c < ncols;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (a < d) {
@@ -615,6 +671,32 @@ __global__ void __launch_bounds__(32 * kRgWarps, 2) k_rowgather(const float* __r
     const int cc = idx / kRgWarps, w = idx % kRgWarps;
     if (c0 + cc < ncols && a0 + w < d) yt[(int64_t)(c0 + cc) * d + a0 + w] = tile[w][cc];
   }
+}
+
+__global__ void __launch_bounds__(32 * kRgWarps, 2) k_rowgather(const float* __restrict__ B, int64_t ldb, int ncols,
+                                                             const int32_t* __restrict__ col_ptr,
+                                                             const int32_t* __restrict__ row_idx,
+                                                             const float* __restrict__ csc_val, int d,
+                                                             float* __restrict__ yt) {
+  rowgather_block(B, ldb, ncols, col_ptr, row_idx, csc_val, d, yt, blockIdx.x, blockIdx.y);
+}
+
+// The second stage of several matrices in one launch: block b belongs to
+// the matrix whose [block_begin, block_end) holds it and is that matrix's
+// block (b % gx, b / gx) of its own grid.
+struct MultiRowGatherArgs {
+  RowGatherArgs a[kMaxLayerMats];
+  int32_t gx[kMaxLayerMats];
+  int32_t block_end[kMaxLayerMats];
+  int32_t count;
+};
+
+__global__ void __launch_bounds__(32 * kRgWarps, 2) k_rowgather_multi(const __grid_constant__ MultiRowGatherArgs M) {
+  int i = 0;
+  while (i + 1 < M.count && (int)blockIdx.x >= M.block_end[i]) ++i;
+  const int b = (int)blockIdx.x - (i > 0 ? M.block_end[i - 1] : 0);
+  const RowGatherArgs& R = M.a[i];
+  rowgather_block(R.B, R.ldb, R.ncols, R.col_ptr, R.row_idx, R.csc_val, R.d, R.yt, b % M.gx[i], b / M.gx[i]);
 }
 
 // out[e] = sum over splits s = 0, 1, ... of part[s][e], in that order.
@@ -1392,21 +1474,31 @@ bool tma_ok(const void* B, int64_t ldb, size_t esize) {
          tensor_map_encoder() != nullptr && on_current_device(B);
 }
 
+// The staged gather's launch for one matrix: its arguments, tensor map,
+// dynamic shared memory and block count.  Returns false when the shape or
+// the operand's placement needs the plain-load kernel instead.
+struct GatherLaunch {
+  GatherArgs A;
+  CUtensorMap map;
+  size_t smem;
+  int blocks;           // on a 1D grid
+  dim3 grid;            // the same blocks as this launch's own grid
+  int block_threads;
+  bool tail;
+};
+
 template <typename TB>
-sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, int64_t ncols, const GatherPlan& p,
-                        float* yt_final, float* yt_partial, cudaStream_t stream) {
+sf_status prepare_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, int64_t ncols, const GatherPlan& p,
+                         float* yt_final, float* yt_partial, GatherLaunch* L, bool* staged) {
   const int64_t rows = Aproj->rows;
   const int d = Aproj->d;
   const size_t es = sizeof(TB);
-  if (!tma_ok(B, ldb, es) || Aproj->a_rng != kGatherOut * p.warps || gather_smem_estimate(Aproj, es) > kMaxGatherSmem) {
-    const int64_t total = ncols * d;
-    k_gather_generic<TB><<<(unsigned)ceil_div<int64_t>(total, 256), 256, 0, stream>>>(
-        B, ldb, ncols, d, Aproj->col_ptr, Aproj->row_idx, Aproj->csc_val, yt_final);
-    return check_launch("k_gather_generic");
-  }
+  *staged = tma_ok(B, ldb, es) && Aproj->a_rng == kGatherOut * p.warps &&
+            gather_smem_estimate(Aproj, es) <= kMaxGatherSmem;
+  if (!*staged) return SF_OK;
   const int align_elems = (int)(16 / es);
   const int cbx = (int)std::min<int64_t>(kColsPerCta, ceil_div<int64_t>(ncols, align_elems) * align_elems);
-  GatherArgs A;
+  GatherArgs& A = L->A;
   A.wptr = Aproj->wptr;
   A.went = Aproj->went;
   A.gdesc = Aproj->gdesc;
@@ -1436,47 +1528,121 @@ sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, 
   A.stages = (int)std::min<size_t>(kMaxStages, (kMaxGatherSmem - 2048) / A.stage_stride);
   A.vec_out = (d % 4 == 0) && (reinterpret_cast<uintptr_t>(A.yt) % 16 == 0) ? 1 : 0;
 
-  CUtensorMap map;
   cuuint64_t dims[2] = {(cuuint64_t)ncols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ldb * (int64_t)es)};
   cuuint32_t box[2] = {(cuuint32_t)cbx, (cuuint32_t)kWinRows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = tensor_map_encoder()(&map, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+  CUresult r = tensor_map_encoder()(&L->map, es == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                     2, const_cast<TB*>(B), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(SF_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  L->smem = (size_t)A.stages * A.stage_stride + 2 * kMaxStages * sizeof(uint64_t) + kMaxStages * 4 + 8 + 1024;
+  L->tail = tail;
+  L->blocks = tail ? A.main_tiles + (p.n_cb - p.cb_main) * p.n_ar * p.tail_splits : p.n_cb * p.n_ar * p.splits;
+  L->grid = tail ? dim3((unsigned)L->blocks) : dim3((unsigned)p.n_cb, (unsigned)p.n_ar, (unsigned)p.splits);
+  L->block_threads = 32 * p.warps;
+  return SF_OK;
+}
 
-  const size_t smem = (size_t)A.stages * A.stage_stride + 2 * kMaxStages * sizeof(uint64_t) + kMaxStages * 4 + 8 + 1024;
-  SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&k_gather_t<TB>), kMaxGatherSmem));
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = tail ? dim3((unsigned)(A.main_tiles + (p.n_cb - p.cb_main) * p.n_ar * p.tail_splits))
-                     : dim3((unsigned)p.n_cb, (unsigned)p.n_ar, (unsigned)p.splits);
-  cfg.blockDim = dim3(32 * p.warps);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gather_t<TB>, map, A), "launch k_gather_t");
-  if (tail) {
+// After the gather kernel: the split tail's partials added into Y^T, or the
+// row splits' partials reduced into it.
+sf_status finish_gather(const GatherPlan& p, int64_t ncols, int d, float* yt_final, float* yt_partial,
+                        cudaStream_t stream) {
+  if (p.tail_splits > 1) {
+    const int64_t tail_c0 = (int64_t)p.cb_main * kColsPerCta;
     const int64_t n_out = (ncols - tail_c0) * d;
     const int blocks = (int)std::min<int64_t>(ceil_div<int64_t>(n_out, 256), (int64_t)sm_count() * 4);
     SF_CUDA_TRY(launch_pdl(k_add_splits, dim3(blocks), dim3(256), 0, stream, yt_partial, p.tail_splits - 1,
                            n_out, n_out, yt_final + tail_c0 * d),
                 "launch k_add_splits");
-    return SF_OK;
-  }
-  if (p.splits > 1) {
+  } else if (p.splits > 1) {
     const int64_t n_out = ncols * d;
     const int blocks = (int)std::min<int64_t>(ceil_div<int64_t>(n_out, 256), (int64_t)sm_count() * 4);
     SF_CUDA_TRY(launch_pdl(k_reduce_splits, dim3(blocks), dim3(256), 0, stream, yt_partial, p.splits, n_out, n_out,
                            yt_final),
                 "launch k_reduce_splits");
-    return SF_OK;
   }
+  return SF_OK;
+}
+
+template <typename TB>
+sf_status launch_generic_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, int64_t ncols, float* yt_final,
+                                cudaStream_t stream) {
+  const int64_t total = ncols * Aproj->d;
+  k_gather_generic<TB><<<(unsigned)ceil_div<int64_t>(total, 256), 256, 0, stream>>>(
+      B, ldb, ncols, Aproj->d, Aproj->col_ptr, Aproj->row_idx, Aproj->csc_val, yt_final);
+  return check_launch("k_gather_generic");
+}
+
+cudaLaunchConfig_t pdl_config(dim3 grid, int threads, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <typename TB>
+sf_status launch_gather(const lsp_projector_s* Aproj, const TB* B, int64_t ldb, int64_t ncols, const GatherPlan& p,
+                        float* yt_final, float* yt_partial, cudaStream_t stream) {
+  GatherLaunch L;
+  bool staged = false;
+  SF_TRY(prepare_gather<TB>(Aproj, B, ldb, ncols, p, yt_final, yt_partial, &L, &staged));
+  if (!staged) return launch_generic_gather<TB>(Aproj, B, ldb, ncols, yt_final, stream);
+  SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&k_gather_t<TB>), kMaxGatherSmem));
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = pdl_config(L.grid, L.block_threads, L.smem, stream, attr);
+  SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gather_t<TB>, L.map, L.A), "launch k_gather_t");
+  return finish_gather(p, ncols, Aproj->d, yt_final, yt_partial, stream);
+}
+
+// The stage-1 gathers of several matrices of one element type and one block
+// shape in one launch, matrices with the longest tiles first (they set the
+// launch's length); each matrix's tiles, partials and sums exactly as in its
+// own launch.
+template <typename TB>
+sf_status launch_gather_multi(int count, const lsp_projector_s* const* Aproj, const TB* const* B, const int64_t* ldb,
+                              const int64_t* ncols, const GatherPlan* p, float* const* yt_final,
+                              float* const* yt_partial, cudaStream_t stream) {
+  std::vector<int> staged_ids;
+  std::vector<GatherLaunch> L(count);
+  for (int i = 0; i < count; ++i) {
+    bool staged = false;
+    SF_TRY(prepare_gather<TB>(Aproj[i], B[i], ldb[i], ncols[i], p[i], yt_final[i], yt_partial[i], &L[i], &staged));
+    if (staged) staged_ids.push_back(i);
+    else SF_TRY(launch_generic_gather<TB>(Aproj[i], B[i], ldb[i], ncols[i], yt_final[i], stream));
+  }
+  // longest tiles first; gathers whose block shape differs go alone
+  std::stable_sort(staged_ids.begin(), staged_ids.end(), [&](int a, int b) { return p[a].n_win > p[b].n_win; });
+  size_t at = 0;
+  while (at < staged_ids.size()) {
+    MultiGatherArgs M;
+    M.count = 0;
+    size_t smem = 0;
+    int blocks = 0;
+    const int threads = L[staged_ids[at]].block_threads;
+    while (at < staged_ids.size() && M.count < kMaxLayerMats && L[staged_ids[at]].block_threads == threads) {
+      const GatherLaunch& g = L[staged_ids[at]];
+      M.map[M.count] = g.map;
+      M.a[M.count] = g.A;
+      blocks += g.blocks;
+      M.block_end[M.count] = blocks;
+      smem = std::max(smem, g.smem);
+      ++M.count;
+      ++at;
+    }
+    SF_TRY(allow_dynamic_smem(reinterpret_cast<const void*>(&k_gather_t_multi<TB>), kMaxGatherSmem));
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), threads, smem, stream, attr);
+    SF_CUDA_TRY(cudaLaunchKernelEx(&cfg, k_gather_t_multi<TB>, M), "launch k_gather_t_multi");
+  }
+  for (int i : staged_ids) SF_TRY(finish_gather(p[i], ncols[i], Aproj[i]->d, yt_final[i], yt_partial[i], stream));
   return SF_OK;
 }
 
@@ -1491,6 +1657,40 @@ sf_status launch_stage2(const lsp_projector_s* Aproj, const float* B, int64_t ld
                          Aproj->row_idx, Aproj->csc_val, Aproj->d, yt_final),
               "launch k_rowgather");
   return SF_OK;
+}
+
+// The second stage of several matrices: one k_rowgather_multi launch per
+// kMaxLayerMats matrices whose Rᵀ rows are 16-byte aligned, the staged
+// gather for the others.
+sf_status launch_stage2_multi(int count, const lsp_projector_s* const* Aproj, const float* const* B, const int64_t* ldb,
+                              const int64_t* ncols, const GatherPlan* p, float* const* yt_final,
+                              float* const* yt_partial, cudaStream_t stream) {
+  MultiRowGatherArgs M;
+  M.count = 0;
+  int blocks = 0;
+  auto flush = [&]() -> sf_status {
+    if (M.count == 0) return SF_OK;
+    SF_CUDA_TRY(launch_pdl(k_rowgather_multi, dim3((unsigned)blocks), dim3(32 * kRgWarps), 0, stream, M),
+                "launch k_rowgather_multi");
+    M.count = 0;
+    blocks = 0;
+    return SF_OK;
+  };
+  for (int i = 0; i < count; ++i) {
+    if ((reinterpret_cast<uintptr_t>(B[i]) % 16) != 0 || ldb[i] % 4 != 0 || ncols[i] % 4 != 0 ||
+        ncols[i] > INT32_MAX) {
+      SF_TRY(launch_gather<float>(Aproj[i], B[i], ldb[i], ncols[i], p[i], yt_final[i], yt_partial[i], stream));
+      continue;
+    }
+    const int gx = ceil_div(Aproj[i]->d, kRgWarps), gy = (int)ceil_div<int64_t>(ncols[i], kRgCols);
+    M.a[M.count] = RowGatherArgs{B[i], ldb[i], (int)ncols[i], Aproj[i]->col_ptr, Aproj[i]->row_idx,
+                                 Aproj[i]->csc_val, Aproj[i]->d, yt_final[i]};
+    M.gx[M.count] = gx;
+    blocks += gx * gy;
+    M.block_end[M.count] = blocks;
+    if (++M.count == kMaxLayerMats) SF_TRY(flush());
+  }
+  return flush();
 }
 
 sf_status check_proj(const lsp_projector_s* p, const char* name) {
@@ -1683,6 +1883,87 @@ sf_status lsp_compress(lsp_projector P, lsp_projector Q, const void* G, sf_dtype
   else
     SF_TRY(sf::launch_gather<__nv_bfloat16>(P, static_cast<const __nv_bfloat16*>(G), n, n, cp.g1, rt, rtp, s));
   return sf::launch_stage2(Q, rt, d, d, cp.g2, S, sp, s);
+}
+
+size_t lsp_compress_layer_workspace_bytes(int count, const int64_t* m, const int64_t* n, int32_t d) {
+  if (count < 1 || !m || !n || d < 1) return 0;
+  size_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    if (m[i] < 1 || n[i] < 1) return 0;
+    total += sf::align_up(sf::plan_compress(m[i], n[i], d).bytes, 256);
+  }
+  return total;
+}
+
+sf_status lsp_compress_layer(int count, const lsp_projector* P, const lsp_projector* Q, const void* const* G,
+                             const int32_t* g_dtype, const int64_t* m, const int64_t* n, float* const* S, void* ws,
+                             size_t ws_bytes, void* stream_) {
+  sf::clear_error();
+  sf::NvtxRange nvtx_range("lsp_compress_layer");
+  if (count < 1 || !P || !Q || !G || !g_dtype || !m || !n || !S)
+    return fail(SF_ERR_INVALID, "need count >= 1 and non-NULL arrays");
+  int d = 0;
+  for (int i = 0; i < count; ++i) {
+    SF_TRY(sf::check_proj(P[i], "P[i]"));
+    SF_TRY(sf::check_proj(Q[i], "Q[i]"));
+    if (!G[i] || !S[i]) return fail(SF_ERR_INVALID, "matrix %d: G or S is NULL", i);
+    if (P[i]->rows != m[i] || Q[i]->rows != n[i])
+      return fail(SF_ERR_INVALID, "matrix %d: P has %lld rows, Q %lld: need m = %lld, n = %lld", i,
+                  (long long)P[i]->rows, (long long)Q[i]->rows, (long long)m[i], (long long)n[i]);
+    if (P[i]->d != Q[i]->d || (i > 0 && P[i]->d != d))
+      return fail(SF_ERR_INVALID, "matrix %d: every projector of the layer needs the same d", i);
+    d = P[i]->d;
+    if (g_dtype[i] != SF_BF16 && g_dtype[i] != SF_FP32)
+      return fail(SF_ERR_INVALID, "matrix %d: g_dtype must be SF_BF16 or SF_FP32", i);
+  }
+  const size_t need = lsp_compress_layer_workspace_bytes(count, m, n, d);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) % 256) != 0)
+    return fail(SF_ERR_INVALID, "workspace needs %zu bytes, 256-byte aligned (got %zu)", need, ws_bytes);
+  cudaStream_t s = sf::as_stream(stream_);
+  std::vector<sf::CompressPlan> cp(count);
+  std::vector<float*> rt(count), rtp(count), sp(count);
+  std::vector<int64_t> ld(count), dd(count, d);
+  char* w = static_cast<char*>(ws);
+  for (int i = 0; i < count; ++i) {
+    cp[i] = sf::plan_compress(m[i], n[i], d);
+    rt[i] = reinterpret_cast<float*>(w + cp[i].off_rt);
+    rtp[i] = reinterpret_cast<float*>(w + cp[i].off_rtp);
+    sp[i] = reinterpret_cast<float*>(w + cp[i].off_sp);
+    ld[i] = n[i];
+    w += sf::align_up(cp[i].bytes, 256);
+  }
+  // stage 1, one launch per element type of G
+  for (const int32_t dt : {(int32_t)SF_FP32, (int32_t)SF_BF16}) {
+    std::vector<const lsp_projector_s*> a;
+    std::vector<const void*> b;
+    std::vector<int64_t> ldb, nc;
+    std::vector<sf::GatherPlan> pl;
+    std::vector<float*> yf, yp;
+    for (int i = 0; i < count; ++i) {
+      if (g_dtype[i] != dt) continue;
+      a.push_back(P[i]);
+      b.push_back(G[i]);
+      ldb.push_back(n[i]);
+      nc.push_back(n[i]);
+      pl.push_back(cp[i].g1);
+      yf.push_back(rt[i]);
+      yp.push_back(rtp[i]);
+    }
+    if (a.empty()) continue;
+    if (dt == SF_FP32)
+      SF_TRY(sf::launch_gather_multi<float>((int)a.size(), a.data(), reinterpret_cast<const float* const*>(b.data()),
+                                            ldb.data(), nc.data(), pl.data(), yf.data(), yp.data(), s));
+    else
+      SF_TRY(sf::launch_gather_multi<__nv_bfloat16>((int)a.size(), a.data(),
+                                                    reinterpret_cast<const __nv_bfloat16* const*>(b.data()),
+                                                    ldb.data(), nc.data(), pl.data(), yf.data(), yp.data(), s));
+  }
+  // stage 2 for every matrix
+  std::vector<const lsp_projector_s*> q(Q, Q + count);
+  std::vector<const float*> rtc(rt.begin(), rt.end());
+  std::vector<sf::GatherPlan> p2(count);
+  for (int i = 0; i < count; ++i) p2[i] = cp[i].g2;
+  return sf::launch_stage2_multi(count, q.data(), rtc.data(), dd.data(), dd.data(), p2.data(), S, sp.data(), s);
 }
 
 }  // extern "C"

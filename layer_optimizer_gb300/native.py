@@ -24,7 +24,7 @@ EXPORTS = [
     "lsp_projector_destroy", "lsp_workspace_bytes", "lsp_compress", "lsp_adamw_compressed",
     "lsp_decompress_apply", "sf_window_create", "sf_slide_window_step", "sf_window_sync",
     "sf_window_destroy", "sf_sync_status", "sf_last_error", "sf_version",
-    "sf_test_fail_copy_after", "lsp_compress_noalloc",
+    "sf_test_fail_copy_after", "lsp_compress_noalloc", "lsp_compress_layer_workspace_bytes", "lsp_compress_layer",
     "lsp_window_create", "lsp_slide_window_step", "lsp_window_sync", "lsp_window_destroy",
     "lsp_window_create_host_update", "lsp_window_timeline_start", "lsp_window_timeline_read",
     "sf_adamw_host_step", "lsp_fit_workspace_bytes", "lsp_projector_fit_step", "lsp_projector_export_values",
@@ -88,6 +88,8 @@ _SIGS = {
     "lsp_workspace_bytes": (ctypes.c_size_t, [_I64, _I64, _I32]),
     "lsp_compress": (_ST, [_P, _P, _P, _INT, _I64, _I64, _P, _P, ctypes.c_size_t, _P]),
     "lsp_compress_noalloc": (_ST, [_P, _P, _P, _INT, _I64, _I64, _P, _P]),
+    "lsp_compress_layer_workspace_bytes": (ctypes.c_size_t, [_INT, _P, _P, ctypes.c_int32]),
+    "lsp_compress_layer": (_ST, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "lsp_adamw_compressed": (_ST, [_P, _P, _P, _P, _I64, ctypes.POINTER(sf_adamw_hparams), _I64, _P]),
     "lsp_decompress_apply": (_ST, [_P, _P, _P, _P, _INT, _P, _I64, _I64, _P, ctypes.c_size_t, _P]),
     "sf_window_create": (_ST, [_INT, ctypes.POINTER(ctypes.POINTER(sf_tensor)), _INT, _P, _P, _P, ctypes.POINTER(_P)]),
@@ -251,6 +253,22 @@ def lsp_workspace_bytes(m, n, d):
 def lsp_compress(P, Q, G, g_dtype, m, n, S, ws, ws_bytes, stream=None):
     _check(load().lsp_compress(P.handle, Q.handle, _addr(G), g_dtype, m, n, _addr(S), _addr(ws),
                                ws_bytes, _stream(stream)))
+
+
+def lsp_compress_layer_workspace_bytes(ms, ns, d):
+    c = len(ms)
+    return load().lsp_compress_layer_workspace_bytes(c, (ctypes.c_int64 * c)(*ms), (ctypes.c_int64 * c)(*ns), d)
+
+
+def lsp_compress_layer(Ps, Qs, Gs, g_dtypes, ms, ns, Ss, ws, ws_bytes, stream=None):
+    """One layer's matrices in one call: lists of projectors, gradients, dtypes, sizes and outputs."""
+    c = len(Ps)
+    _check(load().lsp_compress_layer(c, (ctypes.c_void_p * c)(*[p.handle for p in Ps]),
+                                     (ctypes.c_void_p * c)(*[q.handle for q in Qs]),
+                                     (ctypes.c_void_p * c)(*[_addr(g) for g in Gs]),
+                                     (ctypes.c_int32 * c)(*g_dtypes), (ctypes.c_int64 * c)(*ms),
+                                     (ctypes.c_int64 * c)(*ns), (ctypes.c_void_p * c)(*[_addr(x) for x in Ss]),
+                                     _addr(ws), ws_bytes, _stream(stream)))
 
 
 def lsp_compress_noalloc(P, Q, G, g_dtype, m, n, S, stream=None):
