@@ -332,9 +332,10 @@ __device__ __forceinline__ ulonglong2 tile_load2(uint32_t addr) {
 // windows.  On a 1D grid (A.main_tiles > 0) blocks [0, main_tiles) take the
 // first cb_main column blocks whole (whole waves of the GPU) and the rest
 // split the windows of the remaining column blocks, so the last wave is not
-// left with a few whole tiles; otherwise block b of a flattened grid is
-// (b % n_cb, b / n_cb % n_ar, b / (n_cb n_ar)), the order in which the
-// hardware walks a 3D grid.
+// left with a few whole tiles; otherwise the blocks walk (output range,
+// column block, split).  Either way the output range varies fastest, so the
+// CTAs that read the same windows of B are dispatched together and each
+// tile comes from DRAM once, whatever wave they fall in.
 struct GatherTile {
   int cb, ar, z, wps;
 };
@@ -343,21 +344,21 @@ __device__ __forceinline__ GatherTile tile_of_block(const GatherArgs& A, int b) 
   GatherTile t;
   if (A.main_tiles > 0) {
     if (b < A.main_tiles) {
-      t.cb = b % A.cb_main;
-      t.ar = b / A.cb_main;
+      t.ar = b % A.n_ar;
+      t.cb = b / A.n_ar;
       t.z = 0;
       t.wps = A.n_win;
     } else {
-      const int r = b - A.main_tiles, tail_cbs = A.n_cb - A.cb_main;
-      t.cb = A.cb_main + r % tail_cbs;
-      t.ar = (r / tail_cbs) % A.n_ar;
-      t.z = r / (tail_cbs * A.n_ar);
+      const int r = b - A.main_tiles, tail_splits = (A.n_win + A.tail_wps - 1) / A.tail_wps;
+      t.ar = r % A.n_ar;
+      t.z = (r / A.n_ar) % tail_splits;
+      t.cb = A.cb_main + r / (A.n_ar * tail_splits);
       t.wps = A.tail_wps;
     }
   } else {
-    t.cb = b % A.n_cb;
-    t.ar = (b / A.n_cb) % A.n_ar;
-    t.z = b / (A.n_cb * A.n_ar);
+    t.ar = b % A.n_ar;
+    t.cb = (b / A.n_ar) % A.n_cb;
+    t.z = b / (A.n_ar * A.n_cb);
     t.wps = A.win_per_split;
   }
   return t;
