@@ -28,7 +28,12 @@
 // window-major column list (entries of window w and column a, rows
 // ascending, with a prefix table), so a warp finds its (window, a) entries
 // with a few broadcast loads.  Row splits (for grid size) write partial
-// outputs that one reduction sums in split order.
+// outputs that one reduction sums in split order; grids past whole waves
+// split only the column blocks left over after the whole waves.  The CTAs
+// that read the same windows (one per output range) are dispatched next to
+// each other, so each tile comes from DRAM once.  A layer's matrices can go
+// through one launch per stage (k_gather_t_multi, k_rowgather_multi), every
+// tile computed as in its own launch.
 //
 // Measured on GB300 for one 4096 x 4096 fp32 G (stage 1, 134 M multiply-
 // adds): this kernel 46 us; k_rowgather reading G's rows straight from L2
@@ -40,8 +45,9 @@
 // would split every output's accumulators over the quarters.
 //
 // Decompress:
-//   V = dS Q^T (d x n)          k_v: dS^T block resident in shared memory,
-//                               Q rows as warp-uniform entries
+//   V = dS Q^T (d x n)          k_transpose_dd + k_v_rows: row gathers of
+//                               dS^T (k = 8); k_v: dS^T block resident in
+//                               shared memory, Q rows as warp-uniform entries
 //   W[i, :] -= sum_l P[i,a_l] V[a_l, :]   k_apply: a 64-column block of V
 //                               resident in shared memory, W read and
 //                               written once, coalesced.
