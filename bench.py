@@ -107,6 +107,9 @@ def dist_init(args):
     if world > 1:
         import torch.distributed as dist
         backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))   # this rank's GPU before its communicator
         dist.init_process_group(backend)
     return rank, world
 
